@@ -1,0 +1,311 @@
+"""Pins for the float64 oracle: checks against facts that do not come from the
+oracle itself (an independent complex-number formulation of RoPE, pure-Python
+brute force over tiny inputs, closed forms and invariants the pages fix).
+
+Each check takes the oracle module, so the mutation tests can run the same
+checks against an oracle with a planted mistake and see at least one fail.
+"""
+from __future__ import annotations
+
+import cmath
+import math
+
+import numpy as np
+
+# --------------------------------------------------------------------------
+# Independent pure-Python formulations (no numpy, no oracle code)
+# --------------------------------------------------------------------------
+
+
+def bf_rope(x, pos, theta):
+    """RoPE as complex multiplication: z_i = x_i + i x_{i+d/2} times
+    exp(i * pos * theta^(-2i/d)) (RoFormer's complex form, rotate-half pairing)."""
+    d = len(x)
+    h = d // 2
+    out = [0.0] * d
+    for i in range(h):
+        z = complex(x[i], x[i + h]) * cmath.exp(1j * pos * theta ** (-2.0 * i / d))
+        out[i], out[i + h] = z.real, z.imag
+    return out
+
+
+def bf_member(mode, j, L, W, n_sink):
+    """Which segment key j belongs to, by the plain definitions: None, 'loc' or
+    'far'."""
+    if not 0 <= j < L:
+        return None
+    if mode in ("full", "sharp"):
+        return "loc"
+    if mode == "window":
+        return "loc" if (j < n_sink or j >= L - W) else None
+    return "loc" if j >= L - W else "far"
+
+
+def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
+                  beta=0.0, n_ref=4096, theta=1e4):
+    """One query row by brute force: per-key loops, math.exp, Python floats."""
+    d = len(q)
+    c = 1.0 / math.sqrt(d)
+    qr = bf_rope(q, p, theta)
+    segs = {"loc": [], "far": []}
+    for j in range(L):
+        m = bf_member(mode, j, L, W, n_sink)
+        if m is not None:
+            segs[m].append(j)
+    gamma = 1.0
+    if mode == "sharp" and segs["loc"]:
+        gamma = max(1.0, 1.0 + beta * math.log(len(segs["loc"]) / n_ref))
+
+    def seg_out(js, key_pos, mult):
+        if not js:
+            return [0.0] * d, []
+        logits = []
+        for j in js:
+            kr = bf_rope(K[j], key_pos(j), theta)
+            logits.append(mult * c * sum(a * b for a, b in zip(qr, kr)))
+        mx = max(logits)
+        e = [math.exp(s - mx) for s in logits]
+        z = sum(e)
+        w = [x / z for x in e]
+        o = [sum(w[n] * V[j][i] for n, j in enumerate(js)) for i in range(d)]
+        return o, w
+
+    o_loc, w_loc = seg_out(segs["loc"], lambda j: j, gamma)
+    if mode != "fold":
+        return o_loc, w_loc, []
+    pf = L - W - 1
+    o_far, w_far = seg_out(segs["far"], lambda j: pf, alpha)
+    lam_eff = lam if segs["far"] else 0.0
+    o = [(1 - lam_eff) * a + lam_eff * b for a, b in zip(o_loc, o_far)]
+    return o, [(1 - lam_eff) * w for w in w_loc], [lam_eff * w for w in w_far]
+
+
+# --------------------------------------------------------------------------
+# Checks (raise AssertionError on failure)
+# --------------------------------------------------------------------------
+
+
+def check_rope_complex(orc):
+    rng = np.random.default_rng(11)
+    for d, theta in ((8, 1e4), (16, 1e6), (64, 1e4)):
+        for pos in (0, 1, 7, 4096, 131075, 1048581):
+            x = rng.standard_normal(d)
+            got = orc.rope(x, pos, theta)
+            want = np.array(bf_rope(list(x), pos, theta))
+            assert np.max(np.abs(got - want)) < 1e-9, (d, theta, pos)
+
+
+def check_rope_d2(orc):
+    # d = 2: a single pair with inv_freq 1, i.e. a plane rotation by pos radians.
+    for pos in (0, 1, 2, 3, 100):
+        x = np.array([0.3, -1.7])
+        a = float(pos)
+        want = np.array([0.3 * math.cos(a) + 1.7 * math.sin(a),
+                         -1.7 * math.cos(a) + 0.3 * math.sin(a)])
+        assert np.allclose(orc.rope(x, pos, 1e4), want, atol=1e-14)
+
+
+def check_inv_freq(orc):
+    assert np.allclose(orc.rope_inv_freq(4, 1e4), [1.0, 0.01], rtol=1e-15)
+    assert np.allclose(orc.rope_inv_freq(8, 1e4), [1.0, 0.1, 0.01, 0.001], rtol=1e-14)
+    assert np.allclose(orc.rope_inv_freq(4, 1e6), [1.0, 1e-3], rtol=1e-14)
+
+
+def check_selection(orc):
+    cases = [(0, 4, 2), (1, 4, 2), (5, 4, 0), (10, 4, 2), (10, 8, 2), (10, 10, 3),
+             (10, 12, 0), (64, 16, 4), (65, 64, 4), (200, 63, 5), (7, 3, 10)]
+    for L, W, ns in cases:
+        for mode in ("full", "window", "fold", "sharp"):
+            sel = orc.select_keys(mode, L, W, ns if mode == "window" else 0)
+            want_loc = [j for j in range(L)
+                        if bf_member(mode, j, L, W, ns) == "loc"]
+            want_far = [j for j in range(L)
+                        if bf_member(mode, j, L, W, ns) == "far"]
+            assert list(sel["loc"]) == want_loc, (mode, L, W, ns)
+            assert list(sel["far"]) == want_far, (mode, L, W, ns)
+
+
+def check_brute_force(orc):
+    rng = np.random.default_rng(5)
+    d = 8
+    configs = [
+        dict(mode="full", L=37), dict(mode="full", L=1),
+        dict(mode="window", L=50, W=16, n_sink=3), dict(mode="window", L=20, W=32, n_sink=4),
+        dict(mode="window", L=40, W=10, n_sink=0),
+        dict(mode="fold", L=45, W=12, alpha=2.0, lam=0.5),
+        dict(mode="fold", L=30, W=7, alpha=0.7, lam=0.25),
+        dict(mode="fold", L=9, W=12, alpha=2.0, lam=0.5),
+        dict(mode="sharp", L=60, beta=0.4, n_ref=8),
+        dict(mode="sharp", L=5, beta=0.4, n_ref=8),
+    ]
+    for cfg in configs:
+        L = cfg["L"]
+        K = rng.standard_normal((L, d))
+        V = rng.standard_normal((L, d))
+        q = rng.standard_normal(d)
+        p = L + int(rng.integers(0, 3))
+        prm = orc.Params(mode=cfg["mode"], window=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
+                         alpha=cfg.get("alpha", 1.0), far_mix=cfg.get("lam", 0.0),
+                         scale_slope=cfg.get("beta", 0.0), scale_ref=cfg.get("n_ref", 4096),
+                         rope_theta=1e4)
+        got = orc.attend_group(q[None], p, K, V, L, prm)[0]
+        want, _, _ = bf_attend_row(cfg["mode"], list(q), p, K.tolist(), V.tolist(), L,
+                                   W=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
+                                   alpha=cfg.get("alpha", 1.0), lam=cfg.get("lam", 0.0),
+                                   beta=cfg.get("beta", 0.0), n_ref=cfg.get("n_ref", 4096))
+        assert np.max(np.abs(got - np.array(want))) < 1e-12, cfg
+
+
+def check_closed_forms(orc):
+    rng = np.random.default_rng(9)
+    d = 16
+    K = rng.standard_normal((40, d))
+    V = rng.standard_normal((40, d))
+    # one visible key -> its value
+    for mode in ("full", "window", "sharp", "fold"):
+        prm = orc.Params(mode=mode, window=4, n_sink=0, alpha=2.0, far_mix=0.5)
+        o = orc.attend_group(rng.standard_normal(d)[None], 3, K, V, 1, prm)[0]
+        assert np.allclose(o, V[0], atol=1e-14), mode
+    # zero query: every logit equal -> mean of the selected values
+    q0 = np.zeros((1, d))
+    assert np.allclose(orc.attend_group(q0, 40, K, V, 40, orc.Params("full"))[0],
+                       V.mean(0), atol=1e-13)
+    prm = orc.Params("window", window=10, n_sink=3)
+    idx = list(range(3)) + list(range(30, 40))
+    assert np.allclose(orc.attend_group(q0, 40, K, V, 40, prm)[0], V[idx].mean(0), atol=1e-13)
+    prm = orc.Params("fold", window=10, alpha=3.0, far_mix=0.3)
+    want = 0.7 * V[30:40].mean(0) + 0.3 * V[:30].mean(0)
+    assert np.allclose(orc.attend_group(q0, 40, K, V, 40, prm)[0], want, atol=1e-13)
+    # two keys: weights are a logistic function of the logit difference.
+    Kt = np.zeros((2, d)); Vt = np.zeros((2, d))
+    Kt[0, 0] = 1.0; Kt[1, 1] = 1.0       # at positions 0 and 1, theta large -> d/2.. dims
+    Vt[0, 2] = 1.0; Vt[1, 3] = 1.0
+    q = np.zeros(d); q[0] = 2.0
+    # with p = 0 and theta huge, only pair 0 rotates (by j radians); key 0 is at 0.
+    prm = orc.Params("full", rope_theta=1e30)
+    o = orc.attend_group(q[None], 0, Kt, Vt, 2, prm)[0]
+    c = 1.0 / math.sqrt(d)
+    s0 = c * 2.0 * 1.0                      # <q, k0> with no rotation
+    s1 = c * 2.0 * 0.0                      # k1 = e_1 stays e_1 (pair 1 angle ~ 0)
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    assert abs(o[2] - w0) < 1e-12 and abs(o[3] - (1 - w0)) < 1e-12
+    # a dominant key: q aligned with one rotated key and scaled up -> its value
+    p = 40
+    j = 17
+    kr = orc.rope(K[j], j, 1e4)
+    qd = orc.rope(kr * 200.0, -p, 1e4)      # un-rotate so that RoPE(q, p) = 200 kr
+    o = orc.attend_group(qd[None], p, K, V, 40, orc.Params("full"))[0]
+    assert np.allclose(o, V[j], atol=1e-6)
+
+
+def check_weights_sum(orc):
+    rng = np.random.default_rng(3)
+    d = 8
+    K = rng.standard_normal((300, d)) * 3
+    V = rng.standard_normal((300, d))
+    for prm in (orc.Params("full"), orc.Params("window", window=40, n_sink=4),
+                orc.Params("fold", window=50, alpha=2.0, far_mix=0.5),
+                orc.Params("sharp", scale_slope=0.05, scale_ref=16)):
+        o, w = orc.attend_group(rng.standard_normal((3, d)), 300, K, V, 300, prm,
+                                return_weights=True)
+        total = sum(ww.sum(axis=0) for _, ww in w.values())
+        assert np.allclose(total, 1.0, atol=1e-12), prm.mode
+        for _, ww in w.values():
+            assert (ww >= 0).all()
+        # o must be the weight-average of the values
+        o2 = sum(ww.T @ V[idx] for idx, ww in w.values())
+        assert np.allclose(o, o2, atol=1e-12)
+
+
+def check_mode_equivalences(orc):
+    rng = np.random.default_rng(4)
+    d = 16
+    L = 90
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    q = rng.standard_normal((4, d))
+    full = orc.attend_group(q, L, K, V, L, orc.Params("full"))
+    # window with W >= L is full attention (with or without sinks)
+    for W, ns in ((L, 0), (L + 5, 3), (L - 2, 4)):
+        o = orc.attend_group(q, L, K, V, L, orc.Params("window", window=W, n_sink=ns))
+        assert np.allclose(o, full, atol=1e-13), (W, ns)
+    # fold with an empty far memory (L <= W) is window attention without sinks
+    for W in (L, L + 1, 200):
+        o = orc.attend_group(q, L, K, V, L, orc.Params("fold", window=W, alpha=3.0, far_mix=0.5))
+        w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=W, n_sink=0))
+        assert np.allclose(o, w, atol=1e-13)
+    # fold with lambda = 0 is window attention over the last W keys
+    o = orc.attend_group(q, L, K, V, L, orc.Params("fold", window=30, alpha=3.0, far_mix=0.0))
+    w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=30, n_sink=0))
+    assert np.allclose(o, w, atol=1e-13)
+    # sharp with slope 0, or with |S| <= N_ref (clamp), is plain attention
+    o = orc.attend_group(q, L, K, V, L, orc.Params("sharp", scale_slope=0.0, scale_ref=4))
+    assert np.allclose(o, full, atol=1e-13)
+    o = orc.attend_group(q, L, K, V, L, orc.Params("sharp", scale_slope=0.3, scale_ref=L))
+    assert np.allclose(o, full, atol=1e-13)
+    # sharp equals full attention of the query scaled by gamma (closed form)
+    beta, nref = 0.3, 10
+    gamma = 1.0 + beta * math.log(L / nref)
+    o = orc.attend_group(q, L, K, V, L, orc.Params("sharp", scale_slope=beta, scale_ref=nref))
+    assert np.allclose(o, orc.attend_group(gamma * q, L, K, V, L, orc.Params("full")),
+                       atol=1e-13)
+    assert abs(orc.sharp_gamma(int(round(nref * math.e ** 2)), beta, nref)
+               - (1 + beta * math.log(round(nref * math.e ** 2) / nref))) < 1e-15
+
+
+def check_fold_shared_position(orc):
+    """Far logits use keys rotated at P_far = L-W-1.  Pinned through the
+    relative-position identity <R(p)q, R(P)k> = <R(p-P)q, k> (RoPE's rotation
+    matrices compose), computed here from the complex form."""
+    rng = np.random.default_rng(8)
+    d, L, W, alpha = 8, 40, 12, 2.5
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    q = rng.standard_normal(d)
+    p = L
+    pf = L - W - 1
+    # far-only output: lambda = 1
+    o = orc.attend_group(q[None], p, K, V, L, orc.Params("fold", window=W, alpha=alpha, far_mix=1.0))[0]
+    qd = bf_rope(list(q), p - pf, 1e4)
+    c = 1.0 / math.sqrt(d)
+    logits = [alpha * c * sum(a * b for a, b in zip(qd, K[j])) for j in range(L - W)]
+    mx = max(logits)
+    e = [math.exp(s - mx) for s in logits]
+    want = sum(e[j] * V[j] for j in range(L - W)) / sum(e)
+    assert np.allclose(o, want, atol=1e-12)
+    sl = orc.selection_list("fold", L, p, orc.Params("fold", window=W))
+    far = sl["segment"] == orc.SEG_FAR
+    assert (sl["key_rope_pos"][far] == pf).all()
+    assert (sl["q_rope_pos"][far] == p - pf).all()
+    assert (sl["key_rope_pos"][~far] == sl["position"][~far]).all()
+    assert (sl["q_rope_pos"][~far] == p).all()
+
+
+def check_gqa(orc):
+    rng = np.random.default_rng(12)
+    B, n_q, H_q, H_kv, d, L = 1, 2, 6, 3, 8, 20
+    q = rng.standard_normal((B, n_q, H_q, d))
+    K = rng.standard_normal((L, H_kv, d))
+    V = rng.standard_normal((L, H_kv, d))
+    prm = orc.Params("full")
+    out = orc.attend(q, [[L, L + 1]], [K], [V], [L], prm)
+    for t in range(n_q):
+        for h in range(H_q):
+            g = h // (H_q // H_kv)
+            o = orc.attend_group(q[0, t, h][None], L + t, K[:, g], V[:, g], L, prm)[0]
+            assert np.allclose(out[0, t, h], o, atol=1e-14), (t, h)
+
+
+def check_page_slot(orc):
+    bt = [5, 2, 7, 0]
+    P = 4
+    pos = np.arange(16)
+    phys, slot, flat = orc.page_slot(pos, bt, P)
+    for j in range(16):
+        assert phys[j] == bt[j // P] and slot[j] == j % P and flat[j] == bt[j // P] * P + j % P
+
+
+ALL_CHECKS = [check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
+              check_brute_force, check_closed_forms, check_weights_sum,
+              check_mode_equivalences, check_fold_shared_position, check_gqa,
+              check_page_slot]

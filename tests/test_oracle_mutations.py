@@ -1,0 +1,74 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+catch every one of them: a pin set that lets a dropped term, a wrong sign, an
+off-by-one or a transposed operand through would not be worth trusting."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.draft_attn_oracle as orc
+from tests import oracle_pins as pins
+
+
+def _rope_sign(x, pos, theta):
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    a = orc.rope_angles(pos, d, theta)
+    c, s = np.cos(a), np.sin(a)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+
+
+def _rope_adjacent_pairs(x, pos, theta):
+    # interleaved (x_2i, x_2i+1) pairing instead of rotate-half
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    a = orc.rope_angles(pos, d, theta)
+    c, s = np.cos(a), np.sin(a)
+    xe, xo = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = xe * c - xo * s
+    out[..., 1::2] = xo * c + xe * s
+    return out
+
+
+MUTATIONS = {
+    "rope_sign": ("rope", _rope_sign),
+    "rope_pairing": ("rope", _rope_adjacent_pairs),
+    "inv_freq_missing_2": ("rope_inv_freq",
+                           lambda d, theta: np.power(float(theta), -np.arange(d // 2) / d)),
+    "window_off_by_one": ("window_start", lambda L, W: max(0, L - W + 1)),
+    "far_position_off_by_one": ("fold_far_position", lambda L, W: L - W),
+    "gamma_no_clamp": ("sharp_gamma", lambda n, b, r: 1.0 + b * math.log(max(n, 1) / r)),
+    "gamma_log2": ("sharp_gamma", lambda n, b, r: max(1.0, 1 + b * math.log2(max(n, 1) / r))),
+    "softmax_no_normalise": ("_softmax",
+                             lambda s: np.exp(s - s.max(axis=0, keepdims=True)) if s.shape[0] else s),
+    "weighted_sum_drop_last_chunk": ("_weighted_sum",
+                                     lambda w, v, chunk: (w[:-1].T @ np.asarray(v[:-1], dtype=np.float64))),
+    "page_slot_transposed": ("page_slot",
+                             lambda pos, bt, P=64: (np.asarray(bt)[np.asarray(pos) % P],
+                                                    np.asarray(pos) // P,
+                                                    np.asarray(bt)[np.asarray(pos) % P] * P + np.asarray(pos) // P)),
+}
+
+
+def _run_all():
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    attr, bad = MUTATIONS[name]
+    monkeypatch.setattr(orc, attr, bad)
+    failed = _run_all()
+    assert failed, f"no pin caught the planted mistake {name!r}"
+
+
+def test_unmutated_oracle_passes_all():
+    assert _run_all() == []
