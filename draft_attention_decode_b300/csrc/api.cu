@@ -1,0 +1,327 @@
+// The C ABI (include/draft_attn.h): host-side validation, plans, tensor-map
+// encoding and launches.  No exceptions cross this boundary.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+// One status word per device; kernels OR DA_STATUS_* bits into it.
+__device__ uint32_t g_da_status;
+
+struct da_plan_s {
+  da_params p;
+  int device;
+  int num_sms;
+  int rows;
+  da::Choice choice;
+  size_t pfx_bytes;
+  size_t ws_bytes;
+  uint32_t* status;
+  double inv_freq[64];
+  float scale_log2;
+};
+
+namespace {
+
+constexpr int kAbiVersion = 100;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a cache array: rows = num_pages * H_kv * 64 tokens, columns =
+// head_dim elements; box = 64 rows x 128 bytes with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int es = p.dtype == DA_DTYPE_BF16 ? 2 : 4;
+  cuuint64_t gdim[2] = {(cuuint64_t)p.head_dim,
+                        (cuuint64_t)p.num_pages * p.num_kv_heads * da::kPage};
+  cuuint64_t gstride[1] = {(cuuint64_t)p.head_dim * es};
+  cuuint32_t box[2] = {(cuuint32_t)(da::kSwizzleRow / es), (cuuint32_t)da::kPage};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, p.dtype == DA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
+  const da_params& p = pl->p;
+  std::memset(a, 0, sizeof(*a));
+  a->status = pl->status;
+  a->B = p.batch;
+  a->n_q = p.n_q;
+  a->H_q = p.num_q_heads;
+  a->H_kv = p.num_kv_heads;
+  a->G = p.num_q_heads / p.num_kv_heads;
+  a->R = pl->rows;
+  a->max_pages = p.max_pages_per_seq;
+  a->num_pages = p.num_pages;
+  a->mode = p.mode;
+  a->W = p.window;
+  a->n_sink = p.mode == DA_MODE_WINDOW ? p.n_sink : 0;
+  a->alpha = p.alpha;
+  a->far_mix = p.far_mix;
+  a->beta = p.scale_slope;
+  a->n_ref = p.scale_ref;
+  a->scale_log2 = pl->scale_log2;
+  a->n_cta = p.num_ctas;
+  for (int i = 0; i < 64; ++i) a->inv_freq[i] = pl->inv_freq[i];
+}
+
+}  // namespace
+
+extern "C" {
+
+int draft_attn_version(void) { return kAbiVersion; }
+
+const char* draft_attn_error_string(int code) {
+  switch (code) {
+    case DA_OK: return "ok";
+    case DA_ERR_INVALID_ARG: return "invalid argument";
+    case DA_ERR_UNSUPPORTED: return "unsupported shape or parameter combination";
+    case DA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DA_ERR_CUDA: return "CUDA runtime error";
+    case DA_ERR_DEVICE_FAULT: return "device status word reported a fault";
+    default: return "unknown error";
+  }
+}
+
+int draft_attn_check_params(const da_params* p) {
+  if (!p) return DA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->batch > da::kMaxBatch) return DA_ERR_INVALID_ARG;
+  if (p->n_q < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return DA_ERR_INVALID_ARG;
+  if (p->num_q_heads % p->num_kv_heads != 0) return DA_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return DA_ERR_INVALID_ARG;
+  if (p->page_size != da::kPage) return DA_ERR_INVALID_ARG;
+  if (p->num_pages < 1 || p->max_pages_per_seq < 1) return DA_ERR_INVALID_ARG;
+  if ((int64_t)p->num_pages * p->num_kv_heads * da::kPage >= (int64_t)1 << 31)
+    return DA_ERR_INVALID_ARG;
+  if ((int64_t)p->max_pages_per_seq * da::kPage >= (int64_t)1 << 31) return DA_ERR_INVALID_ARG;
+  if (p->dtype != DA_DTYPE_BF16 && p->dtype != DA_DTYPE_FP32) return DA_ERR_INVALID_ARG;
+  if (p->mode < DA_MODE_FULL || p->mode > DA_MODE_SHARP) return DA_ERR_INVALID_ARG;
+  if (!(p->rope_theta > 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return DA_ERR_INVALID_ARG;
+  if (p->num_ctas < 0 || p->num_ctas > 65535) return DA_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
+  if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
+    if (p->window < 1) return DA_ERR_INVALID_ARG;
+  }
+  if (p->mode == DA_MODE_WINDOW && p->n_sink < 0) return DA_ERR_INVALID_ARG;
+  if (p->mode == DA_MODE_FOLD) {
+    if (p->n_sink != 0) return DA_ERR_INVALID_ARG;
+    if (!(p->alpha > 0.f) || !std::isfinite(p->alpha)) return DA_ERR_INVALID_ARG;
+    if (!(p->far_mix >= 0.f && p->far_mix <= 1.f)) return DA_ERR_INVALID_ARG;
+  }
+  if (p->mode == DA_MODE_SHARP) {
+    if (!(p->scale_slope >= 0.f) || !std::isfinite(p->scale_slope)) return DA_ERR_INVALID_ARG;
+    if (p->scale_ref < 1) return DA_ERR_INVALID_ARG;
+  }
+  const int64_t rows = (int64_t)(p->num_q_heads / p->num_kv_heads) * p->n_q;
+  if (rows > 32) return DA_ERR_UNSUPPORTED;
+  if (rows > 8 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
+  return DA_OK;
+}
+
+int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t* workspace_bytes) {
+  if (!plan) return DA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  int rc = draft_attn_check_params(params);
+  if (rc != DA_OK) return rc;
+  DeviceGuard g(device);
+  if (!g.ok) return DA_ERR_CUDA;
+  int sms = 0, max_smem = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess)
+    return DA_ERR_CUDA;
+  da_plan_s* pl = new (std::nothrow) da_plan_s();
+  if (!pl) return DA_ERR_CUDA;
+  pl->p = *params;
+  pl->device = device;
+  pl->num_sms = sms;
+  pl->rows = (params->num_q_heads / params->num_kv_heads) * params->n_q;
+  if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, max_smem,
+                         &pl->choice)) {
+    delete pl;
+    return DA_ERR_UNSUPPORTED;
+  }
+  if (pl->p.num_ctas == 0) pl->p.num_ctas = sms;  // one persistent CTA per SM
+  const int d = params->head_dim;
+  pl->pfx_bytes = ((size_t)(2 * params->batch + 1) * 4 + 255) / 256 * 256;
+  const size_t slots = (size_t)pl->p.num_ctas + (size_t)2 * params->batch * params->num_kv_heads;
+  pl->ws_bytes = pl->pfx_bytes + slots * (size_t)pl->choice.rk * (d + 2) * sizeof(float);
+  for (int i = 0; i < 64; ++i)
+    pl->inv_freq[i] = i < d / 2 ? std::pow(params->rope_theta, -2.0 * i / d) : 0.0;
+  const double c = params->softmax_scale > 0.f ? (double)params->softmax_scale
+                                               : 1.0 / std::sqrt((double)d);
+  pl->scale_log2 = (float)(c * 1.4426950408889634074);  // log2(e)
+  void* sp = nullptr;
+  if (cudaGetSymbolAddress(&sp, g_da_status) != cudaSuccess ||
+      da::prepare_decode(pl->choice, params->dtype, d) != cudaSuccess) {
+    delete pl;
+    return DA_ERR_CUDA;
+  }
+  pl->status = static_cast<uint32_t*>(sp);
+  *plan = pl;
+  if (workspace_bytes) *workspace_bytes = pl->ws_bytes;
+  return DA_OK;
+}
+
+int draft_attn_plan_info(da_plan_t pl, da_plan_info* info) {
+  if (!pl || !info) return DA_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->num_ctas = pl->p.num_ctas;
+  info->num_sms = pl->num_sms;
+  info->rows_per_kv_head = pl->rows;
+  info->kernel_rows = pl->choice.rk;
+  info->engine = pl->choice.engine;
+  info->stages = pl->choice.stages;
+  info->smem_bytes = (int32_t)pl->choice.smem;
+  info->workspace_bytes = pl->ws_bytes;
+  return DA_OK;
+}
+
+void draft_attn_plan_destroy(da_plan_t pl) { delete pl; }
+
+int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, const int32_t* pos,
+                         int32_t batch, int32_t n_new, const int32_t* block_table, void* k_cache,
+                         void* v_cache, void* k_side, void* stream) {
+  if (!pl || batch < 0 || batch > pl->p.batch || n_new < 0) return DA_ERR_INVALID_ARG;
+  if (batch == 0 || n_new == 0) return DA_OK;
+  if (!k_new || !v_new || !pos || !block_table || !k_cache || !v_cache) return DA_ERR_INVALID_ARG;
+  if (pl->p.mode == DA_MODE_FOLD && !k_side) return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  da::AppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.k = k_new;
+  a.v = v_new;
+  a.pos = pos;
+  a.block_table = block_table;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_side = k_side;
+  a.status = pl->status;
+  a.B = batch;
+  a.n_new = n_new;
+  a.H_kv = pl->p.num_kv_heads;
+  a.max_pages = pl->p.max_pages_per_seq;
+  a.num_pages = pl->p.num_pages;
+  for (int i = 0; i < 64; ++i) a.inv_freq[i] = pl->inv_freq[i];
+  cudaError_t e = da::launch_append(pl->p.dtype, pl->p.head_dim, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
+                   const int32_t* block_table, const void* k_cache, const void* v_cache,
+                   const void* k_side, void* out, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (!pl || !q || !q_pos || !ctx_lens || !block_table || !k_cache || !v_cache || !out ||
+      !workspace)
+    return DA_ERR_INVALID_ARG;
+  const bool fold = pl->p.mode == DA_MODE_FOLD;
+  if (fold && !k_side) return DA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      (k_side && !aligned(k_side, 16)))
+    return DA_ERR_INVALID_ARG;
+  if (workspace_bytes < pl->ws_bytes) return DA_ERR_WORKSPACE_TOO_SMALL;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  CUtensorMap mk, mv, ms;
+  if (!encode_cache_map(&mk, k_cache, pl->p) || !encode_cache_map(&mv, v_cache, pl->p))
+    return DA_ERR_CUDA;
+  if (fold) {
+    if (!encode_cache_map(&ms, k_side, pl->p)) return DA_ERR_CUDA;
+  } else {
+    ms = mk;
+  }
+  da::DecodeArgs a;
+  fill_args(pl, &a);
+  a.q = q;
+  a.q_pos = q_pos;
+  a.ctx_lens = ctx_lens;
+  a.block_table = block_table;
+  a.out = out;
+  a.pfx = static_cast<int32_t*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->pfx_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, a, mk, mv, ms, st) != cudaSuccess)
+    return DA_ERR_CUDA;
+  if (da::launch_combine(pl->p.dtype, pl->p.head_dim, pl->choice.rk, a, st) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* ctx_lens,
+                            const int32_t* block_table, int32_t b, int32_t t, int32_t* positions,
+                            int64_t* phys_slot, int32_t* key_rope_pos, int32_t* q_rope_pos,
+                            int8_t* segment, int64_t capacity, int64_t* count, void* stream) {
+  if (!pl || !q_pos || !ctx_lens || !block_table || !count || capacity < 0) return DA_ERR_INVALID_ARG;
+  if (b < 0 || b >= pl->p.batch || t < 0 || t >= pl->p.n_q) return DA_ERR_INVALID_ARG;
+  if (capacity > 0 && (!positions || !phys_slot || !key_rope_pos || !q_rope_pos || !segment))
+    return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  da::DecodeArgs a;
+  fill_args(pl, &a);
+  a.q_pos = q_pos;
+  a.ctx_lens = ctx_lens;
+  a.block_table = block_table;
+  da::GatherOut o{positions, phys_slot, key_rope_pos, q_rope_pos, segment, capacity, count};
+  return da::launch_gather(a, b, t, o, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_CUDA;
+}
+
+int draft_attn_get_status(da_plan_t pl, void* stream, uint32_t* bits) {
+  if (!pl) return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, pl->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DA_ERR_CUDA;
+  if (v) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(pl->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return DA_ERR_CUDA;
+  }
+  if (bits) *bits = v;
+  return v ? DA_ERR_DEVICE_FAULT : DA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,301 @@
+// Shared device helpers of the draft-attention kernels (sm_103a).
+//
+// Everything here is used by more than one kernel so that the decode kernels,
+// the append kernel and the debug-gather hook take the same decisions: the
+// mode's key ranges, the block-table translation, the RoPE angle.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "draft_attn.h"
+
+namespace da {
+
+constexpr int kPage = 64;            // tokens per page (the only page size built)
+constexpr int kSwizzleRow = 128;     // bytes per row of a 128B-swizzled TMA box
+constexpr int kBoxBytes = kPage * kSwizzleRow;  // one 64-row x 128-byte box
+constexpr int kMaxBatch = 1024;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+// Two consumer warpgroups plus one producer warpgroup (only its first warp
+// works).  Launched at 168 registers per thread; the producer group gives
+// registers back (setmaxnreg 40) so the consumers can hold 232:
+// 128 * 40 + 256 * 232 = 384 * 168.
+constexpr int kThreads = kConsumerThreads + 128;
+constexpr int kProducerRegs = 40;
+constexpr int kConsumerRegs = 232;
+
+// ---------------------------------------------------------------------------
+// Parameters shared by the split-KV kernels and the combine pass.
+// ---------------------------------------------------------------------------
+struct DecodeArgs {
+  const void* q;
+  const int32_t* q_pos;
+  const int32_t* ctx_lens;
+  const int32_t* block_table;
+  void* out;
+  float* part;          // partial (m, l, o) slots
+  int32_t* pfx;         // per-(b, range) page prefix, written by CTA 0
+  uint32_t* status;
+  int32_t B, n_q, H_q, H_kv, G, R;  // R = G * n_q rows per KV head
+  int32_t max_pages, num_pages;
+  int32_t mode, W, n_sink;
+  float alpha, far_mix, beta;
+  int32_t n_ref;
+  float scale_log2;     // softmax scale * log2(e)
+  int32_t n_cta;
+  double inv_freq[64];  // theta^(-2i/d), i < d/2
+};
+
+// ---------------------------------------------------------------------------
+// Mode -> key ranges.  Two half-open ranges per sequence, in ascending
+// position order; range 0 of FOLD is the far memory, everything else belongs
+// to the main (local) softmax.
+//   full / sharp : [0, L)                              "Windowed-MTP", Abstract
+//   window       : [0, n_sink) u [L-W, L)  (merged into [0, L) when they touch)
+//   fold         : far [0, L-W), local [L-W, L)        "FOLD", abstract
+// ---------------------------------------------------------------------------
+struct Ranges {
+  int32_t k0[2], k1[2];
+};
+
+__host__ __device__ __forceinline__ Ranges mode_ranges(int mode, int32_t L, int32_t W,
+                                                       int32_t n_sink) {
+  Ranges r;
+  r.k0[0] = 0; r.k1[0] = 0; r.k0[1] = L; r.k1[1] = L;
+  if (L <= 0) { r.k0[1] = r.k1[1] = 0; return r; }
+  int32_t ws = L - W > 0 ? L - W : 0;
+  switch (mode) {
+    case DA_MODE_WINDOW:
+      if (n_sink > 0 && ws > n_sink) {
+        r.k0[0] = 0; r.k1[0] = n_sink; r.k0[1] = ws; r.k1[1] = L;
+      } else if (n_sink > 0) {
+        r.k0[0] = 0; r.k1[0] = L;
+      } else {
+        r.k0[0] = ws; r.k1[0] = L;
+      }
+      break;
+    case DA_MODE_FOLD:
+      r.k0[0] = 0; r.k1[0] = ws; r.k0[1] = ws; r.k1[1] = L;
+      break;
+    default:  // full, sharp
+      r.k0[0] = 0; r.k1[0] = L;
+      break;
+  }
+  return r;
+}
+
+__host__ __device__ __forceinline__ bool range_is_far(int mode, int r) {
+  return mode == DA_MODE_FOLD && r == 0;
+}
+
+__host__ __device__ __forceinline__ int32_t range_pages(int32_t k0, int32_t k1) {
+  return k1 > k0 ? (k1 + kPage - 1) / kPage - k0 / kPage : 0;
+}
+
+// Shared virtual position of the FOLD far memory (the newest far token).
+__host__ __device__ __forceinline__ int32_t fold_far_pos(int32_t L, int32_t W) {
+  return L - W - 1;
+}
+
+// Number of keys the main softmax of a sequence sees (SharpDraft's |S|).
+__host__ __device__ __forceinline__ int32_t visible_keys(int mode, int32_t L, int32_t W,
+                                                        int32_t n_sink) {
+  Ranges r = mode_ranges(mode, L, W, n_sink);
+  int32_t n = 0;
+  for (int i = 0; i < 2; ++i)
+    if (!range_is_far(mode, i) && r.k1[i] > r.k0[i]) n += r.k1[i] - r.k0[i];
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// RoPE angle.  angle = pos * inv_freq is formed in double precision (positions
+// reach ~1M, where a float product would be off by ~0.06 rad), reduced modulo
+// 2*pi with Cody and Waite's two-constant additive reduction (2*pi split into
+// a double and its double-rounded remainder), and only then narrowed to float
+// for the library sincosf, which is accurate on [-pi, pi].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void rope_cos_sin(int32_t pos, double inv_freq, float& c, float& s) {
+  const double kInvTwoPi = 0.15915494309189533577;    // 1 / (2 pi)
+  const double kTwoPiHi = 6.28318530717958623200;     // 2 pi rounded to double
+  const double kTwoPiLo = 2.44929359829470635445e-16; // 2 pi - kTwoPiHi
+  double a = (double)pos * inv_freq;
+  double k = rint(a * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, a);
+  r = fma(-k, kTwoPiLo, r);
+  sincosf((float)r, &s, &c);
+}
+
+// ---------------------------------------------------------------------------
+// Block-table translation (PagedAttention layout).  Returns -1 and flags the
+// status word when the entry is outside [0, num_pages).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t phys_page(const int32_t* bt, int32_t b, int32_t page,
+                                             int32_t max_pages, int32_t num_pages,
+                                             uint32_t* status) {
+  if (page < 0 || page >= max_pages) {
+    atomicOr(status, DA_STATUS_BAD_CTX_LEN);
+    return -1;
+  }
+  int32_t p = __ldg(bt + (int64_t)b * max_pages + page);
+  if (p < 0 || p >= num_pages) {
+    atomicOr(status, DA_STATUS_BAD_PAGE);
+    return -1;
+  }
+  return p;
+}
+
+// Context length clamped to what the block table can hold.
+__device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint32_t* status) {
+  int64_t cap = (int64_t)max_pages * kPage;
+  if (L < 0 || (int64_t)L > cap) {
+    atomicOr(status, DA_STATUS_BAD_CTX_LEN);
+    return L < 0 ? 0 : (int32_t)cap;
+  }
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Flat work partition.  The pages of every (b, range, kv head) are laid end
+// to end (b outer, then range, then head); CTA i of n takes positions
+// [floor(i*TP/n), floor((i+1)*TP/n)).  A "piece" is the part of one
+// (b, range, head) sequence that one CTA covers; it writes its partial to
+// slot (cta + sequence index), which is unique because both indices only grow
+// along the line and every new piece advances at least one of them.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int64_t n) {
+  return (i * TP) / n;
+}
+// The CTA whose (non-empty) range holds flat position x.
+__host__ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t TP, int64_t n) {
+  return ((x + 1) * n - 1) / TP;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, register reallocation, misc.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^31 SM cycles (about a second), sets the
+// timeout status bit and returns false.  Never expected to trigger.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > (1ll << 31)) {
+      atomicOr(status, DA_STATUS_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled TMA load of one 64-row x 128-byte box into shared memory,
+// completing on `bar` (transaction bytes).  x is the element column (a
+// multiple of 128 bytes here), y the row.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read once (the KV stream): evict first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Address of element (row, byte offset) inside a stage buffer laid out as
+// consecutive 64-row x 128-byte boxes with the 128-byte TMA swizzle: the
+// 16-byte chunk index inside a row is XOR-ed with the row index mod 8.
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int byte) {
+  int box = byte >> 7;
+  int chunk = (byte >> 4) & 7;
+  return base + box * kBoxBytes + row * kSwizzleRow + ((chunk ^ (row & 7)) << 4) + (byte & 15);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+}  // namespace da

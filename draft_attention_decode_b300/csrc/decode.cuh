@@ -1,0 +1,561 @@
+// Split-KV decode kernel: the pipeline of pipeline.cuh driving one of two
+// compute engines.
+//
+//  * CoreEngine (<= 8 query rows per KV head: one draft token, GQA groups up
+//    to 8).  QK^T and PV on the FP32 pipes with packed two-wide FMAs; no
+//    tensor cores, since with this few rows the page read, not arithmetic, is
+//    the bound.  Each warp owns 8 of the page's 64 keys: for QK^T eight lanes
+//    share one key (16 dimensions each at d = 128) and a reduce-scatter
+//    butterfly leaves lane i with row i's score; for PV every lane owns d/32
+//    dimensions of all rows.
+//  * MmaEngine (9..32 rows: draft trees of several tokens).  QK^T and PV as
+//    bf16 m16n8k16 tensor-core MMAs with FP32 accumulation, keys on the M side
+//    of QK^T (S^T = K Q^T) so that 8-row query tiles need no padding, P^T
+//    moved into the PV operand layout with movmatrix.
+//
+// Both keep one online softmax (m, l, o) per warp and query row, in the log2
+// domain (the query is pre-scaled by softmax_scale * log2 e and by alpha or
+// gamma), and merge the eight warps only at the end of a piece.
+#pragma once
+
+#include "pipeline.cuh"
+
+namespace da {
+
+// ---------------------------------------------------------------------------
+// Query preparation for a piece: RoPE at the query position (or at
+// q_pos - P_far for FOLD far memory, which equals rotating the keys at P_far:
+// <R(p)q, R(P)k> = <R(p-P)q, k>), times the logit multiplier, into s.q
+// [rk][d] as FP32.  Rows >= R are zero.  Consumer threads only.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int RK>
+__device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
+  const int tid = threadIdx.x;
+  const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1, r = e & 1;
+  const int32_t L = s.len[b];
+  float mult = a.scale_log2;
+  int32_t shift = 0;
+  if (range_is_far(a.mode, r)) {
+    mult *= a.alpha;                     // "FOLD", abstract: concentration factor
+    shift = fold_far_pos(L, a.W);
+  } else if (a.mode == DA_MODE_SHARP) {  // "SharpDraft", Abstract: query scaling
+    const int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
+    if (n > 0) mult *= fmaxf(1.f, 1.f + a.beta * logf((float)n / (float)a.n_ref));
+  }
+  float2* cs = reinterpret_cast<float2*>(s.mo);
+  for (int i = tid; i < a.n_q * (D / 2); i += kConsumerThreads) {
+    const int t = i / (D / 2), f = i - t * (D / 2);
+    const int32_t p = __ldg(a.q_pos + b * a.n_q + t) - shift;
+    float c, sn;
+    rope_cos_sin(p, s.invf[f], c, sn);
+    cs[i] = make_float2(c, sn);
+  }
+  named_barrier(1, kConsumerThreads);
+  const T* qb = static_cast<const T*>(a.q);
+  for (int i = tid; i < RK * (D / 2); i += kConsumerThreads) {
+    const int row = i / (D / 2), f = i - row * (D / 2);
+    float xr = 0.f, yr = 0.f;
+    if (row < a.R) {
+      const int t = row / a.G, j = row - t * a.G;
+      const T* src = qb + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D;
+      const float x = to_f32<T>(src[f]), y = to_f32<T>(src[f + D / 2]);
+      const float2 c = cs[t * (D / 2) + f];
+      xr = (x * c.x - y * c.y) * mult;
+      yr = (y * c.x + x * c.y) * mult;
+    }
+    s.q[row * D + f] = xr;
+    s.q[row * D + f + D / 2] = yr;
+  }
+  named_barrier(1, kConsumerThreads);
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// Reduce-scatter of RK per-lane partial sums over the 8 lanes of a key group
+// (lane bits 0..2): afterwards lane ds holds the total for row ds & (RK-1).
+template <int RK>
+__device__ __forceinline__ float reduce_scatter8(float (&v)[RK], int ds) {
+#pragma unroll
+  for (int m = RK / 2; m >= 1; m >>= 1) {
+    const bool up = (ds & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = up ? v[i] : v[i + m];
+      const float keep = up ? v[i + m] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int m = RK; m < 8; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+template <typename T>
+struct Chunk;  // one 16-byte shared-memory chunk as floats
+template <>
+struct Chunk<__nv_bfloat16> {
+  __device__ __forceinline__ static void load(uint32_t addr, float (&f)[8]) {
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
+    f[0] = bf16lo(w0); f[1] = bf16hi(w0); f[2] = bf16lo(w1); f[3] = bf16hi(w1);
+    f[4] = bf16lo(w2); f[5] = bf16hi(w2); f[6] = bf16lo(w3); f[7] = bf16hi(w3);
+  }
+};
+template <>
+struct Chunk<float> {
+  __device__ __forceinline__ static void load(uint32_t addr, float (&f)[4]) {
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(addr));
+  }
+};
+
+// DPL consecutive elements (the PV slice of one lane) as floats.
+template <typename T, int DPL>
+__device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
+  if constexpr (sizeof(T) == 2 && DPL == 4) {
+    uint32_t w0, w1;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr));
+    f[0] = bf16lo(w0); f[1] = bf16hi(w0); f[2] = bf16lo(w1); f[3] = bf16hi(w1);
+  } else if constexpr (sizeof(T) == 2 && DPL == 2) {
+    uint32_t w0;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(addr));
+    f[0] = bf16lo(w0); f[1] = bf16hi(w0);
+  } else if constexpr (sizeof(T) == 4 && DPL == 4) {
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(addr));
+  } else {
+    static_assert(sizeof(T) == 4 && DPL == 2, "slice shape");
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(f[0]), "=f"(f[1]) : "r"(addr));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core engine.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int RK>
+struct CoreEngine {
+  static constexpr int ES = sizeof(T);
+  static constexpr int DQ = D / 8;            // QK dims per lane
+  static constexpr int NCH = DQ * ES / 16;    // 16-byte chunks per lane (1, 2 or 4)
+  static constexpr int EPC = 16 / ES;         // elements per chunk
+  static constexpr int DPL = D / 32;          // PV dims per lane
+  static_assert(RK == 1 || RK == 2 || RK == 4 || RK == 8, "rows");
+  static_assert(NCH >= 1 && (NCH & (NCH - 1)) == 0, "chunks");
+
+  float2 q2[RK][DQ / 2];
+  float2 o2[RK][DPL / 2];
+  float m_run, l_run;
+  int lane, warp, kg, ds;
+
+  __device__ __forceinline__ void init() {
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    kg = lane >> 3;
+    ds = lane & 7;
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int r = 0; r < RK; ++r)
+#pragma unroll
+      for (int e = 0; e < DPL / 2; ++e) o2[r][e] = make_float2(0.f, 0.f);
+    m_run = -INFINITY;
+    l_run = 0.f;
+  }
+
+  __device__ __forceinline__ void begin(const Smem& s) {
+    // The lane's QK dims, chunk order rotated by ds so that the eight lanes of
+    // a key group hit eight different 16-byte bank groups.
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
+      const int d0 = (ds * NCH + ic) * EPC;
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e)
+          q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0 + 2 * e], s.q[r * D + d0 + 2 * e + 1]);
+    }
+    reset();
+  }
+
+  __device__ __forceinline__ void pv_key(uint32_t vbase, const float* pw, int key, int j) {
+    float v[DPL];
+    load_slice<T, DPL>(swz_addr(vbase, key, lane * DPL * ES), v);
+    float pj[RK];
+    if constexpr (RK >= 4) {
+#pragma unroll
+      for (int r = 0; r < RK; r += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(pw + j * RK + r);
+        pj[r] = x.x; pj[r + 1] = x.y; pj[r + 2] = x.z; pj[r + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < RK; ++r) pj[r] = pw[j * RK + r];
+    }
+#pragma unroll
+    for (int r = 0; r < RK; ++r)
+#pragma unroll
+      for (int e = 0; e < DPL / 2; ++e)
+        o2[r][e] = ffma2(make_float2(pj[r], pj[r]), make_float2(v[2 * e], v[2 * e + 1]), o2[r][e]);
+  }
+
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+    const int wk0 = warp * 8;
+    float sc[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int key = wk0 + kg + 4 * it;
+      float2 acc[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) acc[r] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
+        float f[EPC];
+        Chunk<T>::load(swz_addr(kbase, key, (ds * NCH + ic) * 16), f);
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
+#pragma unroll
+          for (int r = 0; r < RK; ++r) acc[r] = ffma2(q2[r][i * (EPC / 2) + e], kk, acc[r]);
+        }
+      }
+      float v[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
+      const float sr = reduce_scatter8<RK>(v, ds);
+      sc[it] = (key >= lo && key < hi) ? sr : -INFINITY;
+    }
+    // Online softmax for row ds & (RK-1) over the warp's 8 keys.
+    float mx = fmaxf(sc[0], sc[1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_new = fmaxf(m_run, mx);
+    float alpha = 1.f, p0 = 0.f, p1 = 0.f;
+    if (m_new != -INFINITY) {
+      alpha = fast_exp2(m_run - m_new);
+      p0 = fast_exp2(sc[0] - m_new);
+      p1 = fast_exp2(sc[1] - m_new);
+    }
+    l_run = l_run * alpha + p0 + p1;
+    m_run = m_new;
+    float* pw = s.p + warp * 9 * RK;
+    __syncwarp();
+    if (ds < RK) {
+      pw[kg * RK + ds] = p0;
+      pw[(kg + 4) * RK + ds] = p1;
+      if (kg == 0) pw[8 * RK + ds] = alpha;
+    }
+    __syncwarp();
+    // PV over the warp's valid keys.
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      const float al = pw[8 * RK + r];
+#pragma unroll
+      for (int e = 0; e < DPL / 2; ++e) {
+        o2[r][e].x *= al;
+        o2[r][e].y *= al;
+      }
+    }
+    const int jlo = max(lo - wk0, 0), jhi = min(hi - wk0, 8);
+    if (jlo == 0 && jhi == 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pv_key(vbase, pw, wk0 + j, j);
+    } else {
+      for (int j = jlo; j < jhi; ++j) pv_key(vbase, pw, wk0 + j, j);
+    }
+  }
+
+  // Merge the eight warps' states and write the piece's partial to `slot`.
+  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+    float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
+#pragma unroll
+    for (int r = 0; r < RK; ++r)
+#pragma unroll
+      for (int e = 0; e < DPL / 2; ++e)
+        *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + lane * DPL + 2 * e) = o2[r][e];
+    named_barrier(1, kConsumerThreads);
+    float* part = a.part + slot * (int64_t)(RK * (D + 2));
+    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+      const int r = idx / D, dim = idx - r * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
+      float o = 0.f, l = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float2 ml = s.ml[w * RK + r];
+          const float sc = fast_exp2(ml.x - M);
+          o += sc * s.mo[(w * RK + r) * D + dim];
+          l += sc * ml.y;
+        }
+      }
+      part[2 * RK + r * D + dim] = o;
+      if (dim == 0) {
+        part[r] = M;
+        part[RK + r] = l;
+      }
+    }
+    named_barrier(1, kConsumerThreads);
+    reset();
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Tensor-core engine (bf16 only, 32 rows).  Warp w: key block kb = w & 3 (16
+// keys of the page), row group rg = w >> 2 (16 query rows, two n8 tiles).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+struct MmaEngine {
+  static constexpr int RK = 32;
+  static constexpr int KS = D / 16;   // k-steps of QK^T, m-tiles of PV
+  uint32_t qf[KS][2][2];
+  float O[KS][2][4];
+  float m[2][2], l[2][2];
+  int lane, warp, kb, rg, g, t;
+
+  __device__ __forceinline__ void init() {
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    kb = warp & 3;
+    rg = warp >> 2;
+    g = lane >> 2;
+    t = lane & 3;
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) O[mt][nt][c] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) { m[nt][cc] = -INFINITY; l[nt][cc] = 0.f; }
+  }
+
+  __device__ __forceinline__ void begin(const Smem& s) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float* qr = s.q + (16 * rg + 8 * nt + g) * D + 16 * ks + 2 * t;
+        qf[ks][nt][0] = pack_bf16(qr[0], qr[1]);
+        qf[ks][nt][1] = pack_bf16(qr[8], qr[9]);
+      }
+    reset();
+  }
+
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+    const int key0 = 16 * kb;
+    if (hi <= key0 || lo >= key0 + 16) return;
+    float S[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) S[nt][c] = 0.f;
+    const int krow = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(swz_addr(kbase, krow, (16 * ks + (lane >> 4) * 8) * 2), a);
+      mma_bf16(S[0], a, qf[ks][0][0], qf[ks][0][1]);
+      mma_bf16(S[1], a, qf[ks][1][0], qf[ks][1][1]);
+    }
+    const bool oka = (key0 + g >= lo) && (key0 + g < hi);
+    const bool okb = (key0 + g + 8 >= lo) && (key0 + g + 8 < hi);
+    float alpha[2][2];
+    uint32_t bp[2][2];
+    bool all_one = true;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float P[4];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const float v0 = oka ? S[nt][cc] : -INFINITY;
+        const float v1 = okb ? S[nt][cc + 2] : -INFINITY;
+        float mx = fmaxf(v0, v1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[nt][cc], mx);
+        float al = 1.f, p0 = 0.f, p1 = 0.f;
+        if (mn != -INFINITY) {
+          al = fast_exp2(m[nt][cc] - mn);
+          p0 = fast_exp2(v0 - mn);
+          p1 = fast_exp2(v1 - mn);
+        }
+        l[nt][cc] = l[nt][cc] * al + p0 + p1;
+        m[nt][cc] = mn;
+        alpha[nt][cc] = al;
+        all_one &= (al == 1.f);
+        P[cc] = p0;
+        P[cc + 2] = p1;
+      }
+      bp[nt][0] = movm_t(pack_bf16(P[0], P[1]));
+      bp[nt][1] = movm_t(pack_bf16(P[2], P[3]));
+    }
+    if (!__all_sync(0xffffffffu, all_one)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          O[mt][nt][0] *= alpha[nt][0];
+          O[mt][nt][1] *= alpha[nt][1];
+          O[mt][nt][2] *= alpha[nt][0];
+          O[mt][nt][3] *= alpha[nt][1];
+        }
+    }
+    // Keys outside [lo, hi) may hold anything (NaN included): zero their V.
+    uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
+    if (lo > key0 || hi < key0 + 16) {
+      const int k2 = key0 + 2 * t;
+      auto ok = [&](int k) { return k >= lo && k < hi; };
+      mask01 = (ok(k2) ? 0x0000ffffu : 0u) | (ok(k2 + 1) ? 0xffff0000u : 0u);
+      mask23 = (ok(k2 + 8) ? 0x0000ffffu : 0u) | (ok(k2 + 9) ? 0xffff0000u : 0u);
+    }
+    const int vrow = key0 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldsm_x4_t(swz_addr(vbase, vrow, (16 * mt + ((lane >> 3) & 1) * 8) * 2), a);
+      a[0] &= mask01; a[1] &= mask01; a[2] &= mask23; a[3] &= mask23;
+      mma_bf16(O[mt][0], a, bp[0][0], bp[0][1]);
+      mma_bf16(O[mt][1], a, bp[1][0], bp[1][1]);
+    }
+  }
+
+  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float lt = l[nt][cc];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        if (g == 0) s.ml[warp * 16 + 8 * nt + 2 * t + cc] = make_float2(m[nt][cc], lt);
+      }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int lr = 8 * nt + 2 * t;
+        float* base = s.mo + (warp * 16) * D + 16 * mt + g;
+        base[lr * D] = O[mt][nt][0];
+        base[(lr + 1) * D] = O[mt][nt][1];
+        base[lr * D + 8] = O[mt][nt][2];
+        base[(lr + 1) * D + 8] = O[mt][nt][3];
+      }
+    named_barrier(1, kConsumerThreads);
+    float* part = a.part + slot * (int64_t)(RK * (D + 2));
+    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+      const int r = idx / D, dim = idx - r * D;
+      const int grp = r >> 4, lr = r & 15;
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) M = fmaxf(M, s.ml[(grp * 4 + k) * 16 + lr].x);
+      float o = 0.f, lsum = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int w = grp * 4 + k;
+          const float2 ml = s.ml[w * 16 + lr];
+          const float sc = fast_exp2(ml.x - M);
+          o += sc * s.mo[(w * 16 + lr) * D + dim];
+          lsum += sc * ml.y;
+        }
+      }
+      part[2 * RK + r * D + dim] = o;
+      if (dim == 0) {
+        part[r] = M;
+        part[RK + r] = lsum;
+      }
+    }
+    named_barrier(1, kConsumerThreads);
+    reset();
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <typename T, int D, class Engine, int ENGINE_ID, int RK>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ms,
+                  int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr int ES = sizeof(T);
+  constexpr int NCB = D * ES / kSwizzleRow;
+  const Layout L = make_layout(ENGINE_ID, ES, D, RK, stages, a.B);
+  Smem s = carve(smem_raw, L);
+  prologue<D>(a, s, L);
+  const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
+  const int64_t xs = cta_begin(blockIdx.x, TP, a.n_cta);
+  const int64_t xe = cta_begin(blockIdx.x + 1, TP, a.n_cta);
+  const int warp = threadIdx.x >> 5;
+  if (warp >= kConsumerWarps) {
+    regs_dec<kProducerRegs>();
+    if (warp == kConsumerWarps) producer<ES, NCB>(a, s, L, xs, xe, &mk, &mv, &ms);
+    return;
+  }
+  regs_inc<kConsumerRegs>();
+  Engine eng;
+  eng.init();
+  const uint32_t base = smem_u32(s.stage);
+  uint32_t n = 0;
+  for (int64_t x = xs; x < xe; ++x, ++n) {
+    const uint32_t st = n % L.stages;
+    const uint32_t par = (n / L.stages) & 1u;
+    if (!mbar_wait(&s.full[st], par, a.status)) break;
+    const PageInfo inf = s.info[st];
+    if (inf.flags & kFirst) {
+      prep_queries<T, D, RK>(a, s, inf.seq);
+      eng.begin(s);
+    }
+    if (inf.flags & kValid) {
+      const uint32_t kb = base + st * L.stage_bytes;
+      eng.page(s, kb, kb + NCB * kBoxBytes, inf.lohi & 0xffff, inf.lohi >> 16);
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
+    if (inf.flags & kLast) eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
+  }
+}
+
+}  // namespace da

@@ -1,0 +1,51 @@
+// Host-side interface between the C ABI (api.cu) and the kernel translation
+// units (decode.cu, aux.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace da {
+
+struct Choice {
+  int engine;      // DA_ENGINE_CUDA_CORE or DA_ENGINE_MMA
+  int rk;          // rows the kernel instance computes
+  int stages;      // pipeline depth
+  uint32_t smem;   // dynamic shared memory bytes
+};
+
+// Picks the kernel instance for `rows` query rows per KV head; false when
+// none exists or it does not fit in `max_smem` bytes of shared memory.
+bool choose_kernel(int dtype, int d, int rows, int batch, int max_smem, Choice* c);
+
+cudaError_t prepare_decode(const Choice& c, int dtype, int d);
+cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,
+                          const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
+                          cudaStream_t st);
+cudaError_t launch_combine(int dtype, int d, int rk, const DecodeArgs& a, cudaStream_t st);
+
+struct AppendArgs {
+  const void* k;
+  const void* v;
+  const int32_t* pos;
+  const int32_t* block_table;
+  void* k_cache;
+  void* v_cache;
+  void* k_side;
+  uint32_t* status;
+  int32_t B, n_new, H_kv, max_pages, num_pages;
+  double inv_freq[64];
+};
+cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st);
+
+struct GatherOut {
+  int32_t* positions;
+  int64_t* phys_slot;
+  int32_t* key_rope_pos;
+  int32_t* q_rope_pos;
+  int8_t* segment;
+  int64_t capacity;
+  int64_t* count;
+};
+cudaError_t launch_gather(const DecodeArgs& a, int b, int t, const GatherOut& o, cudaStream_t st);
+
+}  // namespace da

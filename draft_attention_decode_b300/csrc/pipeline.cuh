@@ -1,0 +1,217 @@
+// Split-KV decode pipeline shared by the two compute engines.
+//
+// One persistent CTA per SM: warp 8 is the producer, warps 0..7 consume.
+// The CTA owns a contiguous stretch of the flat page line (see cta_begin in
+// common.cuh).  For every page on it the producer translates the block table,
+// then issues 2-D TMA loads of the page's K slab (from the rotated cache, or
+// from the un-rotated side cache for FOLD far memory) and V slab into a ring
+// of shared-memory stages, 128-byte swizzled.  The consumers run the online
+// softmax over each page; at the end of each piece they merge their eight
+// per-warp states and write one partial (m, l, o) per query row.
+#pragma once
+
+#include "common.cuh"
+
+namespace da {
+
+enum : int { kFirst = 1, kLast = 2, kValid = 4 };
+
+struct PageInfo {
+  int32_t seq;    // e * H_kv + h, e = 2 * b + range
+  int32_t lohi;   // first and one-past-last valid key in the page
+  int32_t flags;
+  int32_t pad;
+};
+
+// Shared-memory layout (host and device agree on it).
+struct Layout {
+  uint32_t stage_bytes, stages;
+  uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// engine 0: CUDA cores (merge rows per warp = rk, per-warp p buffer);
+// engine 1: mma (merge rows per warp = 16, no p buffer).
+__host__ __device__ inline Layout make_layout(int engine, int es, int d, int rk, int stages,
+                                              int batch) {
+  Layout L;
+  L.stage_bytes = 2u * (uint32_t)(d * es / kSwizzleRow) * kBoxBytes;
+  L.stages = stages;
+  uint32_t off = L.stage_bytes * stages;
+  int rm = engine == 0 ? rk : 16;
+  L.q_off = off;     off += align_up((uint32_t)rk * d * 4, 128);
+  L.mo_off = off;    off += align_up((uint32_t)kConsumerWarps * rm * d * 4, 128);
+  L.ml_off = off;    off += align_up((uint32_t)kConsumerWarps * rm * 8, 128);
+  L.p_off = off;     off += engine == 0 ? align_up((uint32_t)kConsumerWarps * 9 * rk * 4, 128) : 0;
+  L.info_off = off;  off += align_up((uint32_t)stages * sizeof(PageInfo), 128);
+  L.bar_off = off;   off += align_up((uint32_t)stages * 16, 128);
+  L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);
+  L.len_off = off;   off += align_up((uint32_t)batch * 4, 128);
+  L.pfx_off = off;   off += align_up((uint32_t)(2 * batch + 1) * 4, 128);
+  L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
+  return L;
+}
+
+struct Smem {
+  uint8_t* stage;       // stages x [K boxes | V boxes]
+  float* q;             // [rk][d] rotated, scaled queries of the current piece
+  float* mo;            // merge buffer for o (also the cos/sin table during prep)
+  float2* ml;           // merge buffer for (m, l)
+  float* p;             // CUDA-core engine: per-warp probabilities
+  PageInfo* info;
+  uint64_t* full;
+  uint64_t* empty;
+  double* invf;
+  int32_t* len;
+  int32_t* pfx;
+};
+
+__device__ inline Smem carve(uint8_t* raw, const Layout& L) {
+  uint32_t base = smem_u32(raw);
+  uint8_t* p = raw + (align_up(base, 1024) - base);
+  Smem s;
+  s.stage = p;
+  s.q = reinterpret_cast<float*>(p + L.q_off);
+  s.mo = reinterpret_cast<float*>(p + L.mo_off);
+  s.ml = reinterpret_cast<float2*>(p + L.ml_off);
+  s.p = reinterpret_cast<float*>(p + L.p_off);
+  s.info = reinterpret_cast<PageInfo*>(p + L.info_off);
+  s.full = reinterpret_cast<uint64_t*>(p + L.bar_off);
+  s.empty = s.full + L.stages;
+  s.invf = reinterpret_cast<double*>(p + L.invf_off);
+  s.len = reinterpret_cast<int32_t*>(p + L.len_off);
+  s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
+  return s;
+}
+
+// Prologue: context lengths and the page prefix over (b, range); CTA 0 also
+// publishes the prefix for the combine pass.  All threads take part.
+template <int D>
+__device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.inv_freq[i];
+  for (int b = tid; b < a.B; b += blockDim.x)
+    s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
+  if (tid == 0) {
+    for (uint32_t i = 0; i < L.stages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    int32_t carry = 0;
+    const int n = 2 * a.B;
+    for (int base = 0; base < n; base += 32) {
+      int e = base + lane;
+      int32_t v = 0;
+      if (e < n) {
+        Ranges r = mode_ranges(a.mode, s.len[e >> 1], a.W, a.n_sink);
+        v = (e & 1) ? range_pages(r.k0[1], r.k1[1]) : range_pages(r.k0[0], r.k1[0]);
+      }
+      int32_t inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (e < n) s.pfx[e] = carry + inc - v;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) s.pfx[n] = carry;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= 2 * a.B; i += blockDim.x) a.pfx[i] = s.pfx[i];
+}
+
+// Flat position -> (entry e = 2b + range, head h, page k inside the range).
+__device__ __forceinline__ void locate(const int32_t* pfx, int n_entries, int H, int64_t x,
+                                       int& e, int& h, int& k) {
+  int lo = 0, hi = n_entries - 1;  // largest e with pfx[e] * H <= x
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)pfx[mid] * H <= x) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  int64_t rel = x - (int64_t)pfx[e] * H;
+  int32_t n = pfx[e + 1] - pfx[e];
+  h = (int)(rel / n);
+  k = (int)(rel - (int64_t)h * n);
+}
+
+// The producer warp: block-table translation and TMA issue for the CTA's
+// stretch [xs, xe) of the page line.  ES = element bytes, NCB = 128-byte
+// column boxes per row (head_dim * ES / 128).
+template <int ES, int NCB>
+__device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
+                                int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
+                                const CUtensorMap* ms) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t pol = policy_evict_first();
+  if (lane == 0) {
+    prefetch_tmap(mk);
+    prefetch_tmap(mv);
+    if (a.mode == DA_MODE_FOLD) prefetch_tmap(ms);
+  }
+  const int n_entries = 2 * a.B;
+  uint32_t n = 0;
+  for (int64_t base = xs; base < xe; base += 32) {
+    const int64_t x = base + lane;
+    int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0;
+    if (x < xe) {
+      int e, k;
+      locate(s.pfx, n_entries, a.H_kv, x, e, h, k);
+      const int b = e >> 1, r = e & 1;
+      const Ranges rg = mode_ranges(a.mode, s.len[b], a.W, a.n_sink);
+      const int32_t k0 = r ? rg.k0[1] : rg.k0[0], k1 = r ? rg.k1[1] : rg.k1[0];
+      const int32_t P = k0 / kPage + k;
+      const int32_t pk0 = P * kPage;
+      const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;
+      const int32_t npg = s.pfx[e + 1] - s.pfx[e];
+      seq = e * a.H_kv + h;
+      lohi = lo | (hi << 16);
+      phys = phys_page(a.block_table, b, P, a.max_pages, a.num_pages, a.status);
+      flags = ((x == xs || k == 0) ? kFirst : 0) | ((x == xe - 1 || k == npg - 1) ? kLast : 0) |
+              (phys >= 0 ? kValid : 0);
+      far = range_is_far(a.mode, r) ? 1 : 0;
+    }
+    const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
+    for (int j = 0; j < cnt; ++j) {
+      const int32_t jseq = __shfl_sync(0xffffffffu, seq, j);
+      const int32_t jlohi = __shfl_sync(0xffffffffu, lohi, j);
+      const int32_t jflags = __shfl_sync(0xffffffffu, flags, j);
+      const int32_t jphys = __shfl_sync(0xffffffffu, phys, j);
+      const int32_t jfar = __shfl_sync(0xffffffffu, far, j);
+      const int32_t jh = __shfl_sync(0xffffffffu, h, j);
+      if (lane == 0) {
+        const uint32_t st = n % L.stages;
+        const uint32_t par = (n / L.stages) & 1u;
+        if (mbar_wait(&s.empty[st], par ^ 1u, a.status)) {
+          s.info[st] = PageInfo{jseq, jlohi, jflags, 0};
+          uint8_t* kdst = s.stage + st * L.stage_bytes;
+          uint8_t* vdst = kdst + NCB * kBoxBytes;
+          if (jflags & kValid) {
+            mbar_arrive_expect_tx(&s.full[st], L.stage_bytes);
+            const int32_t y = (jphys * a.H_kv + jh) * kPage;
+            const CUtensorMap* km = jfar ? ms : mk;
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+              tma_load_2d(kdst + cb * kBoxBytes, km, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+              tma_load_2d(vdst + cb * kBoxBytes, mv, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+            }
+          } else {
+            mbar_arrive(&s.full[st]);
+          }
+        }
+      }
+      ++n;
+      __syncwarp();
+    }
+  }
+}
+
+}  // namespace da

@@ -1,0 +1,201 @@
+/*
+ * draft_attn.h -- C ABI of the speculative-draft decode attention library.
+ *
+ * One data-parallel hot path: the attention of an MTP/NEXTN-style draft head
+ * over a long, paged KV cache, in four modes:
+ *
+ *   DA_MODE_FULL    every key of the context (the "full-context draft-KV tax").
+ *                   "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
+ *                   Million-Token Context", Abstract.
+ *   DA_MODE_WINDOW  the last W keys plus the first n_sink keys (attention
+ *                   sinks), so the draft's KV read stops growing with context.
+ *                   Same page, Abstract.
+ *   DA_MODE_FOLD    two softmaxes: the last W keys at their exact RoPE
+ *                   positions, and every older key as far memory, read from
+ *                   an unrotated side cache and rotated at one shared position
+ *                   P_far = L - W - 1, its logits sharpened by alpha; the two
+ *                   are mixed as (1 - far_mix) * local + far_mix * far
+ *                   (far_mix counts only when the far memory is non-empty).
+ *                   "FOLD: Position-Free Far Memory with Local Order for
+ *                   Long-Context Speculative Decoding", summary and abstract.
+ *   DA_MODE_SHARP   all keys, logits scaled by
+ *                   gamma = max(1, 1 + scale_slope * ln(|S| / scale_ref)),
+ *                   |S| the number of visible keys.  "SharpDraft: Accelerating
+ *                   Long-Context Speculative Decoding with Cardinality-Aware
+ *                   Query Scaling", Abstract.  (The page prints no formula;
+ *                   this fixed-slope form is the one the library implements.)
+ *
+ * RoPE is rotate-half (pairs (x_i, x_{i+d/2}), inv_freq_i = theta^(-2i/d)),
+ * after "RoFormer: Enhanced Transformer with Rotary Position Embedding", which
+ * the Windowed-MTP page lists under "Builds on"; the paged cache follows
+ * "Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention", listed there too.
+ *
+ * Layouts (row-major, element type = params.dtype for q, caches and out):
+ *   q            [batch][n_q][num_q_heads][head_dim]
+ *   out          [batch][n_q][num_q_heads][head_dim]
+ *   k_new, v_new [batch][n_new][num_kv_heads][head_dim]
+ *   k_cache, v_cache, k_side
+ *                [num_pages][num_kv_heads][page_size][head_dim]
+ *                k_cache holds keys rotated at their own positions, k_side
+ *                the same keys un-rotated (FOLD only), v_cache the values.
+ *   block_table  int32 [batch][max_pages_per_seq]; logical page j of sequence
+ *                b lives in physical page block_table[b][j].
+ *   ctx_lens     int32 [batch]: keys 0 .. ctx_lens[b]-1 are visible.
+ *   q_pos        int32 [batch][n_q]: RoPE position of each query token.
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: the caller allocates and owns every device buffer (q, caches,
+ * block table, lengths, out and the workspace).  The library owns only the
+ * opaque host-side plan and one 4-byte device status word per device.  All
+ * device work is asynchronous on the given stream; no call allocates device
+ * memory, and none synchronises except draft_attn_get_status.  Every pointer
+ * argument of the run/append/gather calls is a DEVICE pointer unless stated
+ * otherwise.
+ *
+ * Errors: every call returns DA_OK (0) or a negative DA_ERR_* code; nothing
+ * throws or aborts across this ABI.  Faults found on the device (an invalid
+ * block-table entry, a context length beyond the block table, a position out
+ * of range) never trap: the affected keys are skipped, a bit is set in the
+ * device status word, and draft_attn_get_status reports it.
+ */
+#ifndef DRAFT_ATTN_H
+#define DRAFT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DA_OK                        0
+#define DA_ERR_INVALID_ARG          -1  /* null pointer, bad size or parameter   */
+#define DA_ERR_UNSUPPORTED          -2  /* valid, but no kernel for this shape   */
+#define DA_ERR_WORKSPACE_TOO_SMALL  -3  /* workspace_bytes below the plan's need */
+#define DA_ERR_CUDA                 -4  /* a CUDA runtime call or launch failed  */
+#define DA_ERR_DEVICE_FAULT         -5  /* the device status word was non-zero   */
+
+/* Device status bits (draft_attn_get_status). */
+#define DA_STATUS_BAD_PAGE      1u  /* block-table entry outside [0, num_pages) */
+#define DA_STATUS_BAD_CTX_LEN   2u  /* ctx_len < 0 or > max_pages_per_seq*page  */
+#define DA_STATUS_BAD_POSITION  4u  /* append position beyond the block table   */
+#define DA_STATUS_WAIT_TIMEOUT  8u  /* a pipeline wait gave up (never expected) */
+
+typedef enum { DA_MODE_FULL = 0, DA_MODE_WINDOW = 1, DA_MODE_FOLD = 2, DA_MODE_SHARP = 3 } da_mode;
+typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP32 = 1 } da_dtype;
+
+/* Kernel engines (da_plan_info.engine). */
+#define DA_ENGINE_CUDA_CORE 0  /* <= 8 query rows per KV head: FP32 FMA path      */
+#define DA_ENGINE_MMA       1  /* 9..32 rows (draft trees): bf16 tensor-core path */
+
+typedef struct {
+  double  rope_theta;        /* RoPE base theta, > 0                               */
+  int32_t batch;             /* sequences, 1..1024                                 */
+  int32_t n_q;               /* query tokens per sequence (draft-tree width)       */
+  int32_t num_q_heads;       /* H_q, a multiple of num_kv_heads                    */
+  int32_t num_kv_heads;      /* H_kv                                               */
+  int32_t head_dim;          /* 64 or 128                                          */
+  int32_t page_size;         /* tokens per page; must be 64                        */
+  int32_t num_pages;         /* physical pages in each cache array                 */
+  int32_t max_pages_per_seq; /* row length of the block table                      */
+  int32_t dtype;             /* da_dtype of q, caches and out                      */
+  int32_t mode;              /* da_mode                                            */
+  int32_t window;            /* W (window, fold), >= 1                             */
+  int32_t n_sink;            /* sink tokens (window only), >= 0                    */
+  float   alpha;             /* FOLD far-logit concentration factor, > 0           */
+  float   far_mix;           /* FOLD far-memory weight lambda in [0, 1]            */
+  float   scale_slope;       /* SharpDraft slope beta, >= 0                        */
+  int32_t scale_ref;         /* SharpDraft reference key count N_ref, >= 1         */
+  float   softmax_scale;     /* logit scale c; 0 selects 1/sqrt(head_dim)          */
+  int32_t num_ctas;          /* persistent CTAs; 0 = one per SM (tests vary this)  */
+  int32_t reserved[6];       /* must be zero                                       */
+} da_params;
+
+typedef struct {
+  int32_t num_ctas;          /* grid of the split-KV kernel                        */
+  int32_t num_sms;
+  int32_t rows_per_kv_head;  /* (num_q_heads / num_kv_heads) * n_q                 */
+  int32_t kernel_rows;       /* rows the chosen kernel instance computes           */
+  int32_t engine;            /* DA_ENGINE_*                                        */
+  int32_t stages;            /* shared-memory pipeline depth (pages in flight)     */
+  int32_t smem_bytes;        /* dynamic shared memory of the split-KV kernel       */
+  int32_t reserved;
+  size_t  workspace_bytes;   /* what draft_attn_run needs                          */
+} da_plan_info;
+
+typedef struct da_plan_s* da_plan_t;
+
+/* Validates params on the host only (no CUDA call).  DA_OK, INVALID_ARG or
+ * UNSUPPORTED. */
+int draft_attn_check_params(const da_params* params);
+
+/* Builds an immutable plan for `params` on CUDA device `device` and returns,
+ * in *workspace_bytes, the size of the device workspace draft_attn_run needs.
+ * The plan fixes the grid (one CTA per SM unless params->num_ctas is set) and
+ * depends only on shapes, never on context lengths, so one plan serves every
+ * draft step and can be captured in a CUDA graph.  Thread-safe after
+ * creation.  Allocates no device memory. */
+int draft_attn_plan(const da_params* params, int device, da_plan_t* plan,
+                    size_t* workspace_bytes);
+
+int draft_attn_plan_info(da_plan_t plan, da_plan_info* info);
+
+void draft_attn_plan_destroy(da_plan_t plan);
+
+/* KV append + RoPE: for every (b, token, kv head) with pos[b][token] >= 0,
+ * writes RoPE(k_new, pos) to k_cache, k_new unchanged to k_side (when
+ * k_side != NULL) and v_new to v_cache, at page
+ * block_table[b][pos / page_size], slot pos % page_size.  Angles are formed
+ * in double precision, the rotation in FP32, the store rounds to nearest
+ * even.  A negative position skips the token (padding for ragged batches).
+ * batch may be below params.batch (pass a block_table offset by rows to
+ * append to a subset).  k_side is required when params.mode is FOLD.
+ * "FOLD ...", review (the unrotated side cache); Windowed-MTP, Abstract (the
+ * draft KV grows by one token per draft step). */
+int draft_attn_append_kv(da_plan_t plan, const void* k_new, const void* v_new,
+                         const int32_t* pos, int32_t batch, int32_t n_new,
+                         const int32_t* block_table, void* k_cache, void* v_cache,
+                         void* k_side, void* stream);
+
+/* Draft attention for every (b, query token, q head): the mode's key
+ * selection, split-KV flash-decoding over the pages (one online softmax, two
+ * for FOLD), then a combine pass that merges the splits and writes out.
+ * k_side may be NULL unless the mode is FOLD.  workspace: device scratch of at
+ * least the plan's workspace_bytes, 256-byte aligned, contents need not be
+ * initialised; calls that share a workspace must not overlap on the GPU. */
+int draft_attn_run(da_plan_t plan, const void* q, const int32_t* q_pos,
+                   const int32_t* ctx_lens, const int32_t* block_table,
+                   const void* k_cache, const void* v_cache, const void* k_side,
+                   void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test hook: the keys query token t of sequence b selects, computed by the
+ * same device routines as draft_attn_run.  Per key, ascending by position:
+ * positions (int32), phys_slot = physical_page * page_size + slot (int64, -1
+ * for an invalid block-table entry), key_rope_pos (the position the key is
+ * rotated at: its own, or P_far for FOLD far keys), q_rope_pos (the position
+ * the kernel rotates the query by: q_pos, or q_pos - P_far for far keys) and
+ * segment (0 main/local, 1 FOLD far).  At most `capacity` entries are written;
+ * *count (device int64) receives the total. */
+int draft_attn_debug_gather(da_plan_t plan, const int32_t* q_pos, const int32_t* ctx_lens,
+                            const int32_t* block_table, int32_t b, int32_t t,
+                            int32_t* positions, int64_t* phys_slot, int32_t* key_rope_pos,
+                            int32_t* q_rope_pos, int8_t* segment, int64_t capacity,
+                            int64_t* count, void* stream);
+
+/* Synchronises `stream`, reads and clears the plan device's status word.
+ * Returns DA_OK when it was zero, DA_ERR_DEVICE_FAULT otherwise; *bits (host
+ * pointer, may be NULL) receives the DA_STATUS_* bits. */
+int draft_attn_get_status(da_plan_t plan, void* stream, uint32_t* bits);
+
+const char* draft_attn_error_string(int code);
+
+/* ABI version (major * 100 + minor). */
+int draft_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DRAFT_ATTN_H */
