@@ -637,6 +637,25 @@ def all_workloads(dev, args, flush, dist, peak):
     return table
 
 
+def profile_loop(args):
+    """Runs the draft loop of one workload and mode eagerly `reps` times (no
+    timing): the command the ncu launch lists and captures are taken on."""
+    from draft_attention_decode_b300 import binding as B
+    dev = torch.device("cuda", 0)
+    wl = WL.WORKLOADS[args.workload]
+    if args.ctx:
+        wl = WL.resized(wl, args.ctx)
+    dl = DraftLoop(wl, dev, (args.profile_loop,))
+    for _ in range(args.reps):
+        dl.loop(args.profile_loop)
+    torch.cuda.synchronize()
+    code, bits = dl.plans[args.profile_loop].status()
+    dl.close()
+    if code != B.DA_OK:
+        raise SystemExit(f"device status {bits:#x}")
+    print(f"profile loop ok: {wl.name} ctx={wl.ctx[0]} mode={args.profile_loop} reps={args.reps}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -646,7 +665,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", default=None, help="also time every workload; write JSON here")
+    ap.add_argument("--profile-loop", default=None, metavar="MODE",
+                    help="run the draft loop of --workload in MODE --reps times, untimed")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--ctx", type=int, default=0, help="override the workload's context")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_loop:
+        profile_loop(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     dist = Dist()
