@@ -273,7 +273,8 @@ class DraftAttention:
         self.params = make_params(**kw)
         self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
         self.plan, self.workspace_bytes = draft_attn_plan(self.params, self.device.index or 0)
-        self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
+        # zero-filled once: the run keeps its page counters at zero between calls
+        self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=self.device)
         self.dtype = TORCH_DTYPES[self.params.dtype]
 
     def info(self) -> dict:

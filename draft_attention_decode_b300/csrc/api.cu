@@ -18,7 +18,7 @@ struct da_plan_s {
   int num_sms;
   int rows;
   da::Choice choice;
-  size_t pfx_bytes;
+  size_t cnt_bytes;
   size_t ws_bytes;
   uint32_t* status;
   double inv_freq[64];
@@ -181,9 +181,10 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   }
   if (pl->p.num_ctas == 0) pl->p.num_ctas = sms;  // one persistent CTA per SM
   const int d = params->head_dim;
-  pl->pfx_bytes = ((size_t)(2 * params->batch + 1) * 4 + 255) / 256 * 256;
+  // workspace: per-(b, kv head) page counters, then the partial (m, l, o) slots
+  pl->cnt_bytes = ((size_t)params->batch * params->num_kv_heads * 4 + 255) / 256 * 256;
   const size_t slots = (size_t)pl->p.num_ctas + (size_t)2 * params->batch * params->num_kv_heads;
-  pl->ws_bytes = pl->pfx_bytes + slots * (size_t)pl->choice.rk * (d + 2) * sizeof(float);
+  pl->ws_bytes = pl->cnt_bytes + slots * (size_t)pl->choice.rk * (d + 2) * sizeof(float);
   for (int i = 0; i < 64; ++i)
     pl->inv_freq[i] = i < d / 2 ? std::pow(params->rope_theta, -2.0 * i / d) : 0.0;
   const double c = params->softmax_scale > 0.f ? (double)params->softmax_scale
@@ -276,12 +277,10 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
   a.ctx_lens = ctx_lens;
   a.block_table = block_table;
   a.out = out;
-  a.pfx = static_cast<int32_t*>(workspace);
-  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->pfx_bytes);
+  a.cnt = static_cast<uint32_t*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->cnt_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, a, mk, mv, ms, st) != cudaSuccess)
-    return DA_ERR_CUDA;
-  if (da::launch_combine(pl->p.dtype, pl->p.head_dim, pl->choice.rk, a, st) != cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;
 }

@@ -1,4 +1,4 @@
-// KV append with RoPE, the split combine pass, and the debug-gather hook.
+// KV append with RoPE, and the debug-gather hook.
 #include "internal.h"
 
 namespace da {
@@ -66,96 +66,6 @@ cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st
   } else {
     if (d == 128) append_kernel<float, 128><<<grid, 256, 0, st>>>(a);
     else append_kernel<float, 64><<<grid, 256, 0, st>>>(a);
-  }
-  return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-// Combine: for each (b, kv head) and query row, log-sum-exp merge of the
-// pieces' partials of each softmax segment, then (FOLD) the far/local mix
-// (1 - lambda_eff) o_loc + lambda_eff o_far, lambda_eff = 0 when the far
-// memory is empty ("FOLD", abstract: separate control of the far memory's
-// total weight).  One warp per row, lane owns d/32 dimensions.  CTAs whose
-// page range is empty wrote no partial and are skipped.
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ DecodeArgs a, int RK) {
-  constexpr int DPL = D / 32;
-  const int b = blockIdx.x / a.H_kv, h = blockIdx.x - b * a.H_kv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t* pfx = a.pfx;
-  const int64_t TP = (int64_t)pfx[2 * a.B] * a.H_kv;
-  const int64_t slot_f = (int64_t)RK * (D + 2);
-  const bool fold = a.mode == DA_MODE_FOLD;
-  int64_t i0[2], i1[2], sq[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int e = 2 * b + rr;
-    const int32_t n = pfx[e + 1] - pfx[e];
-    sq[rr] = (int64_t)e * a.H_kv + h;
-    if (n == 0) {
-      i0[rr] = 0;
-      i1[rr] = -1;
-    } else {
-      const int64_t x0 = (int64_t)pfx[e] * a.H_kv + (int64_t)h * n;
-      i0[rr] = cta_of(x0, TP, a.n_cta);
-      i1[rr] = cta_of(x0 + n - 1, TP, a.n_cta);
-    }
-  }
-  const float lam = (fold && pfx[2 * b + 1] > pfx[2 * b]) ? a.far_mix : 0.f;
-  const int nseg = fold ? 2 : 1;
-  for (int r = warp; r < a.R; r += 8) {
-    float res[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) res[e] = 0.f;
-    for (int seg = 0; seg < nseg; ++seg) {
-      float M = -INFINITY;
-      for (int rr = 0; rr < 2; ++rr) {
-        if ((fold && rr == 0 ? 1 : 0) != seg) continue;
-        for (int64_t i = i0[rr] + lane; i <= i1[rr]; i += 32)
-          if (cta_begin(i, TP, a.n_cta) < cta_begin(i + 1, TP, a.n_cta))
-            M = fmaxf(M, a.part[(i + sq[rr]) * slot_f + r]);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      if (M == -INFINITY) continue;
-      float O[DPL], Ls = 0.f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) O[e] = 0.f;
-      for (int rr = 0; rr < 2; ++rr) {
-        if ((fold && rr == 0 ? 1 : 0) != seg) continue;
-        for (int64_t i = i0[rr]; i <= i1[rr]; ++i) {
-          if (cta_begin(i, TP, a.n_cta) == cta_begin(i + 1, TP, a.n_cta)) continue;
-          const float* base = a.part + (i + sq[rr]) * slot_f;
-          const float w = fast_exp2(base[r] - M);
-          Ls += w * base[RK + r];
-          const float* o = base + 2 * RK + (int64_t)r * D + lane * DPL;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) O[e] += w * o[e];
-        }
-      }
-      const float wseg = fold ? (seg == 1 ? lam : 1.f - lam) : 1.f;
-      if (Ls > 0.f) {
-        const float inv = wseg / Ls;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) res[e] += O[e] * inv;
-      }
-    }
-    const int t = r / a.G, j = r - t * a.G;
-    T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + lane * DPL;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) out[e] = from_f32<T>(res[e]);
-  }
-}
-
-cudaError_t launch_combine(int dtype, int d, int rk, const DecodeArgs& a, cudaStream_t st) {
-  const dim3 grid((unsigned)(a.B * a.H_kv));
-  if (dtype == DA_DTYPE_BF16) {
-    if (d == 128) combine_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(a, rk);
-    else combine_kernel<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(a, rk);
-  } else {
-    if (d == 128) combine_kernel<float, 128><<<grid, 256, 0, st>>>(a, rk);
-    else combine_kernel<float, 64><<<grid, 256, 0, st>>>(a, rk);
   }
   return cudaGetLastError();
 }

@@ -38,7 +38,8 @@ struct DecodeArgs {
   const int32_t* block_table;
   void* out;
   float* part;          // partial (m, l, o) slots
-  int32_t* pfx;         // per-(b, range) page prefix, written by CTA 0
+  uint32_t* cnt;        // per-(b, kv head) count of pages finished; the CTA that
+                        // completes the count merges and resets it to zero
   uint32_t* status;
   int32_t B, n_q, H_q, H_kv, G, R;  // R = G * n_q rows per KV head
   int32_t max_pages, num_pages;

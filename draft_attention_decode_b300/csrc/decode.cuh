@@ -302,6 +302,7 @@ struct CoreEngine {
         part[RK + r] = l;
       }
     }
+    __threadfence();
     named_barrier(1, kConsumerThreads);
     reset();
   }
@@ -506,10 +507,131 @@ struct MmaEngine {
         part[RK + r] = lsum;
       }
     }
+    __threadfence();
     named_barrier(1, kConsumerThreads);
     reset();
   }
 };
+
+// ---------------------------------------------------------------------------
+// Split merge, fused into the decode kernel.  Every piece adds its page count
+// to cnt[b, h]; the CTA whose addition completes the (b, h) total (both ranges)
+// is the last writer, and merges all pieces' partials: per softmax segment a
+// log-sum-exp merge, then for FOLD the far/local mix
+// (1 - lambda_eff) o_loc + lambda_eff o_far with lambda_eff = 0 when the far
+// memory is empty ("FOLD", abstract: the far memory's total weight is
+// controlled separately).  No CTA ever waits for another.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t seq_pages(const int32_t* pfx, int b) {
+  return pfx[2 * b + 2] - pfx[2 * b];
+}
+
+template <typename T, int D, int RK>
+__device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b, int h) {
+  const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
+  const int64_t n_cta = a.n_cta;
+  const bool dense = TP >= n_cta;            // then no CTA's stretch is empty
+  const int64_t slot_f = (int64_t)RK * (D + 2);
+  const bool fold = a.mode == DA_MODE_FOLD;
+  int64_t i0[2], i1[2], sq[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int e = 2 * b + rr;
+    const int32_t n = s.pfx[e + 1] - s.pfx[e];
+    sq[rr] = (int64_t)e * a.H_kv + h;
+    if (n == 0) {
+      i0[rr] = 0;
+      i1[rr] = -1;
+    } else {
+      const int64_t x0 = (int64_t)s.pfx[e] * a.H_kv + (int64_t)h * n;
+      i0[rr] = cta_of(x0, TP, n_cta);
+      i1[rr] = cta_of(x0 + n - 1, TP, n_cta);
+    }
+  }
+  const float lam = (fold && s.pfx[2 * b + 1] > s.pfx[2 * b]) ? a.far_mix : 0.f;
+  for (int idx = threadIdx.x; idx < a.R * D; idx += kConsumerThreads) {
+    const int r = idx / D, dim = idx - r * D;
+    float M[2] = {-INFINITY, -INFINITY}, Ls[2] = {0.f, 0.f}, O[2] = {0.f, 0.f};
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int sg = (fold && rr == 0) ? 1 : 0;
+      for (int64_t i = i0[rr]; i <= i1[rr]; i += 4) {
+        float mm[4], ll[4], oo[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t ii = i + u;
+          mm[u] = -INFINITY;
+          ll[u] = 0.f;
+          oo[u] = 0.f;
+          if (ii <= i1[rr] &&
+              (dense || cta_begin(ii, TP, n_cta) < cta_begin(ii + 1, TP, n_cta))) {
+            const float* base = a.part + (ii + sq[rr]) * slot_f;
+            mm[u] = __ldcg(base + r);
+            ll[u] = __ldcg(base + RK + r);
+            oo[u] = __ldcg(base + 2 * RK + r * D + dim);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (mm[u] == -INFINITY) continue;
+          const float mn = fmaxf(M[sg], mm[u]);
+          const float so = fast_exp2(M[sg] - mn), sn = fast_exp2(mm[u] - mn);
+          Ls[sg] = Ls[sg] * so + ll[u] * sn;
+          O[sg] = O[sg] * so + oo[u] * sn;
+          M[sg] = mn;
+        }
+      }
+    }
+    float res;
+    if (fold) {
+      res = (Ls[0] > 0.f ? (1.f - lam) * O[0] / Ls[0] : 0.f) +
+            (Ls[1] > 0.f ? lam * O[1] / Ls[1] : 0.f);
+    } else {
+      res = Ls[0] > 0.f ? O[0] / Ls[0] : 0.f;
+    }
+    const int t = r / a.G, j = r - t * a.G;
+    T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + dim;
+    *out = from_f32<T>(res);
+  }
+}
+
+// After a piece's partial is written: take the ticket, merge when last.
+template <typename T, int D, int RK>
+__device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pages) {
+  const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1;
+  uint32_t* c = a.cnt + (int64_t)b * a.H_kv + h;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t total = (uint32_t)seq_pages(s.pfx, b);
+    const uint32_t old = atomicAdd(c, pages);
+    const int last = old + pages == total;
+    if (last) {
+      __threadfence();
+      atomicExch(c, 0u);  // every piece of (b, h) has arrived: ready for the next call
+    }
+    s.flag[0] = last;
+  }
+  named_barrier(1, kConsumerThreads);
+  const int last = s.flag[0];
+  named_barrier(1, kConsumerThreads);
+  if (last) merge_sequence<T, D, RK>(a, s, b, h);
+}
+
+// Rows of (b, h) whose selection is empty get a zero output (nobody merges
+// them); CTA (b * H_kv + h) mod n_cta writes it.
+template <typename T, int D>
+__device__ inline void zero_empty(const DecodeArgs& a, const Smem& s) {
+  for (int bh = blockIdx.x; bh < a.B * a.H_kv; bh += a.n_cta) {
+    const int b = bh / a.H_kv, h = bh - b * a.H_kv;
+    if (seq_pages(s.pfx, b) != 0) continue;
+    for (int idx = threadIdx.x; idx < a.R * D; idx += kConsumerThreads) {
+      const int r = idx / D, dim = idx - r * D;
+      const int t = r / a.G, j = r - t * a.G;
+      static_cast<T*>(a.out)[((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + dim] =
+          from_f32<T>(0.f);
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // The kernel.
@@ -537,14 +659,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_inc<kConsumerRegs>();
   Engine eng;
   eng.init();
+  zero_empty<T, D>(a, s);
+  // The first piece's queries are prepared while its first pages load.
+  if (xs < xe) {
+    int e, h, k;
+    locate(s.pfx, 2 * a.B, a.H_kv, xs, e, h, k);
+    prep_queries<T, D, RK>(a, s, e * a.H_kv + h);
+    eng.begin(s);
+  }
   const uint32_t base = smem_u32(s.stage);
-  uint32_t n = 0;
+  uint32_t n = 0, pages = 0;
   for (int64_t x = xs; x < xe; ++x, ++n) {
     const uint32_t st = n % L.stages;
     const uint32_t par = (n / L.stages) & 1u;
     if (!mbar_wait(&s.full[st], par, a.status)) break;
     const PageInfo inf = s.info[st];
-    if (inf.flags & kFirst) {
+    if ((inf.flags & kFirst) && x != xs) {
       prep_queries<T, D, RK>(a, s, inf.seq);
       eng.begin(s);
     }
@@ -552,9 +682,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kb = base + st * L.stage_bytes;
       eng.page(s, kb, kb + NCB * kBoxBytes, inf.lohi & 0xffff, inf.lohi >> 16);
     }
+    ++pages;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
-    if (inf.flags & kLast) eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
+    if (inf.flags & kLast) {
+      eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
+      ticket<T, D, RK>(a, s, inf.seq, pages);
+      pages = 0;
+    }
   }
 }
 

@@ -21,7 +21,6 @@ cudaError_t prepare_decode(const Choice& c, int dtype, int d);
 cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,
                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
                           cudaStream_t st);
-cudaError_t launch_combine(int dtype, int d, int rk, const DecodeArgs& a, cudaStream_t st);
 
 struct AppendArgs {
   const void* k;

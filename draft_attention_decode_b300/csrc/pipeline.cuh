@@ -26,7 +26,8 @@ struct PageInfo {
 // Shared-memory layout (host and device agree on it).
 struct Layout {
   uint32_t stage_bytes, stages;
-  uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, total;
+  uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, flag_off,
+      total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -49,6 +50,7 @@ __host__ __device__ inline Layout make_layout(int engine, int es, int d, int rk,
   L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);
   L.len_off = off;   off += align_up((uint32_t)batch * 4, 128);
   L.pfx_off = off;   off += align_up((uint32_t)(2 * batch + 1) * 4, 128);
+  L.flag_off = off;  off += 128;
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
 }
@@ -65,6 +67,7 @@ struct Smem {
   double* invf;
   int32_t* len;
   int32_t* pfx;
+  int32_t* flag;        // broadcast of the merge ticket
 };
 
 __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
@@ -82,11 +85,12 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.invf = reinterpret_cast<double*>(p + L.invf_off);
   s.len = reinterpret_cast<int32_t*>(p + L.len_off);
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
+  s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
   return s;
 }
 
-// Prologue: context lengths and the page prefix over (b, range); CTA 0 also
-// publishes the prefix for the combine pass.  All threads take part.
+// Prologue: context lengths and the page prefix over (b, range), computed
+// identically by every CTA.  All threads take part.
 template <int D>
 __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
@@ -124,8 +128,6 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
     if (lane == 0) s.pfx[n] = carry;
   }
   __syncthreads();
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= 2 * a.B; i += blockDim.x) a.pfx[i] = s.pfx[i];
 }
 
 // Flat position -> (entry e = 2b + range, head h, page k inside the range).

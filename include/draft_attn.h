@@ -161,10 +161,15 @@ int draft_attn_append_kv(da_plan_t plan, const void* k_new, const void* v_new,
 
 /* Draft attention for every (b, query token, q head): the mode's key
  * selection, split-KV flash-decoding over the pages (one online softmax, two
- * for FOLD), then a combine pass that merges the splits and writes out.
- * k_side may be NULL unless the mode is FOLD.  workspace: device scratch of at
- * least the plan's workspace_bytes, 256-byte aligned, contents need not be
- * initialised; calls that share a workspace must not overlap on the GPU. */
+ * for FOLD) in one persistent kernel, whose last CTA to finish a (sequence,
+ * KV head) merges that pair's splits and writes out.  k_side may be NULL
+ * unless the mode is FOLD.
+ * workspace: device scratch of at least the plan's workspace_bytes, 256-byte
+ * aligned.  It holds per-(sequence, KV head) page counters that must be zero
+ * when a call starts: zero-fill the buffer once before its first use (every
+ * call leaves the counters at zero again), and once more after a call that
+ * reported DA_STATUS_WAIT_TIMEOUT.  Calls that share a workspace must not
+ * overlap on the GPU. */
 int draft_attn_run(da_plan_t plan, const void* q, const int32_t* q_pos,
                    const int32_t* ctx_lens, const int32_t* block_table,
                    const void* k_cache, const void* v_cache, const void* k_side,
