@@ -135,7 +135,8 @@ int draft_attn_check_params(const da_params* p) {
   if (!(p->rope_theta > 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return DA_ERR_INVALID_ARG;
   if (p->num_ctas < 0 || p->num_ctas > 65535) return DA_ERR_INVALID_ARG;
-  for (int i = 0; i < 6; ++i)
+  if (p->engine < 0 || p->engine > 2) return DA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
     if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;
@@ -152,7 +153,8 @@ int draft_attn_check_params(const da_params* p) {
   }
   const int64_t rows = (int64_t)(p->num_q_heads / p->num_kv_heads) * p->n_q;
   if (rows > 32) return DA_ERR_UNSUPPORTED;
-  if (rows > 8 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
+  if (rows > 8 && (p->dtype != DA_DTYPE_BF16 || p->engine == 1)) return DA_ERR_UNSUPPORTED;
+  if (p->engine == 2 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -174,8 +176,8 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   pl->device = device;
   pl->num_sms = sms;
   pl->rows = (params->num_q_heads / params->num_kv_heads) * params->n_q;
-  if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, max_smem,
-                         &pl->choice)) {
+  if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, params->engine,
+                         max_smem, &pl->choice)) {
     delete pl;
     return DA_ERR_UNSUPPORTED;
   }
@@ -184,7 +186,7 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   // workspace: per-(b, kv head) page counters, then the partial (m, l, o) slots
   pl->cnt_bytes = ((size_t)params->batch * params->num_kv_heads * 4 + 255) / 256 * 256;
   const size_t slots = (size_t)pl->p.num_ctas + (size_t)2 * params->batch * params->num_kv_heads;
-  pl->ws_bytes = pl->cnt_bytes + slots * (size_t)pl->choice.rk * (d + 2) * sizeof(float);
+  pl->ws_bytes = pl->cnt_bytes + slots * (size_t)da::slot_floats(pl->choice.rk, d) * sizeof(float);
   for (int i = 0; i < 64; ++i)
     pl->inv_freq[i] = i < d / 2 ? std::pow(params->rope_theta, -2.0 * i / d) : 0.0;
   const double c = params->softmax_scale > 0.f ? (double)params->softmax_scale

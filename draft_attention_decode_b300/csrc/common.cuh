@@ -51,6 +51,11 @@ struct DecodeArgs {
   double inv_freq[64];  // theta^(-2i/d), i < d/2
 };
 
+// Partial slot of one piece: m[RK], l[RK], padding to a 16-byte boundary,
+// then o[RK][D] (16-byte aligned, so the merge reads it as float4).
+__host__ __device__ constexpr int slot_o_off(int rk) { return (2 * rk + 3) / 4 * 4; }
+__host__ __device__ constexpr int slot_floats(int rk, int d) { return slot_o_off(rk) + rk * d; }
+
 // ---------------------------------------------------------------------------
 // Mode -> key ranges.  Two half-open ranges per sequence, in ascending
 // position order; range 0 of FOLD is the far memory, everything else belongs

@@ -1,19 +1,28 @@
 // Instantiations and dispatch of the split-KV decode kernel.
+#include <type_traits>
+
 #include "decode.cuh"
 #include "internal.h"
 
 namespace da {
 
-bool choose_kernel(int dtype, int d, int rows, int batch, int max_smem, Choice* c) {
+bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int max_smem,
+                   Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
-  if (rows <= 8) {
+  // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
+  // from 5 on, QK^T and PV are dense enough for an n8 tensor-core tile
+  // (bf16 only).  engine_hint 1/2 forces the CUDA cores / tensor cores.
+  bool mma = dtype == DA_DTYPE_BF16 && rows > 4;
+  if (engine_hint == 1) mma = false;
+  if (engine_hint == 2) mma = true;
+  if (mma) {
+    if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
+    c->engine = DA_ENGINE_MMA;
+    c->rk = rows <= 8 ? 8 : rows <= 16 ? 16 : 32;
+  } else {
+    if (rows > 8) return false;
     c->engine = DA_ENGINE_CUDA_CORE;
     c->rk = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
-  } else if (rows <= 32 && dtype == DA_DTYPE_BF16) {
-    c->engine = DA_ENGINE_MMA;
-    c->rk = 32;
-  } else {
-    return false;
   }
   for (int s = 4; s >= 2; --s) {
     const Layout L = make_layout(c->engine, es, d, c->rk, s, batch);
@@ -32,12 +41,18 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
   using bf = __nv_bfloat16;
   if (c.engine == DA_ENGINE_MMA) {
     if (dtype != DA_DTYPE_BF16) return cudaErrorInvalidValue;
-    if (d == 128) return f(decode_kernel<bf, 128, MmaEngine<128>, 1, 32>);
-    return f(decode_kernel<bf, 64, MmaEngine<64>, 1, 32>);
+#define DA_MMA(D, NT, SPLIT, RK) \
+  if (d == D && c.rk == RK) return f(decode_kernel<bf, D, MmaEngine<D, NT, SPLIT>, 1, RK>);
+    DA_MMA(128, 1, true, 8) DA_MMA(128, 2, true, 16) DA_MMA(128, 2, false, 32)
+    DA_MMA(64, 1, true, 8) DA_MMA(64, 2, true, 16) DA_MMA(64, 2, false, 32)
+#undef DA_MMA
+    return cudaErrorInvalidValue;
   }
 #define DA_CORE(T, D, RK) \
   if (dtype == (sizeof(T) == 2 ? DA_DTYPE_BF16 : DA_DTYPE_FP32) && d == D && c.rk == RK) \
-    return f(decode_kernel<T, D, CoreEngine<T, D, RK>, 0, RK>);
+    return f(decode_kernel<T, D, \
+                           std::conditional_t<(RK <= 4), CoreEngine<T, D, RK>, CoreEngineWide<T, D, RK>>, \
+                           0, RK>);
   DA_CORE(bf, 128, 1) DA_CORE(bf, 128, 2) DA_CORE(bf, 128, 4) DA_CORE(bf, 128, 8)
   DA_CORE(bf, 64, 1) DA_CORE(bf, 64, 2) DA_CORE(bf, 64, 4) DA_CORE(bf, 64, 8)
   DA_CORE(float, 128, 1) DA_CORE(float, 128, 2) DA_CORE(float, 128, 4) DA_CORE(float, 128, 8)

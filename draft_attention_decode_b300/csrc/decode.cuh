@@ -1,14 +1,14 @@
 // Split-KV decode kernel: the pipeline of pipeline.cuh driving one of two
 // compute engines.
 //
-//  * CoreEngine (<= 8 query rows per KV head: one draft token, GQA groups up
-//    to 8).  QK^T and PV on the FP32 pipes with packed two-wide FMAs; no
+//  * CoreEngine (<= 4 query rows per KV head by default, <= 8 on request:
+//    one draft token over a small GQA group).  QK^T and PV on the FP32 pipes with packed two-wide FMAs; no
 //    tensor cores, since with this few rows the page read, not arithmetic, is
 //    the bound.  Each warp owns 8 of the page's 64 keys: for QK^T eight lanes
 //    share one key (16 dimensions each at d = 128) and a reduce-scatter
 //    butterfly leaves lane i with row i's score; for PV every lane owns d/32
 //    dimensions of all rows.
-//  * MmaEngine (9..32 rows: draft trees of several tokens).  QK^T and PV as
+//  * MmaEngine (5..32 rows: a GQA group of 8, or draft trees).  QK^T and PV as
 //    bf16 m16n8k16 tensor-core MMAs with FP32 accumulation, keys on the M side
 //    of QK^T (S^T = K Q^T) so that 8-row query tiles need no padding, P^T
 //    moved into the PV operand layout with movmatrix.
@@ -132,10 +132,214 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core engine.
+// CUDA-core engine, 1..4 rows.  Warp w owns keys 8w .. 8w+7 of the page; the
+// eight lanes of key group kg (lane bits 3, 4) share key 8w + kg (+4 on the
+// second pass) and lane ds (bits 0..2) owns D/8 of its dimensions, read as
+// 16-byte chunks whose order is rotated by ds (no bank conflicts under the
+// 128-byte swizzle).  QK^T: per-lane partial dots, reduce-scatter so that lane
+// ds holds row ds's score.  PV runs in the same layout: the row
+// probabilities of the lane's key come back by shuffle, the lane accumulates
+// p * V over its own dimensions, and the four key groups are summed only at
+// the end of a piece.  The running maximum is raised lazily (only when a
+// score exceeds it by more than 2^8): the result is exact for any reference
+// value, and the accumulators are rescaled only a handful of times.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int RK>
 struct CoreEngine {
+  static constexpr int ES = sizeof(T);
+  static constexpr int DQ = D / 8;            // dimensions per lane
+  static constexpr int NCH = DQ * ES / 16;    // 16-byte chunks per lane (1, 2 or 4)
+  static constexpr int EPC = 16 / ES;         // elements per chunk
+  static constexpr float kLazy = 8.f;         // log2 headroom before a rescale
+  static_assert(RK == 1 || RK == 2 || RK == 4, "rows");
+  static_assert(NCH >= 1 && (NCH & (NCH - 1)) == 0, "chunks");
+
+  float2 q2[RK][DQ / 2];
+  float2 o2[RK][DQ / 2];
+  float m_run, l_run;    // row ds & (RK-1): reference maximum, partial sum
+  uint32_t off[2][NCH];  // swizzled byte offsets of the lane's chunks, pass 0/1
+  int lane, warp, kg, ds;
+
+  __device__ __forceinline__ void init() {
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    kg = lane >> 3;
+    ds = lane & 7;
+#pragma unroll
+    for (int it = 0; it < 2; ++it)
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
+        off[it][i] = swz_addr(0u, warp * 8 + kg + 4 * it, (ds * NCH + ic) * 16);
+      }
+  }
+
+  __device__ __forceinline__ bool owns(uint32_t) const { return true; }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int r = 0; r < RK; ++r)
+#pragma unroll
+      for (int e = 0; e < DQ / 2; ++e) o2[r][e] = make_float2(0.f, 0.f);
+    m_run = -INFINITY;
+    l_run = 0.f;
+  }
+
+  // Dimension of element e of chunk slot i of this lane.
+  __device__ __forceinline__ int dim_of(int i, int e) const {
+    const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
+    return (ds * NCH + ic) * EPC + e;
+  }
+
+  __device__ __forceinline__ void begin(const Smem& s) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i)
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          const int d0 = dim_of(i, 2 * e);
+          q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0], s.q[r * D + d0 + 1]);
+        }
+    reset();
+  }
+
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+    float sc[2];
+    bool ok[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int key = warp * 8 + kg + 4 * it;
+      ok[it] = key >= lo && key < hi;
+      float2 acc[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) acc[r] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        float f[EPC];
+        Chunk<T>::load(kbase + off[it][i], f);
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
+#pragma unroll
+          for (int r = 0; r < RK; ++r) acc[r] = ffma2(q2[r][i * (EPC / 2) + e], kk, acc[r]);
+        }
+      }
+      float v[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
+      const float sr = reduce_scatter8<RK>(v, ds);
+      sc[it] = ok[it] ? sr : -INFINITY;
+    }
+    // Row maximum over the warp's 8 keys (lanes with the same ds).
+    float mx = fmaxf(sc[0], sc[1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const bool raise = mx > m_run + kLazy;
+    if (__any_sync(0xffffffffu, raise)) {
+      const float m_new = raise ? mx : m_run;
+      const float al = raise ? fast_exp2(m_run - m_new) : 1.f;   // 0 when m_run = -inf
+      l_run *= al;
+      m_run = m_new;
+#pragma unroll
+      for (int r = 0; r < RK; ++r) {
+        const float ar = __shfl_sync(0xffffffffu, al, (lane & ~7) | r);
+#pragma unroll
+        for (int e = 0; e < DQ / 2; ++e) {
+          o2[r][e].x *= ar;
+          o2[r][e].y *= ar;
+        }
+      }
+    }
+    float p[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) p[it] = sc[it] > -INFINITY ? fast_exp2(sc[it] - m_run) : 0.f;
+    l_run += p[0] + p[1];
+    // PV in the QK^T layout.
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      float pr[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) pr[r] = __shfl_sync(0xffffffffu, p[it], (lane & ~7) | r);
+      if (ok[it]) {   // keys outside [lo, hi) may hold anything, NaN included
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          float f[EPC];
+          Chunk<T>::load(vbase + off[it][i], f);
+#pragma unroll
+          for (int e = 0; e < EPC / 2; ++e) {
+            const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
+#pragma unroll
+            for (int r = 0; r < RK; ++r)
+              o2[r][i * (EPC / 2) + e] = ffma2(make_float2(pr[r], pr[r]), vv, o2[r][i * (EPC / 2) + e]);
+          }
+        }
+      }
+    }
+  }
+
+  // Sum the four key groups, merge the eight warps, write the piece's partial.
+  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+    float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
+#pragma unroll
+    for (int r = 0; r < RK; ++r)
+#pragma unroll
+      for (int e = 0; e < DQ / 2; ++e) {
+        float2 v = o2[r][e];
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+        o2[r][e] = v;
+      }
+    if (kg == 0) {
+#pragma unroll
+      for (int i = 0; i < NCH; ++i)
+#pragma unroll
+        for (int r = 0; r < RK; ++r)
+#pragma unroll
+          for (int e = 0; e < EPC / 2; ++e)
+            *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + dim_of(i, 2 * e)) =
+                o2[r][i * (EPC / 2) + e];
+    }
+    named_barrier(1, kConsumerThreads);
+    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
+    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+      const int r = idx / D, dim = idx - r * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
+      float o = 0.f, l = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float2 ml = s.ml[w * RK + r];
+          const float sc = fast_exp2(ml.x - M);
+          o += sc * s.mo[(w * RK + r) * D + dim];
+          l += sc * ml.y;
+        }
+      }
+      part[slot_o_off(RK) + r * D + dim] = o;
+      if (dim == 0) {
+        part[r] = M;
+        part[RK + r] = l;
+      }
+    }
+    __threadfence();
+    named_barrier(1, kConsumerThreads);
+    reset();
+  }
+};
+
+// ---------------------------------------------------------------------------
+// CUDA-core engine for 5..8 rows (fp32 caches, or on request).  QK^T as in
+// CoreEngine; PV with every lane owning d/32 dimensions of all rows and the
+// probabilities passed through shared memory.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int RK>
+struct CoreEngineWide {
   static constexpr int ES = sizeof(T);
   static constexpr int DQ = D / 8;            // QK dims per lane
   static constexpr int NCH = DQ * ES / 16;    // 16-byte chunks per lane (1, 2 or 4)
@@ -155,6 +359,8 @@ struct CoreEngine {
     kg = lane >> 3;
     ds = lane & 7;
   }
+
+  __device__ __forceinline__ bool owns(uint32_t) const { return true; }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -280,7 +486,7 @@ struct CoreEngine {
       for (int e = 0; e < DPL / 2; ++e)
         *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + lane * DPL + 2 * e) = o2[r][e];
     named_barrier(1, kConsumerThreads);
-    float* part = a.part + slot * (int64_t)(RK * (D + 2));
+    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
     for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
       const int r = idx / D, dim = idx - r * D;
       float M = -INFINITY;
@@ -296,7 +502,7 @@ struct CoreEngine {
           l += sc * ml.y;
         }
       }
-      part[2 * RK + r * D + dim] = o;
+      part[slot_o_off(RK) + r * D + dim] = o;
       if (dim == 0) {
         part[r] = M;
         part[RK + r] = l;
@@ -338,43 +544,57 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+// NT n8 tiles of query rows per warp.  Warp w takes key block kb = w & 3 (16
+// of the page's 64 keys) and belongs to group grp = w >> 2.
+//  * SPLIT_PAGES: the two groups take alternate pages and each holds all
+//    RK = 8 NT rows (8 or 16 rows: one query token with a GQA group of 8, or
+//    a small draft tree).
+//  * otherwise: both groups work on every page, on row halves of
+//    RK = 16 NT rows (32 rows: an 8-token draft tree over a GQA group of 4).
+template <int D, int NT, bool SPLIT_PAGES>
 struct MmaEngine {
-  static constexpr int RK = 32;
+  static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
+  static constexpr int RW = 8 * NT;   // rows per warp
   static constexpr int KS = D / 16;   // k-steps of QK^T, m-tiles of PV
-  uint32_t qf[KS][2][2];
-  float O[KS][2][4];
-  float m[2][2], l[2][2];
-  int lane, warp, kb, rg, g, t;
+  static_assert(RW <= 16, "merge buffer holds 16 rows per warp");
+  uint32_t qf[KS][NT][2];
+  float O[KS][NT][4];
+  float m[NT][2], l[NT][2];
+  int lane, warp, kb, grp, g, t;
 
   __device__ __forceinline__ void init() {
     lane = threadIdx.x & 31;
     warp = threadIdx.x >> 5;
     kb = warp & 3;
-    rg = warp >> 2;
+    grp = warp >> 2;
     g = lane >> 2;
     t = lane & 3;
+  }
+
+  __device__ __forceinline__ bool owns(uint32_t n) const {
+    return SPLIT_PAGES ? (int)(n & 1u) == grp : true;
   }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) O[mt][nt][c] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) { m[nt][cc] = -INFINITY; l[nt][cc] = 0.f; }
   }
 
   __device__ __forceinline__ void begin(const Smem& s) {
+    const int row0 = SPLIT_PAGES ? 0 : grp * RW;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float* qr = s.q + (16 * rg + 8 * nt + g) * D + 16 * ks + 2 * t;
+      for (int nt = 0; nt < NT; ++nt) {
+        const float* qr = s.q + (row0 + 8 * nt + g) * D + 16 * ks + 2 * t;
         qf[ks][nt][0] = pack_bf16(qr[0], qr[1]);
         qf[ks][nt][1] = pack_bf16(qr[8], qr[9]);
       }
@@ -384,9 +604,9 @@ struct MmaEngine {
   __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
     const int key0 = 16 * kb;
     if (hi <= key0 || lo >= key0 + 16) return;
-    float S[2][4];
+    float S[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) S[nt][c] = 0.f;
     const int krow = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -394,16 +614,16 @@ struct MmaEngine {
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(swz_addr(kbase, krow, (16 * ks + (lane >> 4) * 8) * 2), a);
-      mma_bf16(S[0], a, qf[ks][0][0], qf[ks][0][1]);
-      mma_bf16(S[1], a, qf[ks][1][0], qf[ks][1][1]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
     }
     const bool oka = (key0 + g >= lo) && (key0 + g < hi);
     const bool okb = (key0 + g + 8 >= lo) && (key0 + g + 8 < hi);
-    float alpha[2][2];
-    uint32_t bp[2][2];
+    float alpha[NT][2];
+    uint32_t bp[NT][2];
     bool all_one = true;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
       float P[4];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -434,7 +654,7 @@ struct MmaEngine {
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
           O[mt][nt][0] *= alpha[nt][0];
           O[mt][nt][1] *= alpha[nt][1];
           O[mt][nt][2] *= alpha[nt][0];
@@ -455,14 +675,15 @@ struct MmaEngine {
       uint32_t a[4];
       ldsm_x4_t(swz_addr(vbase, vrow, (16 * mt + ((lane >> 3) & 1) * 8) * 2), a);
       a[0] &= mask01; a[1] &= mask01; a[2] &= mask23; a[3] &= mask23;
-      mma_bf16(O[mt][0], a, bp[0][0], bp[0][1]);
-      mma_bf16(O[mt][1], a, bp[1][0], bp[1][1]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(O[mt][nt], a, bp[nt][0], bp[nt][1]);
     }
   }
 
+  // Merge the warps holding each row and write the piece's partial to `slot`.
   __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         float lt = l[nt][cc];
@@ -474,7 +695,7 @@ struct MmaEngine {
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         const int lr = 8 * nt + 2 * t;
         float* base = s.mo + (warp * 16) * D + 16 * mt + g;
         base[lr * D] = O[mt][nt][0];
@@ -483,25 +704,27 @@ struct MmaEngine {
         base[(lr + 1) * D + 8] = O[mt][nt][3];
       }
     named_barrier(1, kConsumerThreads);
-    float* part = a.part + slot * (int64_t)(RK * (D + 2));
+    constexpr int NW = SPLIT_PAGES ? 8 : 4;   // warps holding one row
+    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
     for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
       const int r = idx / D, dim = idx - r * D;
-      const int grp = r >> 4, lr = r & 15;
+      const int w0 = SPLIT_PAGES ? 0 : (r / RW) * 4;
+      const int lr = SPLIT_PAGES ? r : r % RW;
       float M = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) M = fmaxf(M, s.ml[(grp * 4 + k) * 16 + lr].x);
+      for (int k = 0; k < NW; ++k) M = fmaxf(M, s.ml[(w0 + k) * 16 + lr].x);
       float o = 0.f, lsum = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int w = grp * 4 + k;
+        for (int k = 0; k < NW; ++k) {
+          const int w = w0 + k;
           const float2 ml = s.ml[w * 16 + lr];
           const float sc = fast_exp2(ml.x - M);
           o += sc * s.mo[(w * 16 + lr) * D + dim];
           lsum += sc * ml.y;
         }
       }
-      part[2 * RK + r * D + dim] = o;
+      part[slot_o_off(RK) + r * D + dim] = o;
       if (dim == 0) {
         part[r] = M;
         part[RK + r] = lsum;
@@ -526,12 +749,93 @@ __device__ __forceinline__ int32_t seq_pages(const int32_t* pfx, int b) {
   return pfx[2 * b + 2] - pfx[2 * b];
 }
 
+// Running log-sum-exp merge state of one row and four dimensions.
+struct MergeState {
+  float m, l, o[4];
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    l = 0.f;
+    o[0] = o[1] = o[2] = o[3] = 0.f;
+  }
+  __device__ __forceinline__ void add(float pm, float pl, const float4& po) {
+    if (pm == -INFINITY) return;
+    const float mn = fmaxf(m, pm);
+    const float so = fast_exp2(m - mn), sn = fast_exp2(pm - mn);   // so = 0 when m = -inf
+    l = l * so + pl * sn;
+    o[0] = o[0] * so + po.x * sn;
+    o[1] = o[1] * so + po.y * sn;
+    o[2] = o[2] * so + po.z * sn;
+    o[3] = o[3] * so + po.w * sn;
+    m = mn;
+  }
+  __device__ __forceinline__ void add(const MergeState& b) {
+    add(b.m, b.l, make_float4(b.o[0], b.o[1], b.o[2], b.o[3]));
+  }
+  // Merge with the state of lane (lane ^ mask).
+  __device__ __forceinline__ void add_xor(int mask) {
+    MergeState b;
+    b.m = __shfl_xor_sync(0xffffffffu, m, mask);
+    b.l = __shfl_xor_sync(0xffffffffu, l, mask);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b.o[k] = __shfl_xor_sync(0xffffffffu, o[k], mask);
+    add(b);
+  }
+};
+
+// Folds the partials of pieces i0 .. i1 (every `step`-th, starting at i0) of
+// one range into st; eight pieces' loads are in flight at a time.
+template <int D, int RK>
+__device__ __forceinline__ void merge_range(const DecodeArgs& a, int64_t i0, int64_t i1,
+                                            int step, int64_t sq, int64_t TP, bool dense, int r,
+                                            int c4, MergeState& st) {
+  constexpr int64_t SF = slot_floats(RK, D);
+  for (int64_t i = i0; i <= i1; i += 8 * step) {
+    float mm[8], ll[8];
+    float4 oo[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t ii = i + (int64_t)u * step;
+      mm[u] = -INFINITY;
+      ll[u] = 0.f;
+      oo[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ii <= i1 && (dense || cta_begin(ii, TP, a.n_cta) < cta_begin(ii + 1, TP, a.n_cta))) {
+        const float* base = a.part + (ii + sq) * SF;
+        mm[u] = __ldcg(base + r);
+        ll[u] = __ldcg(base + RK + r);
+        oo[u] = __ldcg(reinterpret_cast<const float4*>(base + slot_o_off(RK) + r * D) + c4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) st.add(mm[u], ll[u], oo[u]);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* p, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4]) {
+  uint2 w;
+  w.x = pack_bf16(v[0], v[1]);
+  w.y = pack_bf16(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = w;
+}
+
+// Merge of every piece of (b, h).  Work items are (row, 4 dimensions); when
+// there are fewer items than consumer threads, SPLIT adjacent lanes share an
+// item, each folding every SPLIT-th piece, and combine by shuffles.
 template <typename T, int D, int RK>
 __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b, int h) {
+  constexpr int C4 = D / 4;
+  constexpr int ITEMS = RK * C4;
+  constexpr int SPLIT = ITEMS >= kConsumerThreads ? 1 : kConsumerThreads / ITEMS;
+  static_assert(SPLIT <= 32 && (SPLIT & (SPLIT - 1)) == 0, "split");
   const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
   const int64_t n_cta = a.n_cta;
   const bool dense = TP >= n_cta;            // then no CTA's stretch is empty
-  const int64_t slot_f = (int64_t)RK * (D + 2);
   const bool fold = a.mode == DA_MODE_FOLD;
   int64_t i0[2], i1[2], sq[2];
 #pragma unroll
@@ -549,49 +853,37 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
     }
   }
   const float lam = (fold && s.pfx[2 * b + 1] > s.pfx[2 * b]) ? a.far_mix : 0.f;
-  for (int idx = threadIdx.x; idx < a.R * D; idx += kConsumerThreads) {
-    const int r = idx / D, dim = idx - r * D;
-    float M[2] = {-INFINITY, -INFINITY}, Ls[2] = {0.f, 0.f}, O[2] = {0.f, 0.f};
+  const int sub = threadIdx.x & (SPLIT - 1);
+  for (int item = threadIdx.x / SPLIT; item < a.R * C4; item += kConsumerThreads / SPLIT) {
+    const int r = item / C4, c4 = item - r * C4;
+    // range 0 (sinks, or FOLD far memory) and range 1 (window, local, or all)
+    MergeState s0, s1;
+    s0.init();
+    s1.init();
+    merge_range<D, RK>(a, i0[0] + sub, i1[0], SPLIT, sq[0], TP, dense, r, c4, s0);
+    merge_range<D, RK>(a, i0[1] + sub, i1[1], SPLIT, sq[1], TP, dense, r, c4, s1);
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int sg = (fold && rr == 0) ? 1 : 0;
-      for (int64_t i = i0[rr]; i <= i1[rr]; i += 4) {
-        float mm[4], ll[4], oo[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t ii = i + u;
-          mm[u] = -INFINITY;
-          ll[u] = 0.f;
-          oo[u] = 0.f;
-          if (ii <= i1[rr] &&
-              (dense || cta_begin(ii, TP, n_cta) < cta_begin(ii + 1, TP, n_cta))) {
-            const float* base = a.part + (ii + sq[rr]) * slot_f;
-            mm[u] = __ldcg(base + r);
-            ll[u] = __ldcg(base + RK + r);
-            oo[u] = __ldcg(base + 2 * RK + r * D + dim);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (mm[u] == -INFINITY) continue;
-          const float mn = fmaxf(M[sg], mm[u]);
-          const float so = fast_exp2(M[sg] - mn), sn = fast_exp2(mm[u] - mn);
-          Ls[sg] = Ls[sg] * so + ll[u] * sn;
-          O[sg] = O[sg] * so + oo[u] * sn;
-          M[sg] = mn;
-        }
-      }
+    for (int mask = 1; mask < SPLIT; mask <<= 1) {
+      s0.add_xor(mask);
+      s1.add_xor(mask);
     }
-    float res;
+    float res[4];
     if (fold) {
-      res = (Ls[0] > 0.f ? (1.f - lam) * O[0] / Ls[0] : 0.f) +
-            (Ls[1] > 0.f ? lam * O[1] / Ls[1] : 0.f);
+      // (1 - lambda_eff) o_loc + lambda_eff o_far ("FOLD", abstract)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        res[k] = (s1.l > 0.f ? (1.f - lam) * s1.o[k] / s1.l : 0.f) +
+                 (s0.l > 0.f ? lam * s0.o[k] / s0.l : 0.f);
     } else {
-      res = Ls[0] > 0.f ? O[0] / Ls[0] : 0.f;
+      s1.add(s0);                            // one softmax over both ranges
+#pragma unroll
+      for (int k = 0; k < 4; ++k) res[k] = s1.l > 0.f ? s1.o[k] / s1.l : 0.f;
     }
-    const int t = r / a.G, j = r - t * a.G;
-    T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + dim;
-    *out = from_f32<T>(res);
+    if (sub == 0) {
+      const int t = r / a.G, j = r - t * a.G;
+      T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + 4 * c4;
+      store4<T>(out, res);
+    }
   }
 }
 
@@ -678,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prep_queries<T, D, RK>(a, s, inf.seq);
       eng.begin(s);
     }
-    if (inf.flags & kValid) {
+    if ((inf.flags & kValid) && eng.owns(n)) {
       const uint32_t kb = base + st * L.stage_bytes;
       eng.page(s, kb, kb + NCB * kBoxBytes, inf.lohi & 0xffff, inf.lohi >> 16);
     }

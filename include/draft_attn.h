@@ -86,9 +86,12 @@ extern "C" {
 typedef enum { DA_MODE_FULL = 0, DA_MODE_WINDOW = 1, DA_MODE_FOLD = 2, DA_MODE_SHARP = 3 } da_mode;
 typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP32 = 1 } da_dtype;
 
-/* Kernel engines (da_plan_info.engine). */
-#define DA_ENGINE_CUDA_CORE 0  /* <= 8 query rows per KV head: FP32 FMA path      */
-#define DA_ENGINE_MMA       1  /* 9..32 rows (draft trees): bf16 tensor-core path */
+/* Kernel engines (da_plan_info.engine).  "Rows" are the query rows that share
+ * one KV head: (num_q_heads / num_kv_heads) * n_q.  Automatic choice: up to 4
+ * rows on the FP32 pipes; 5..32 rows (bf16) on the tensor cores, where the
+ * rows fill n8 MMA tiles and QK^T / PV are dense contractions. */
+#define DA_ENGINE_CUDA_CORE 0  /* <= 8 rows: FP32 FMA path                        */
+#define DA_ENGINE_MMA       1  /* 5..32 rows, bf16: m16n8k16 tensor-core path     */
 
 typedef struct {
   double  rope_theta;        /* RoPE base theta, > 0                               */
@@ -110,7 +113,9 @@ typedef struct {
   int32_t scale_ref;         /* SharpDraft reference key count N_ref, >= 1         */
   float   softmax_scale;     /* logit scale c; 0 selects 1/sqrt(head_dim)          */
   int32_t num_ctas;          /* persistent CTAs; 0 = one per SM (tests vary this)  */
-  int32_t reserved[6];       /* must be zero                                       */
+  int32_t engine;            /* 0 automatic, 1 CUDA cores (<= 8 rows), 2 tensor
+                                cores (bf16 only); see DA_ENGINE_*                */
+  int32_t reserved[5];       /* must be zero                                       */
 } da_params;
 
 typedef struct {

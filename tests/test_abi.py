@@ -63,6 +63,11 @@ def _ok_params(**kw):
     (dict(num_pages=40_000_000), -1),                  # 32-bit TMA row index would overflow
     (dict(n_q=16), -2),                                # 64 rows per KV head
     (dict(n_q=4, dtype="fp32"), -2),                   # >8 rows needs bf16 tensor cores
+    (dict(n_q=4, engine="cuda_core"), -2),             # 16 rows: CUDA cores stop at 8
+    (dict(engine="mma"), 0),                           # 4 rows forced onto tensor cores
+    (dict(engine="cuda_core", num_q_heads=64), 0),     # 8 rows forced onto CUDA cores
+    (dict(engine="mma", dtype="fp32"), -2),            # tensor-core path is bf16 only
+    (dict(engine=3), -1),
 ])
 def test_check_params(kw, code):
     assert B.draft_attn_check_params(_ok_params(**kw)) == code

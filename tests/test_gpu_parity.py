@@ -172,6 +172,22 @@ def test_parity_small(shape, mp, dtype, d):
     s.close()
 
 
+@pytest.mark.parametrize("shape,engine", [((64, 8, 1), "cuda_core"), ((32, 8, 2), "cuda_core"),
+                                          ((32, 8, 1), "mma"), ((8, 8, 1), "mma"),
+                                          ((16, 8, 1), "mma")],
+                         ids=lambda x: str(x))
+@pytest.mark.parametrize("mode", ["full", "fold", "window", "sharp"])
+def test_engine_forced(shape, engine, mode):
+    """Either engine, forced, computes the same attention for 1..8 rows."""
+    h, hk, nq = shape
+    s = Setup(batch=2, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
+              ctx=[2500, 700], mode=mode, window=600, n_sink=4 if mode == "window" else 0,
+              alpha=2.0, far_mix=0.5, scale_slope=0.05, scale_ref=256, seed=12, engine=engine)
+    assert s.da.info()["engine_name"] == engine
+    compare(s.run(), s.oracle(), "bf16", f"{mode} {shape} {engine}")
+    s.close()
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 7, 148, 600])
 @pytest.mark.parametrize("mode", ["full", "fold", "window"])
 def test_split_count(num_ctas, mode):
