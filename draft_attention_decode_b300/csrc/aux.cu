@@ -11,6 +11,8 @@ namespace da {
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t total = (int64_t)a.B * a.n_new * a.H_kv;
@@ -18,6 +20,19 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   const int h = (int)(w % a.H_kv);
   const int64_t bt_tok = w / a.H_kv;           // b * n_new + token
   const int b = (int)(bt_tok / a.n_new);
+  // the token's K and V do not depend on where it goes: load them first
+  const int64_t src = (bt_tok * a.H_kv + h) * D;
+  const T* k = static_cast<const T*>(a.k) + src;
+  const T* v = static_cast<const T*>(a.v) + src;
+  T kx[D / 64], ky[D / 64], vx[D / 64], vy[D / 64];
+#pragma unroll
+  for (int u = 0; u < D / 64; ++u) {
+    const int f = lane + 32 * u;
+    kx[u] = k[f];
+    ky[u] = k[f + D / 2];
+    vx[u] = v[f];
+    vy[u] = v[f + D / 2];
+  }
   const int32_t pos = __ldg(a.pos + bt_tok);
   if (pos < 0) return;                          // padding token
   const int32_t pg = pos / kPage;
@@ -30,27 +45,24 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     if (lane == 0) atomicOr(a.status, DA_STATUS_BAD_PAGE);
     return;
   }
-  const int64_t src = (bt_tok * a.H_kv + h) * D;
   const int64_t dst = (((int64_t)phys * a.H_kv + h) * kPage + (pos - pg * kPage)) * D;
-  const T* k = static_cast<const T*>(a.k) + src;
-  const T* v = static_cast<const T*>(a.v) + src;
   T* kc = static_cast<T*>(a.k_cache) + dst;
   T* vc = static_cast<T*>(a.v_cache) + dst;
   T* ks = a.k_side ? static_cast<T*>(a.k_side) + dst : nullptr;
 #pragma unroll
-  for (int f = lane; f < D / 2; f += 32) {
-    const T xr = k[f], yr = k[f + D / 2];
-    const float x = to_f32<T>(xr), y = to_f32<T>(yr);
+  for (int u = 0; u < D / 64; ++u) {
+    const int f = lane + 32 * u;
+    const float x = to_f32<T>(kx[u]), y = to_f32<T>(ky[u]);
     float c, s;
     rope_cos_sin(pos, a.inv_freq[f], c, s);
     kc[f] = from_f32<T>(x * c - y * s);
     kc[f + D / 2] = from_f32<T>(y * c + x * s);
     if (ks) {
-      ks[f] = xr;
-      ks[f + D / 2] = yr;
+      ks[f] = kx[u];
+      ks[f + D / 2] = ky[u];
     }
-    vc[f] = v[f];
-    vc[f + D / 2] = v[f + D / 2];
+    vc[f] = vx[u];
+    vc[f + D / 2] = vy[u];
   }
 }
 
@@ -61,13 +73,11 @@ cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)blocks);
   if (dtype == DA_DTYPE_BF16) {
-    if (d == 128) append_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(a);
-    else append_kernel<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(a);
-  } else {
-    if (d == 128) append_kernel<float, 128><<<grid, 256, 0, st>>>(a);
-    else append_kernel<float, 64><<<grid, 256, 0, st>>>(a);
+    if (d == 128) return launch_pdl(append_kernel<__nv_bfloat16, 128>, grid, 256, 0, st, a);
+    return launch_pdl(append_kernel<__nv_bfloat16, 64>, grid, 256, 0, st, a);
   }
-  return cudaGetLastError();
+  if (d == 128) return launch_pdl(append_kernel<float, 128>, grid, 256, 0, st, a);
+  return launch_pdl(append_kernel<float, 64>, grid, 256, 0, st, a);
 }
 
 // ---------------------------------------------------------------------------

@@ -71,8 +71,7 @@ cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a
                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
                           cudaStream_t st) {
   return with_kernel(c, dtype, d, [&](auto kern) {
-    kern<<<a.n_cta, kThreads, c.smem, st>>>(a, mk, mv, ms, c.stages);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(a.n_cta), dim3(kThreads), c.smem, st, a, mk, mv, ms, c.stages);
   });
 }
 

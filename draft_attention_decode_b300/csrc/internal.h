@@ -2,9 +2,28 @@
 // units (decode.cu, aux.cu).
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace da {
+
+// Launches `kern` with programmatic stream serialisation (see grid_dep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct Choice {
   int engine;      // DA_ENGINE_CUDA_CORE or DA_ENGINE_MMA

@@ -94,9 +94,8 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
 template <int D>
 __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
+  grid_dep_launch_dependents();
   for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.inv_freq[i];
-  for (int b = tid; b < a.B; b += blockDim.x)
-    s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
   if (tid == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
       mbar_init(&s.full[i], 1);
@@ -104,6 +103,9 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
     }
     fence_barrier_init();
   }
+  grid_dep_wait();   // global memory from here on
+  for (int b = tid; b < a.B; b += blockDim.x)
+    s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
   __syncthreads();
   if (tid < 32) {
     const int lane = tid;
