@@ -327,7 +327,6 @@ struct CoreEngine {
         part[RK + r] = l;
       }
     }
-    __threadfence();
     named_barrier(1, kConsumerThreads);
     reset();
   }
@@ -508,7 +507,6 @@ struct CoreEngineWide {
         part[RK + r] = l;
       }
     }
-    __threadfence();
     named_barrier(1, kConsumerThreads);
     reset();
   }
@@ -730,7 +728,6 @@ struct MmaEngine {
         part[RK + r] = lsum;
       }
     }
-    __threadfence();
     named_barrier(1, kConsumerThreads);
     reset();
   }
@@ -893,14 +890,13 @@ __device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pa
   const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1;
   uint32_t* c = a.cnt + (int64_t)b * a.H_kv + h;
   if (threadIdx.x == 0) {
-    __threadfence();
+    // Release: the partial the consumers wrote before the barrier in finish()
+    // is visible before the count; acquire: when last, every other piece's
+    // partial is visible to this CTA (its threads read after the barrier).
     const uint32_t total = (uint32_t)seq_pages(s.pfx, b);
-    const uint32_t old = atomicAdd(c, pages);
+    const uint32_t old = atom_add_acq_rel_gpu(c, pages);
     const int last = old + pages == total;
-    if (last) {
-      __threadfence();
-      atomicExch(c, 0u);  // every piece of (b, h) has arrived: ready for the next call
-    }
+    if (last) atomicExch(c, 0u);  // every piece of (b, h) has arrived: ready for the next call
     s.flag[0] = last;
   }
   named_barrier(1, kConsumerThreads);
