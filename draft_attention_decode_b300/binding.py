@@ -28,6 +28,7 @@ DA_STATUS_BAD_PAGE = 1
 DA_STATUS_BAD_CTX_LEN = 2
 DA_STATUS_BAD_POSITION = 4
 DA_STATUS_WAIT_TIMEOUT = 8
+DA_STATIC_WORKSPACE_BYTES = 8 << 20
 
 MODES = {"full": 0, "window": 1, "fold": 2, "sharp": 3}
 DTYPES = {"bf16": 0, "fp32": 1}
@@ -104,6 +105,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "draft_attn_plan_destroy": (None, [VP]),
         "draft_attn_append_kv": (ctypes.c_int, [VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP]),
         "draft_attn_run": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+        "draft_attn_run_static": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP]),
         "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
                                                    I64, VP, VP]),
         "draft_attn_get_status": (ctypes.c_int, [VP, VP, P(ctypes.c_uint32)]),
@@ -232,6 +234,18 @@ def draft_attn_run(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_si
         plan, _ptr(q), _ptr(q_pos), _ptr(ctx_lens), _ptr(block_table), _ptr(k_cache),
         _ptr(v_cache), _ptr(k_side), _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream)), "draft_attn_run")
+
+
+def draft_attn_run_static(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, out,
+                          stream=None) -> None:
+    """draft_attn_run with the library's own fixed device workspace: for
+    callers that cannot allocate device memory when they run the step."""
+    for name, t in (("q_pos", q_pos), ("ctx_lens", ctx_lens), ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    _check(load_library().draft_attn_run_static(
+        plan, _ptr(q), _ptr(q_pos), _ptr(ctx_lens), _ptr(block_table), _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_side), _ptr(out), _stream(stream)), "draft_attn_run_static")
 
 
 def draft_attn_debug_gather(plan, q_pos, ctx_lens, block_table, b, t, capacity, stream=None) -> dict:

@@ -103,6 +103,17 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
 
 }  // namespace
 
+namespace da {
+bool plan_workspace_layout(const da_plan_s* pl, int* device, size_t* counter_bytes,
+                           size_t* workspace_bytes) {
+  if (!pl) return false;
+  *device = pl->device;
+  *counter_bytes = pl->cnt_bytes;
+  *workspace_bytes = pl->ws_bytes;
+  return true;
+}
+}  // namespace da
+
 extern "C" {
 
 int draft_attn_version(void) { return kAbiVersion; }

@@ -57,6 +57,11 @@ struct AppendArgs {
 };
 cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st);
 
+// Device, counter-region bytes and total workspace bytes of a plan; false for
+// a null plan.
+bool plan_workspace_layout(const da_plan_s* plan, int* device, size_t* counter_bytes,
+                           size_t* workspace_bytes);
+
 struct GatherOut {
   int32_t* positions;
   int64_t* phys_slot;

@@ -180,6 +180,34 @@ int draft_attn_run(da_plan_t plan, const void* q, const int32_t* q_pos,
                    const void* k_cache, const void* v_cache, const void* k_side,
                    void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library-owned workspace that draft_attn_run_static uses
+ * (8 MiB): enough for every shape up to 16 sequences x 8 KV heads x 32 rows
+ * at head_dim 128 on 148 SMs.  Each GPU that loads the library keeps this much
+ * device memory reserved until the process exits. */
+#define DA_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* draft_attn_run without a caller-supplied workspace, for callers that cannot
+ * allocate device memory when they run the draft step (code that runs inside
+ * another framework's allocator or memory pool, or a runtime that hands out
+ * only the buffers it owns).  The scratch is a fixed array of
+ * DA_STATIC_WORKSPACE_BYTES in the library's device image; the call itself
+ * allocates nothing and calls no allocating routine.  The caller still passes
+ * the inputs and out.  (The pages describe no such entry point; it exists for
+ * deployment only.)
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Returns DA_ERR_WORKSPACE_TOO_SMALL when the plan's workspace_bytes
+ *    exceeds DA_STATIC_WORKSPACE_BYTES.
+ *  - Every call shares the one array: each call first clears its counters
+ *    on `stream`, and calls whose GPU work overlaps (different streams, or
+ *    different threads) race and must be serialised by the caller.
+ * Otherwise identical to draft_attn_run. */
+int draft_attn_run_static(da_plan_t plan, const void* q, const int32_t* q_pos,
+                          const int32_t* ctx_lens, const int32_t* block_table,
+                          const void* k_cache, const void* v_cache, const void* k_side,
+                          void* out, void* stream);
+
 /* Test hook: the keys query token t of sequence b selects, computed by the
  * same device routines as draft_attn_run.  Per key, ascending by position:
  * positions (int32), phys_slot = physical_page * page_size + slot (int64, -1
