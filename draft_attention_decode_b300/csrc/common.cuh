@@ -18,12 +18,15 @@ constexpr int kPage = 64;            // tokens per page (the only page size buil
 constexpr int kSwizzleRow = 128;     // bytes per row of a 128B-swizzled TMA box
 constexpr int kBoxBytes = kPage * kSwizzleRow;  // one 64-row x 128-byte box
 constexpr int kMaxBatch = 1024;
+// Kernel variants (shared-memory layout): 0 CUDA cores, 1 tensor cores.
+// Both run two consumer warpgroups plus one producer warpgroup (only its
+// first warp works), launched at 168 registers per thread; the producer group
+// gives registers back (setmaxnreg 40) so the consumers can hold 232:
+// 128 * 40 + 256 * 232 = 384 * 168.
+constexpr int kVariantCore = 0;
+constexpr int kVariantMma = 1;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-// Two consumer warpgroups plus one producer warpgroup (only its first warp
-// works).  Launched at 168 registers per thread; the producer group gives
-// registers back (setmaxnreg 40) so the consumers can hold 232:
-// 128 * 40 + 256 * 232 = 384 * 168.
 constexpr int kThreads = kConsumerThreads + 128;
 constexpr int kProducerRegs = 40;
 constexpr int kConsumerRegs = 232;

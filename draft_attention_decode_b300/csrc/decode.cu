@@ -18,14 +18,16 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int m
   if (mma) {
     if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
     c->engine = DA_ENGINE_MMA;
+    c->variant = kVariantMma;
     c->rk = rows <= 8 ? 8 : rows <= 16 ? 16 : 32;
   } else {
     if (rows > 8) return false;
     c->engine = DA_ENGINE_CUDA_CORE;
     c->rk = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+    c->variant = kVariantCore;
   }
   for (int s = 4; s >= 2; --s) {
-    const Layout L = make_layout(c->engine, es, d, c->rk, s, batch);
+    const Layout L = make_layout(c->variant, es, d, c->rk, s, batch);
     if ((int)L.total <= max_smem) {
       c->stages = s;
       c->smem = L.total;
@@ -48,11 +50,12 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
 #undef DA_MMA
     return cudaErrorInvalidValue;
   }
-#define DA_CORE(T, D, RK) \
-  if (dtype == (sizeof(T) == 2 ? DA_DTYPE_BF16 : DA_DTYPE_FP32) && d == D && c.rk == RK) \
-    return f(decode_kernel<T, D, \
-                           std::conditional_t<(RK <= 4), CoreEngine<T, D, RK>, CoreEngineWide<T, D, RK>>, \
-                           0, RK>);
+#define DA_CORE(T, D, RK)                                                                     \
+  if (dtype == (sizeof(T) == 2 ? DA_DTYPE_BF16 : DA_DTYPE_FP32) && d == D && c.rk == RK)         \
+    return f(decode_kernel<T, D,                                                               \
+                           std::conditional_t<(RK <= 4), CoreEngine<T, D, RK>,                  \
+                                              CoreEngineWide<T, D, RK>>,                        \
+                           kVariantCore, RK>);
   DA_CORE(bf, 128, 1) DA_CORE(bf, 128, 2) DA_CORE(bf, 128, 4) DA_CORE(bf, 128, 8)
   DA_CORE(bf, 64, 1) DA_CORE(bf, 64, 2) DA_CORE(bf, 64, 4) DA_CORE(bf, 64, 8)
   DA_CORE(float, 128, 1) DA_CORE(float, 128, 2) DA_CORE(float, 128, 4) DA_CORE(float, 128, 8)

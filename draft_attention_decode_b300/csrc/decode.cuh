@@ -28,7 +28,7 @@ namespace da {
 // <R(p)q, R(P)k> = <R(p-P)q, k>), times the logit multiplier, into s.q
 // [rk][d] as FP32.  Rows >= R are zero.  Consumer threads only.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int RK>
+template <typename T, int D, int RK, int NCT>
 __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
   const int tid = threadIdx.x;
   const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1, r = e & 1;
@@ -43,16 +43,16 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
     if (n > 0) mult *= fmaxf(1.f, 1.f + a.beta * logf((float)n / (float)a.n_ref));
   }
   float2* cs = reinterpret_cast<float2*>(s.mo);
-  for (int i = tid; i < a.n_q * (D / 2); i += kConsumerThreads) {
+  for (int i = tid; i < a.n_q * (D / 2); i += NCT) {
     const int t = i / (D / 2), f = i - t * (D / 2);
     const int32_t p = __ldg(a.q_pos + b * a.n_q + t) - shift;
     float c, sn;
     rope_cos_sin(p, s.invf[f], c, sn);
     cs[i] = make_float2(c, sn);
   }
-  named_barrier(1, kConsumerThreads);
+  named_barrier(1, NCT);
   const T* qb = static_cast<const T*>(a.q);
-  for (int i = tid; i < RK * (D / 2); i += kConsumerThreads) {
+  for (int i = tid; i < RK * (D / 2); i += NCT) {
     const int row = i / (D / 2), f = i - row * (D / 2);
     float xr = 0.f, yr = 0.f;
     if (row < a.R) {
@@ -66,15 +66,16 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
     s.q[row * D + f] = xr;
     s.q[row * D + f + D / 2] = yr;
   }
-  named_barrier(1, kConsumerThreads);
+  named_barrier(1, NCT);
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// Reduce-scatter of RK per-lane partial sums over the 8 lanes of a key group
-// (lane bits 0..2): afterwards lane ds holds the total for row ds & (RK-1).
-template <int RK>
-__device__ __forceinline__ float reduce_scatter8(float (&v)[RK], int ds) {
+// Reduce-scatter of RK per-lane partial sums over the W lanes of a key group
+// (lane bits below log2 W): afterwards lane ds holds the total for row
+// ds & (RK-1).
+template <int RK, int W>
+__device__ __forceinline__ float reduce_scatter(float (&v)[RK], int ds) {
 #pragma unroll
   for (int m = RK / 2; m >= 1; m >>= 1) {
     const bool up = (ds & m) != 0;
@@ -87,8 +88,12 @@ __device__ __forceinline__ float reduce_scatter8(float (&v)[RK], int ds) {
   }
   float x = v[0];
 #pragma unroll
-  for (int m = RK; m < 8; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  for (int m = RK; m < W; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
   return x;
+}
+template <int RK>
+__device__ __forceinline__ float reduce_scatter8(float (&v)[RK], int ds) {
+  return reduce_scatter<RK, 8>(v, ds);
 }
 
 template <typename T>
@@ -132,25 +137,33 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core engine, 1..4 rows.  Warp w owns keys 8w .. 8w+7 of the page; the
+// CUDA-core engine, 1..4 rows.  Warp w owns keys 8w .. 8w+7 of each page; the
 // eight lanes of key group kg (lane bits 3, 4) share key 8w + kg (+4 on the
 // second pass) and lane ds (bits 0..2) owns D/8 of its dimensions, read as
 // 16-byte chunks whose order is rotated by ds (no bank conflicts under the
-// 128-byte swizzle).  QK^T: per-lane partial dots, reduce-scatter so that lane
-// ds holds row ds's score.  PV runs in the same layout: the row
+// 128-byte swizzle).  QK^T: per-lane partial dots, then a reduce-scatter
+// leaves lane ds with row ds's score.  PV runs in the same layout: the row
 // probabilities of the lane's key come back by shuffle, the lane accumulates
-// p * V over its own dimensions, and the four key groups are summed only at
-// the end of a piece.  The running maximum is raised lazily (only when a
-// score exceeds it by more than 2^8): the result is exact for any reference
-// value, and the accumulators are rescaled only a handful of times.
+// p * V over its own dimensions, and the key groups are summed only at the
+// end of a piece.  Two consecutive pages of a piece are processed together
+// (one softmax step, twice the independent work in flight per warp).  The
+// running maximum is raised lazily (only when a score exceeds it by more than
+// 2^8): the result is exact for any reference value, and the accumulators are
+// rescaled only a handful of times.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int RK>
 struct CoreEngine {
+  static constexpr int NCW = kConsumerWarps;
+  static constexpr int NCT = NCW * 32;
+  static constexpr bool kPairs = true;         // takes two pages per step
+  static constexpr int LPK = 8;                // lanes per key
+  static constexpr int KG = 32 / LPK;          // key groups per pass
+  static constexpr int KPW = 64 / NCW;         // keys per warp and page (= 2 KG)
   static constexpr int ES = sizeof(T);
-  static constexpr int DQ = D / 8;            // dimensions per lane
-  static constexpr int NCH = DQ * ES / 16;    // 16-byte chunks per lane (1, 2 or 4)
-  static constexpr int EPC = 16 / ES;         // elements per chunk
-  static constexpr float kLazy = 8.f;         // log2 headroom before a rescale
+  static constexpr int DQ = D / LPK;           // dimensions per lane
+  static constexpr int NCH = DQ * ES / 16;     // 16-byte chunks per lane (1, 2 or 4)
+  static constexpr int EPC = 16 / ES;          // elements per chunk
+  static constexpr float kLazy = 8.f;          // log2 headroom before a rescale
   static_assert(RK == 1 || RK == 2 || RK == 4, "rows");
   static_assert(NCH >= 1 && (NCH & (NCH - 1)) == 0, "chunks");
 
@@ -160,18 +173,22 @@ struct CoreEngine {
   uint32_t off[2][NCH];  // swizzled byte offsets of the lane's chunks, pass 0/1
   int lane, warp, kg, ds;
 
+  __device__ __forceinline__ int chunk_of(int i) const {
+    return ds * NCH + ((i + ((ds * NCH) >> 3)) & (NCH - 1));
+  }
+  // Dimension of element e of chunk slot i of this lane.
+  __device__ __forceinline__ int dim_of(int i, int e) const { return chunk_of(i) * EPC + e; }
+
   __device__ __forceinline__ void init() {
     lane = threadIdx.x & 31;
     warp = threadIdx.x >> 5;
-    kg = lane >> 3;
-    ds = lane & 7;
+    kg = lane / LPK;
+    ds = lane % LPK;
 #pragma unroll
     for (int it = 0; it < 2; ++it)
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
-        off[it][i] = swz_addr(0u, warp * 8 + kg + 4 * it, (ds * NCH + ic) * 16);
-      }
+      for (int i = 0; i < NCH; ++i)
+        off[it][i] = swz_addr(0u, warp * KPW + kg + KG * it, chunk_of(i) * 16);
   }
 
   __device__ __forceinline__ bool owns(uint32_t) const { return true; }
@@ -183,12 +200,6 @@ struct CoreEngine {
       for (int e = 0; e < DQ / 2; ++e) o2[r][e] = make_float2(0.f, 0.f);
     m_run = -INFINITY;
     l_run = 0.f;
-  }
-
-  // Dimension of element e of chunk slot i of this lane.
-  __device__ __forceinline__ int dim_of(int i, int e) const {
-    const int ic = (i + ((ds * NCH) >> 3)) & (NCH - 1);
-    return (ds * NCH + ic) * EPC + e;
   }
 
   __device__ __forceinline__ void begin(const Smem& s) {
@@ -204,20 +215,26 @@ struct CoreEngine {
     reset();
   }
 
-  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
-    float sc[2];
-    bool ok[2];
+  // NP consecutive pages of one piece: K/V stage addresses and valid key
+  // ranges [lo, hi) inside each page.
+  template <int NP>
+  __device__ __forceinline__ void pages(const uint32_t (&kb)[NP], const uint32_t (&vb)[NP],
+                                        const int (&lo)[NP], const int (&hi)[NP]) {
+    constexpr int NIT = 2 * NP;
+    float sc[NIT];
+    bool ok[NIT];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int key = warp * 8 + kg + 4 * it;
-      ok[it] = key >= lo && key < hi;
+    for (int it = 0; it < NIT; ++it) {
+      const int pg = it >> 1, ps = it & 1;
+      const int key = warp * KPW + kg + KG * ps;
+      ok[it] = key >= lo[pg] && key < hi[pg];
       float2 acc[RK];
 #pragma unroll
       for (int r = 0; r < RK; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         float f[EPC];
-        Chunk<T>::load(kbase + off[it][i], f);
+        Chunk<T>::load(kb[pg] + off[ps][i], f);
 #pragma unroll
         for (int e = 0; e < EPC / 2; ++e) {
           const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
@@ -228,13 +245,15 @@ struct CoreEngine {
       float v[RK];
 #pragma unroll
       for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
-      const float sr = reduce_scatter8<RK>(v, ds);
+      const float sr = reduce_scatter<RK, LPK>(v, ds);
       sc[it] = ok[it] ? sr : -INFINITY;
     }
-    // Row maximum over the warp's 8 keys (lanes with the same ds).
-    float mx = fmaxf(sc[0], sc[1]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    // Row maximum over the warp's keys (lanes with the same ds).
+    float mx = sc[0];
+#pragma unroll
+    for (int it = 1; it < NIT; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+    for (int m = LPK; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
     const bool raise = mx > m_run + kLazy;
     if (__any_sync(0xffffffffu, raise)) {
       const float m_new = raise ? mx : m_run;
@@ -243,7 +262,7 @@ struct CoreEngine {
       m_run = m_new;
 #pragma unroll
       for (int r = 0; r < RK; ++r) {
-        const float ar = __shfl_sync(0xffffffffu, al, (lane & ~7) | r);
+        const float ar = __shfl_sync(0xffffffffu, al, (lane & ~(LPK - 1)) | r);
 #pragma unroll
         for (int e = 0; e < DQ / 2; ++e) {
           o2[r][e].x *= ar;
@@ -251,21 +270,25 @@ struct CoreEngine {
         }
       }
     }
-    float p[2];
+    float p[NIT];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) p[it] = sc[it] > -INFINITY ? fast_exp2(sc[it] - m_run) : 0.f;
-    l_run += p[0] + p[1];
+    for (int it = 0; it < NIT; ++it) {
+      p[it] = sc[it] > -INFINITY ? fast_exp2(sc[it] - m_run) : 0.f;
+      l_run += p[it];
+    }
     // PV in the QK^T layout.
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
+    for (int it = 0; it < NIT; ++it) {
+      const int pg = it >> 1, ps = it & 1;
       float pr[RK];
 #pragma unroll
-      for (int r = 0; r < RK; ++r) pr[r] = __shfl_sync(0xffffffffu, p[it], (lane & ~7) | r);
+      for (int r = 0; r < RK; ++r)
+        pr[r] = __shfl_sync(0xffffffffu, p[it], (lane & ~(LPK - 1)) | r);
       if (ok[it]) {   // keys outside [lo, hi) may hold anything, NaN included
 #pragma unroll
         for (int i = 0; i < NCH; ++i) {
           float f[EPC];
-          Chunk<T>::load(vbase + off[it][i], f);
+          Chunk<T>::load(vb[pg] + off[ps][i], f);
 #pragma unroll
           for (int e = 0; e < EPC / 2; ++e) {
             const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
@@ -278,20 +301,28 @@ struct CoreEngine {
     }
   }
 
-  // Sum the four key groups, merge the eight warps, write the piece's partial.
+  __device__ __forceinline__ void page(const Smem&, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+    const uint32_t kb[1] = {kbase}, vb[1] = {vbase};
+    const int l[1] = {lo}, h[1] = {hi};
+    pages<1>(kb, vb, l, h);
+  }
+
+  // Sum the key groups, merge the consumer warps, write the piece's partial.
   __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
-    float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    float lt = l_run;
+#pragma unroll
+    for (int m = LPK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
     if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
 #pragma unroll
     for (int r = 0; r < RK; ++r)
 #pragma unroll
       for (int e = 0; e < DQ / 2; ++e) {
         float2 v = o2[r][e];
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+#pragma unroll
+        for (int m = LPK; m < 32; m <<= 1) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, m);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, m);
+        }
         o2[r][e] = v;
       }
     if (kg == 0) {
@@ -304,17 +335,17 @@ struct CoreEngine {
             *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + dim_of(i, 2 * e)) =
                 o2[r][i * (EPC / 2) + e];
     }
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     float* part = a.part + slot * (int64_t)slot_floats(RK, D);
-    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
       float o = 0.f, l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < NCW; ++w) {
           const float2 ml = s.ml[w * RK + r];
           const float sc = fast_exp2(ml.x - M);
           o += sc * s.mo[(w * RK + r) * D + dim];
@@ -327,7 +358,7 @@ struct CoreEngine {
         part[RK + r] = l;
       }
     }
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     reset();
   }
 };
@@ -339,6 +370,9 @@ struct CoreEngine {
 // ---------------------------------------------------------------------------
 template <typename T, int D, int RK>
 struct CoreEngineWide {
+  static constexpr bool kPairs = false;
+  static constexpr int NCW = 8;
+  static constexpr int NCT = NCW * 32;
   static constexpr int ES = sizeof(T);
   static constexpr int DQ = D / 8;            // QK dims per lane
   static constexpr int NCH = DQ * ES / 16;    // 16-byte chunks per lane (1, 2 or 4)
@@ -484,17 +518,17 @@ struct CoreEngineWide {
 #pragma unroll
       for (int e = 0; e < DPL / 2; ++e)
         *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + lane * DPL + 2 * e) = o2[r][e];
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     float* part = a.part + slot * (int64_t)slot_floats(RK, D);
-    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
       float o = 0.f, l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < NCW; ++w) {
           const float2 ml = s.ml[w * RK + r];
           const float sc = fast_exp2(ml.x - M);
           o += sc * s.mo[(w * RK + r) * D + dim];
@@ -507,7 +541,7 @@ struct CoreEngineWide {
         part[RK + r] = l;
       }
     }
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     reset();
   }
 };
@@ -551,6 +585,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 //    RK = 16 NT rows (32 rows: an 8-token draft tree over a GQA group of 4).
 template <int D, int NT, bool SPLIT_PAGES>
 struct MmaEngine {
+  static constexpr bool kPairs = false;
+  static constexpr int NCW = 8;
+  static constexpr int NCT = NCW * 32;
   static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
   static constexpr int RW = 8 * NT;   // rows per warp
   static constexpr int KS = D / 16;   // k-steps of QK^T, m-tiles of PV
@@ -701,10 +738,10 @@ struct MmaEngine {
         base[lr * D + 8] = O[mt][nt][2];
         base[(lr + 1) * D + 8] = O[mt][nt][3];
       }
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     constexpr int NW = SPLIT_PAGES ? 8 : 4;   // warps holding one row
     float* part = a.part + slot * (int64_t)slot_floats(RK, D);
-    for (int idx = threadIdx.x; idx < RK * D; idx += kConsumerThreads) {
+    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       const int w0 = SPLIT_PAGES ? 0 : (r / RW) * 4;
       const int lr = SPLIT_PAGES ? r : r % RW;
@@ -728,7 +765,7 @@ struct MmaEngine {
         part[RK + r] = lsum;
       }
     }
-    named_barrier(1, kConsumerThreads);
+    named_barrier(1, NCT);
     reset();
   }
 };
@@ -824,11 +861,11 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
 // Merge of every piece of (b, h).  Work items are (row, 4 dimensions); when
 // there are fewer items than consumer threads, SPLIT adjacent lanes share an
 // item, each folding every SPLIT-th piece, and combine by shuffles.
-template <typename T, int D, int RK>
+template <typename T, int D, int RK, int NCT>
 __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b, int h) {
   constexpr int C4 = D / 4;
   constexpr int ITEMS = RK * C4;
-  constexpr int SPLIT = ITEMS >= kConsumerThreads ? 1 : kConsumerThreads / ITEMS;
+  constexpr int SPLIT = ITEMS >= NCT ? 1 : NCT / ITEMS;
   static_assert(SPLIT <= 32 && (SPLIT & (SPLIT - 1)) == 0, "split");
   const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
   const int64_t n_cta = a.n_cta;
@@ -851,7 +888,7 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
   }
   const float lam = (fold && s.pfx[2 * b + 1] > s.pfx[2 * b]) ? a.far_mix : 0.f;
   const int sub = threadIdx.x & (SPLIT - 1);
-  for (int item = threadIdx.x / SPLIT; item < a.R * C4; item += kConsumerThreads / SPLIT) {
+  for (int item = threadIdx.x / SPLIT; item < a.R * C4; item += NCT / SPLIT) {
     const int r = item / C4, c4 = item - r * C4;
     // range 0 (sinks, or FOLD far memory) and range 1 (window, local, or all)
     MergeState s0, s1;
@@ -885,7 +922,7 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
 }
 
 // After a piece's partial is written: take the ticket, merge when last.
-template <typename T, int D, int RK>
+template <typename T, int D, int RK, int NCT>
 __device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pages) {
   const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1;
   uint32_t* c = a.cnt + (int64_t)b * a.H_kv + h;
@@ -899,20 +936,20 @@ __device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pa
     if (last) atomicExch(c, 0u);  // every piece of (b, h) has arrived: ready for the next call
     s.flag[0] = last;
   }
-  named_barrier(1, kConsumerThreads);
+  named_barrier(1, NCT);
   const int last = s.flag[0];
-  named_barrier(1, kConsumerThreads);
-  if (last) merge_sequence<T, D, RK>(a, s, b, h);
+  named_barrier(1, NCT);
+  if (last) merge_sequence<T, D, RK, NCT>(a, s, b, h);
 }
 
 // Rows of (b, h) whose selection is empty get a zero output (nobody merges
 // them); CTA (b * H_kv + h) mod n_cta writes it.
-template <typename T, int D>
+template <typename T, int D, int NCT>
 __device__ inline void zero_empty(const DecodeArgs& a, const Smem& s) {
   for (int bh = blockIdx.x; bh < a.B * a.H_kv; bh += a.n_cta) {
     const int b = bh / a.H_kv, h = bh - b * a.H_kv;
     if (seq_pages(s.pfx, b) != 0) continue;
-    for (int idx = threadIdx.x; idx < a.R * D; idx += kConsumerThreads) {
+    for (int idx = threadIdx.x; idx < a.R * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       const int t = r / a.G, j = r - t * a.G;
       static_cast<T*>(a.out)[((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + dim] =
@@ -924,7 +961,7 @@ __device__ inline void zero_empty(const DecodeArgs& a, const Smem& s) {
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <typename T, int D, class Engine, int ENGINE_ID, int RK>
+template <typename T, int D, class Engine, int VARIANT, int RK>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ms,
@@ -932,50 +969,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   constexpr int ES = sizeof(T);
   constexpr int NCB = D * ES / kSwizzleRow;
-  const Layout L = make_layout(ENGINE_ID, ES, D, RK, stages, a.B);
+  constexpr int NCW = Engine::NCW;
+  constexpr int NCT = NCW * 32;
+  static_assert(NCW == kConsumerWarps, "consumer warps");
+  const Layout L = make_layout(VARIANT, ES, D, RK, stages, a.B);
   Smem s = carve(smem_raw, L);
-  prologue<D>(a, s, L);
+  prologue<D, NCW>(a, s, L);
   const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
   const int64_t xs = cta_begin(blockIdx.x, TP, a.n_cta);
   const int64_t xe = cta_begin(blockIdx.x + 1, TP, a.n_cta);
   const int warp = threadIdx.x >> 5;
-  if (warp >= kConsumerWarps) {
+  if (warp >= NCW) {
     regs_dec<kProducerRegs>();
-    if (warp == kConsumerWarps) producer<ES, NCB>(a, s, L, xs, xe, &mk, &mv, &ms);
+    if (warp == NCW) producer<ES, NCB>(a, s, L, xs, xe, &mk, &mv, &ms);
     return;
   }
   regs_inc<kConsumerRegs>();
   Engine eng;
   eng.init();
-  zero_empty<T, D>(a, s);
+  zero_empty<T, D, NCT>(a, s);
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
     int e, h, k;
     locate(s.pfx, 2 * a.B, a.H_kv, xs, e, h, k);
-    prep_queries<T, D, RK>(a, s, e * a.H_kv + h);
+    prep_queries<T, D, RK, NCT>(a, s, e * a.H_kv + h);
     eng.begin(s);
   }
   const uint32_t base = smem_u32(s.stage);
   uint32_t n = 0, pages = 0;
-  for (int64_t x = xs; x < xe; ++x, ++n) {
+  for (int64_t x = xs; x < xe;) {
     const uint32_t st = n % L.stages;
-    const uint32_t par = (n / L.stages) & 1u;
-    if (!mbar_wait(&s.full[st], par, a.status)) break;
+    if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status)) break;
     const PageInfo inf = s.info[st];
     if ((inf.flags & kFirst) && x != xs) {
-      prep_queries<T, D, RK>(a, s, inf.seq);
+      prep_queries<T, D, RK, NCT>(a, s, inf.seq);
       eng.begin(s);
     }
-    if ((inf.flags & kValid) && eng.owns(n)) {
-      const uint32_t kb = base + st * L.stage_bytes;
-      eng.page(s, kb, kb + NCB * kBoxBytes, inf.lohi & 0xffff, inf.lohi >> 16);
+    const uint32_t kb0 = base + st * L.stage_bytes;
+    const int lo0 = (inf.flags & kValid) ? (inf.lohi & 0xffff) : 0;
+    const int hi0 = (inf.flags & kValid) ? (inf.lohi >> 16) : 0;
+    bool last = (inf.flags & kLast) != 0;
+    uint32_t taken = 1;
+    if constexpr (Engine::kPairs) {
+      // the next page belongs to the same piece unless this one ends it
+      if (!last) {
+        const uint32_t st1 = (n + 1) % L.stages;
+        if (!mbar_wait(&s.full[st1], ((n + 1) / L.stages) & 1u, a.status)) break;
+        const PageInfo inf1 = s.info[st1];
+        const uint32_t kb1 = base + st1 * L.stage_bytes;
+        const uint32_t kb[2] = {kb0, kb1};
+        const uint32_t vb[2] = {kb0 + NCB * kBoxBytes, kb1 + NCB * kBoxBytes};
+        const int lo[2] = {lo0, (inf1.flags & kValid) ? (inf1.lohi & 0xffff) : 0};
+        const int hi[2] = {hi0, (inf1.flags & kValid) ? (inf1.lohi >> 16) : 0};
+        eng.template pages<2>(kb, vb, lo, hi);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+          mbar_arrive(&s.empty[st]);
+          mbar_arrive(&s.empty[st1]);
+        }
+        taken = 2;
+        last = (inf1.flags & kLast) != 0;
+      }
     }
-    ++pages;
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
-    if (inf.flags & kLast) {
+    if (taken == 1) {
+      if (hi0 > lo0 && eng.owns(n)) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
+    }
+    pages += taken;
+    x += taken;
+    n += taken;
+    if (last) {
       eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
-      ticket<T, D, RK>(a, s, inf.seq, pages);
+      ticket<T, D, RK, NCT>(a, s, inf.seq, pages);
       pages = 0;
     }
   }

@@ -27,6 +27,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 struct Choice {
   int engine;      // DA_ENGINE_CUDA_CORE or DA_ENGINE_MMA
+  int variant;     // kVariantCore or kVariantMma (shared-memory layout)
   int rk;          // rows the kernel instance computes
   int stages;      // pipeline depth
   uint32_t smem;   // dynamic shared memory bytes

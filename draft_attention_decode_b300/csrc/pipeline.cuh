@@ -32,19 +32,21 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// engine 0: CUDA cores (merge rows per warp = rk, per-warp p buffer);
-// engine 1: mma (merge rows per warp = 16, no p buffer).
-__host__ __device__ inline Layout make_layout(int engine, int es, int d, int rk, int stages,
+// Merge buffers hold `rm` rows per consumer warp: rk on the CUDA cores, 16
+// on the tensor cores; the CUDA-core variant also keeps a per-warp
+// probability buffer (used by the 5..8-row engine).
+__host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk, int stages,
                                               int batch) {
   Layout L;
   L.stage_bytes = 2u * (uint32_t)(d * es / kSwizzleRow) * kBoxBytes;
   L.stages = stages;
   uint32_t off = L.stage_bytes * stages;
-  int rm = engine == 0 ? rk : 16;
+  const uint32_t ncw = (uint32_t)kConsumerWarps;
+  const int rm = variant == kVariantMma ? 16 : rk;
   L.q_off = off;     off += align_up((uint32_t)rk * d * 4, 128);
-  L.mo_off = off;    off += align_up((uint32_t)kConsumerWarps * rm * d * 4, 128);
-  L.ml_off = off;    off += align_up((uint32_t)kConsumerWarps * rm * 8, 128);
-  L.p_off = off;     off += engine == 0 ? align_up((uint32_t)kConsumerWarps * 9 * rk * 4, 128) : 0;
+  L.mo_off = off;    off += align_up(ncw * rm * d * 4, 128);
+  L.ml_off = off;    off += align_up(ncw * rm * 8, 128);
+  L.p_off = off;     off += variant == kVariantCore ? align_up(ncw * 9 * rk * 4, 128) : 0;
   L.info_off = off;  off += align_up((uint32_t)stages * sizeof(PageInfo), 128);
   L.bar_off = off;   off += align_up((uint32_t)stages * 16, 128);
   L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);
@@ -91,7 +93,7 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
 
 // Prologue: context lengths and the page prefix over (b, range), computed
 // identically by every CTA.  All threads take part.
-template <int D>
+template <int D, int NCW>
 __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
   grid_dep_launch_dependents();
@@ -99,7 +101,7 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   if (tid == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], kConsumerWarps);
+      mbar_init(&s.empty[i], NCW);
     }
     fence_barrier_init();
   }
