@@ -513,12 +513,14 @@ def run_ours(args, dist):
         graphs["full"].replay()
         torch.cuda.synchronize()
     res = {}
+    torch.cuda.profiler.start()   # profilers started with capture off see only this region
     for m in ("full", "window"):
         ms, _ = time_graph(graphs[m], args.steps, args.warmup, flush, dist)
         nbytes = dl.kv_bytes(m)
         res[m] = {"ms_per_loop": ms, "us_per_draft_step": ms * 1e3 / dl.steps,
                   "kv_bytes_per_loop": nbytes, "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
                   "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+    torch.cuda.profiler.stop()
     clk = clocks.stop()
 
     # roofline of the dominant kernel: the full-mode attention call of the
@@ -543,6 +545,8 @@ def run_ours(args, dist):
     torch.cuda.empty_cache()
 
     sweep = None if args.no_sweep else context_sweep(dev, args, flush, dist, peak)
+    others = None if args.no_workloads else all_workloads(
+        dev, args, flush, dist, peak, ("fold_4x256k", "ragged_tree_16x8"))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -564,11 +568,13 @@ def run_ours(args, dist):
         "gpu_launches": launches,
         "clocks": clk,
         "sweep": sweep,
+        "workloads": others,
     }
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     if args.all and dist.rank == 0:
-        table = all_workloads(dev, args, flush, dist, peak)
+        table = all_workloads(dev, args, flush, dist, peak,
+                              ("fold_4x256k", "ragged_tree_16x8", "tiny_window_fp32"))
         with open(args.all, "w") as f:
             json.dump({"headline": line, "workloads": table}, f, indent=1)
 
@@ -578,7 +584,8 @@ def profiled_traffic():
     summary, when it was taken from the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
-        kv = dict(l.strip().split("=", 1) for l in open(path) if "=" in l)
+        kv = dict(l.strip().split("=", 1) for l in open(path)
+                  if "=" in l and not l.lstrip().startswith("#"))
     except OSError:
         return None
     if kv.get("sources_sha") != sources_sha():
@@ -634,9 +641,11 @@ def context_sweep(dev, args, flush, dist, peak):
             "rows": rows, "window_max_over_min": round(max(w) / min(w), 3)}
 
 
-def all_workloads(dev, args, flush, dist, peak):
+def all_workloads(dev, args, flush, dist, peak, names):
+    """The other workloads, each mode's attention call replayed from a CUDA
+    graph (inputs resident, L2 flushed between replays)."""
     table = []
-    for name in ("fold_4x256k", "ragged_tree_16x8", "tiny_window_fp32"):
+    for name in names:
         wl = WL.WORKLOADS[name]
         dl = DraftLoop(wl, dev, wl.modes)
         for m in wl.modes:
@@ -661,9 +670,12 @@ def profile_loop(args):
     if args.ctx:
         wl = WL.resized(wl, args.ctx)
     dl = DraftLoop(wl, dev, (args.profile_loop,))
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()   # with ncu --profile-from-start off: the loop only
     for _ in range(args.reps):
         dl.loop(args.profile_loop)
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     code, bits = dl.plans[args.profile_loop].status()
     dl.close()
     if code != B.DA_OK:
@@ -679,6 +691,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the FOLD 4x256K and ragged draft-tree timings")
     ap.add_argument("--all", default=None, help="also time every workload; write JSON here")
     ap.add_argument("--profile-loop", default=None, metavar="MODE",
                     help="run the draft loop of --workload in MODE --reps times, untimed")

@@ -168,19 +168,36 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 }
 
 // ---------------------------------------------------------------------------
-// Flat work partition.  The pages of every (b, range, kv head) are laid end
-// to end (b outer, then range, then head); CTA i of n takes positions
-// [floor(i*TP/n), floor((i+1)*TP/n)).  A "piece" is the part of one
-// (b, range, head) sequence that one CTA covers; it writes its partial to
-// slot (cta + sequence index), which is unique because both indices only grow
-// along the line and every new piece advances at least one of them.
+// Flat work partition.  The pages of every (b, kv head) are laid end to end
+// (b outer, then head, then range 0 before range 1); with TP pages in all and
+// n active CTAs, CTA i takes positions [floor(i*TP/n), floor((i+1)*TP/n)).
+// n = min(grid, ceil(TP / kMinPagesPerCta)): a small selection (a window)
+// goes to fewer, fuller CTAs, so that each (b, head) has few pieces to merge.
+// A "piece" is the part of one (b, head, softmax segment) that one CTA covers
+// (the two ranges of window mode are one segment; FOLD's far and local ranges
+// are two).  Its seq = (b * H_kv + head) * 2 + segment never decreases along
+// the line, so slot = cta + seq is unique: every new piece advances the CTA,
+// the seq, or both.
 // ---------------------------------------------------------------------------
+constexpr int kMinPagesPerCta = 4;
+
 __host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int64_t n) {
   return (i * TP) / n;
 }
 // The CTA whose (non-empty) range holds flat position x.
 __host__ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t TP, int64_t n) {
   return ((x + 1) * n - 1) / TP;
+}
+__host__ __device__ __forceinline__ int64_t active_ctas(int64_t TP, int64_t grid) {
+  const int64_t want = (TP + kMinPagesPerCta - 1) / kMinPagesPerCta;
+  return want < 1 ? 1 : (want < grid ? want : grid);
+}
+// Piece id of (b, head, range); FOLD keeps its two ranges apart.
+__host__ __device__ __forceinline__ int32_t piece_seq(int mode, int b, int h, int H, int range) {
+  return (b * H + h) * 2 + (mode == DA_MODE_FOLD ? range : 0);
+}
+__host__ __device__ __forceinline__ bool seq_is_far(int mode, int32_t seq) {
+  return mode == DA_MODE_FOLD && (seq & 1) == 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -233,6 +250,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

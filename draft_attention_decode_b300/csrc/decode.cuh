@@ -31,16 +31,33 @@ namespace da {
 template <typename T, int D, int RK, int NCT>
 __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
   const int tid = threadIdx.x;
-  const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1, r = e & 1;
+  const int bh = seq >> 1, b = bh / a.H_kv, h = bh - b * a.H_kv;
   const int32_t L = s.len[b];
   float mult = a.scale_log2;
   int32_t shift = 0;
-  if (range_is_far(a.mode, r)) {
+  if (seq_is_far(a.mode, seq)) {
     mult *= a.alpha;                     // "FOLD", abstract: concentration factor
     shift = fold_far_pos(L, a.W);
   } else if (a.mode == DA_MODE_SHARP) {  // "SharpDraft", Abstract: query scaling
     const int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
     if (n > 0) mult *= fmaxf(1.f, 1.f + a.beta * logf((float)n / (float)a.n_ref));
+  }
+  // The query elements this thread rotates are loaded first, so that their
+  // latency overlaps the position loads and the angle table.
+  constexpr int PER = (RK * (D / 2) + NCT - 1) / NCT;   // rotate-half pairs per thread
+  const T* qb = static_cast<const T*>(a.q);
+  float qx[PER], qy[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = tid + u * NCT;
+    const int row = i / (D / 2), f = i - row * (D / 2);
+    qx[u] = qy[u] = 0.f;
+    if (i < RK * (D / 2) && row < a.R) {
+      const int t = row / a.G, j = row - t * a.G;
+      const T* src = qb + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D;
+      qx[u] = to_f32<T>(src[f]);
+      qy[u] = to_f32<T>(src[f + D / 2]);
+    }
   }
   float2* cs = reinterpret_cast<float2*>(s.mo);
   for (int i = tid; i < a.n_q * (D / 2); i += NCT) {
@@ -51,20 +68,20 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
     cs[i] = make_float2(c, sn);
   }
   named_barrier(1, NCT);
-  const T* qb = static_cast<const T*>(a.q);
-  for (int i = tid; i < RK * (D / 2); i += NCT) {
-    const int row = i / (D / 2), f = i - row * (D / 2);
-    float xr = 0.f, yr = 0.f;
-    if (row < a.R) {
-      const int t = row / a.G, j = row - t * a.G;
-      const T* src = qb + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D;
-      const float x = to_f32<T>(src[f]), y = to_f32<T>(src[f + D / 2]);
-      const float2 c = cs[t * (D / 2) + f];
-      xr = (x * c.x - y * c.y) * mult;
-      yr = (y * c.x + x * c.y) * mult;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = tid + u * NCT;
+    if (i < RK * (D / 2)) {
+      const int row = i / (D / 2), f = i - row * (D / 2);
+      float xr = 0.f, yr = 0.f;
+      if (row < a.R) {
+        const float2 c = cs[(row / a.G) * (D / 2) + f];
+        xr = (qx[u] * c.x - qy[u] * c.y) * mult;
+        yr = (qy[u] * c.x + qx[u] * c.y) * mult;
+      }
+      s.q[row * D + f] = xr;
+      s.q[row * D + f + D / 2] = yr;
     }
-    s.q[row * D + f] = xr;
-    s.q[row * D + f + D / 2] = yr;
   }
   named_barrier(1, NCT);
 }
@@ -772,7 +789,7 @@ struct MmaEngine {
 
 // ---------------------------------------------------------------------------
 // Split merge, fused into the decode kernel.  Every piece adds its page count
-// to cnt[b, h]; the CTA whose addition completes the (b, h) total (both ranges)
+// to cnt[b, h]; the CTA whose addition completes the (b, h) total (all ranges)
 // is the last writer, and merges all pieces' partials: per softmax segment a
 // log-sum-exp merge, then for FOLD the far/local mix
 // (1 - lambda_eff) o_loc + lambda_eff o_far with lambda_eff = 0 when the far
@@ -780,7 +797,7 @@ struct MmaEngine {
 // controlled separately).  No CTA ever waits for another.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int32_t seq_pages(const int32_t* pfx, int b) {
-  return pfx[2 * b + 2] - pfx[2 * b];
+  return pfx[b + 1] - pfx[b];
 }
 
 // Running log-sum-exp merge state of one row and four dimensions.
@@ -820,8 +837,8 @@ struct MergeState {
 // one range into st; eight pieces' loads are in flight at a time.
 template <int D, int RK>
 __device__ __forceinline__ void merge_range(const DecodeArgs& a, int64_t i0, int64_t i1,
-                                            int step, int64_t sq, int64_t TP, bool dense, int r,
-                                            int c4, MergeState& st) {
+                                            int step, int64_t sq, int64_t TP, int64_t n_act,
+                                            bool dense, int r, int c4, MergeState& st) {
   constexpr int64_t SF = slot_floats(RK, D);
   for (int64_t i = i0; i <= i1; i += 8 * step) {
     float mm[8], ll[8];
@@ -832,7 +849,7 @@ __device__ __forceinline__ void merge_range(const DecodeArgs& a, int64_t i0, int
       mm[u] = -INFINITY;
       ll[u] = 0.f;
       oo[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ii <= i1 && (dense || cta_begin(ii, TP, a.n_cta) < cta_begin(ii + 1, TP, a.n_cta))) {
+      if (ii <= i1 && (dense || cta_begin(ii, TP, n_act) < cta_begin(ii + 1, TP, n_act))) {
         const float* base = a.part + (ii + sq) * SF;
         mm[u] = __ldcg(base + r);
         ll[u] = __ldcg(base + RK + r);
@@ -867,35 +884,39 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
   constexpr int ITEMS = RK * C4;
   constexpr int SPLIT = ITEMS >= NCT ? 1 : NCT / ITEMS;
   static_assert(SPLIT <= 32 && (SPLIT & (SPLIT - 1)) == 0, "split");
-  const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
-  const int64_t n_cta = a.n_cta;
-  const bool dense = TP >= n_cta;            // then no CTA's stretch is empty
+  const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
+  const int64_t n_act = active_ctas(TP, a.n_cta);
+  const bool dense = TP >= n_act;            // then no CTA's stretch is empty
   const bool fold = a.mode == DA_MODE_FOLD;
+  // Pieces of (b, h): FOLD keeps the far range (seq even) and the local range
+  // (seq odd) apart; every other mode has one segment over the head's line.
+  const int32_t nb = s.pfx[b + 1] - s.pfx[b];
+  const int32_t n0 = fold ? s.n0[b] : nb;
+  const int64_t x0 = (int64_t)s.pfx[b] * a.H_kv + (int64_t)h * nb;
+  const int64_t seq0 = ((int64_t)b * a.H_kv + h) * 2;
   int64_t i0[2], i1[2], sq[2];
+  const int64_t beg[2] = {x0, x0 + n0}, len[2] = {n0, nb - n0};
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
-    const int e = 2 * b + rr;
-    const int32_t n = s.pfx[e + 1] - s.pfx[e];
-    sq[rr] = (int64_t)e * a.H_kv + h;
-    if (n == 0) {
+    sq[rr] = seq0 + rr;
+    if (len[rr] == 0) {
       i0[rr] = 0;
       i1[rr] = -1;
     } else {
-      const int64_t x0 = (int64_t)s.pfx[e] * a.H_kv + (int64_t)h * n;
-      i0[rr] = cta_of(x0, TP, n_cta);
-      i1[rr] = cta_of(x0 + n - 1, TP, n_cta);
+      i0[rr] = cta_of(beg[rr], TP, n_act);
+      i1[rr] = cta_of(beg[rr] + len[rr] - 1, TP, n_act);
     }
   }
-  const float lam = (fold && s.pfx[2 * b + 1] > s.pfx[2 * b]) ? a.far_mix : 0.f;
+  const float lam = (fold && n0 > 0) ? a.far_mix : 0.f;
   const int sub = threadIdx.x & (SPLIT - 1);
   for (int item = threadIdx.x / SPLIT; item < a.R * C4; item += NCT / SPLIT) {
     const int r = item / C4, c4 = item - r * C4;
-    // range 0 (sinks, or FOLD far memory) and range 1 (window, local, or all)
+    // s0: FOLD far memory, or the whole selection; s1: FOLD local window
     MergeState s0, s1;
     s0.init();
     s1.init();
-    merge_range<D, RK>(a, i0[0] + sub, i1[0], SPLIT, sq[0], TP, dense, r, c4, s0);
-    merge_range<D, RK>(a, i0[1] + sub, i1[1], SPLIT, sq[1], TP, dense, r, c4, s1);
+    merge_range<D, RK>(a, i0[0] + sub, i1[0], SPLIT, sq[0], TP, n_act, dense, r, c4, s0);
+    merge_range<D, RK>(a, i0[1] + sub, i1[1], SPLIT, sq[1], TP, n_act, dense, r, c4, s1);
 #pragma unroll
     for (int mask = 1; mask < SPLIT; mask <<= 1) {
       s0.add_xor(mask);
@@ -924,8 +945,8 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
 // After a piece's partial is written: take the ticket, merge when last.
 template <typename T, int D, int RK, int NCT>
 __device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pages) {
-  const int e = seq / a.H_kv, h = seq - e * a.H_kv, b = e >> 1;
-  uint32_t* c = a.cnt + (int64_t)b * a.H_kv + h;
+  const int bh = seq >> 1, b = bh / a.H_kv, h = bh - b * a.H_kv;
+  uint32_t* c = a.cnt + (int64_t)bh;
   if (threadIdx.x == 0) {
     // Release: the partial the consumers wrote before the barrier in finish()
     // is visible before the count; acquire: when last, every other piece's
@@ -974,10 +995,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(NCW == kConsumerWarps, "consumer warps");
   const Layout L = make_layout(VARIANT, ES, D, RK, stages, a.B);
   Smem s = carve(smem_raw, L);
-  prologue<D, NCW>(a, s, L);
-  const int64_t TP = (int64_t)s.pfx[2 * a.B] * a.H_kv;
-  const int64_t xs = cta_begin(blockIdx.x, TP, a.n_cta);
-  const int64_t xe = cta_begin(blockIdx.x + 1, TP, a.n_cta);
+  prologue<D, ES, NCW>(a, s, L);
+  const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
+  const int64_t n_act = active_ctas(TP, a.n_cta);
+  const int64_t xs = blockIdx.x < n_act ? cta_begin(blockIdx.x, TP, n_act) : 0;
+  const int64_t xe = blockIdx.x < n_act ? cta_begin(blockIdx.x + 1, TP, n_act) : 0;
   const int warp = threadIdx.x >> 5;
   if (warp >= NCW) {
     regs_dec<kProducerRegs>();
@@ -990,9 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   zero_empty<T, D, NCT>(a, s);
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
-    int e, h, k;
-    locate(s.pfx, 2 * a.B, a.H_kv, xs, e, h, k);
-    prep_queries<T, D, RK, NCT>(a, s, e * a.H_kv + h);
+    const Where w = locate(s, a.B, a.H_kv, xs);
+    prep_queries<T, D, RK, NCT>(a, s, piece_seq(a.mode, w.b, w.h, a.H_kv, w.r));
     eng.begin(s);
   }
   const uint32_t base = smem_u32(s.stage);

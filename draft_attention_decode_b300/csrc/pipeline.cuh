@@ -17,7 +17,7 @@ namespace da {
 enum : int { kFirst = 1, kLast = 2, kValid = 4 };
 
 struct PageInfo {
-  int32_t seq;    // e * H_kv + h, e = 2 * b + range
+  int32_t seq;    // piece id: piece_seq(mode, b, h, H_kv, range)
   int32_t lohi;   // first and one-past-last valid key in the page
   int32_t flags;
   int32_t pad;
@@ -26,8 +26,8 @@ struct PageInfo {
 // Shared-memory layout (host and device agree on it).
 struct Layout {
   uint32_t stage_bytes, stages;
-  uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, flag_off,
-      total;
+  uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
+      flag_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -51,7 +51,8 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.bar_off = off;   off += align_up((uint32_t)stages * 16, 128);
   L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);
   L.len_off = off;   off += align_up((uint32_t)batch * 4, 128);
-  L.pfx_off = off;   off += align_up((uint32_t)(2 * batch + 1) * 4, 128);
+  L.pfx_off = off;   off += align_up((uint32_t)(batch + 1) * 4, 128);
+  L.n0_off = off;    off += align_up((uint32_t)batch * 4, 128);
   L.flag_off = off;  off += 128;
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
@@ -68,7 +69,8 @@ struct Smem {
   uint64_t* empty;
   double* invf;
   int32_t* len;
-  int32_t* pfx;
+  int32_t* pfx;         // [B + 1] pages per head of sequences before b
+  int32_t* n0;          // [B] pages per head of range 0
   int32_t* flag;        // broadcast of the merge ticket
 };
 
@@ -87,13 +89,14 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.invf = reinterpret_cast<double*>(p + L.invf_off);
   s.len = reinterpret_cast<int32_t*>(p + L.len_off);
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
+  s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
   s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
   return s;
 }
 
 // Prologue: context lengths and the page prefix over (b, range), computed
 // identically by every CTA.  All threads take part.
-template <int D, int NCW>
+template <int D, int ES, int NCW>
 __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
   grid_dep_launch_dependents();
@@ -108,17 +111,30 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   grid_dep_wait();   // global memory from here on
   for (int b = tid; b < a.B; b += blockDim.x)
     s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
+  // Small query tensors are pulled into L2 now, while the lengths load: the
+  // query preparation that follows then waits on L2, not on HBM.
+  {
+    const int64_t qbytes = (int64_t)a.B * a.n_q * a.H_q * D * ES;
+    const int64_t pbytes = (int64_t)a.B * a.n_q * 4;
+    if (qbytes <= (64 << 10))
+      for (int64_t off = (int64_t)tid * 128; off < qbytes; off += (int64_t)blockDim.x * 128)
+        prefetch_l2(static_cast<const char*>(a.q) + off);
+    if (pbytes <= (16 << 10))
+      for (int64_t off = (int64_t)tid * 128; off < pbytes; off += (int64_t)blockDim.x * 128)
+        prefetch_l2(reinterpret_cast<const char*>(a.q_pos) + off);
+  }
   __syncthreads();
   if (tid < 32) {
     const int lane = tid;
     int32_t carry = 0;
-    const int n = 2 * a.B;
-    for (int base = 0; base < n; base += 32) {
-      int e = base + lane;
+    for (int base = 0; base < a.B; base += 32) {
+      const int b = base + lane;
       int32_t v = 0;
-      if (e < n) {
-        Ranges r = mode_ranges(a.mode, s.len[e >> 1], a.W, a.n_sink);
-        v = (e & 1) ? range_pages(r.k0[1], r.k1[1]) : range_pages(r.k0[0], r.k1[0]);
+      if (b < a.B) {
+        const Ranges r = mode_ranges(a.mode, s.len[b], a.W, a.n_sink);
+        const int32_t n0 = range_pages(r.k0[0], r.k1[0]);
+        v = n0 + range_pages(r.k0[1], r.k1[1]);
+        s.n0[b] = n0;
       }
       int32_t inc = v;
 #pragma unroll
@@ -126,27 +142,35 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
         int32_t t = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += t;
       }
-      if (e < n) s.pfx[e] = carry + inc - v;
+      if (b < a.B) s.pfx[b] = carry + inc - v;
       carry += __shfl_sync(0xffffffffu, inc, 31);
     }
-    if (lane == 0) s.pfx[n] = carry;
+    if (lane == 0) s.pfx[a.B] = carry;
   }
   __syncthreads();
 }
 
-// Flat position -> (entry e = 2b + range, head h, page k inside the range).
-__device__ __forceinline__ void locate(const int32_t* pfx, int n_entries, int H, int64_t x,
-                                       int& e, int& h, int& k) {
-  int lo = 0, hi = n_entries - 1;  // largest e with pfx[e] * H <= x
+// Flat position -> (sequence b, head h, page k of the head's line, range r,
+// page kr inside that range).
+struct Where {
+  int b, h, k, r, kr;
+};
+__device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) {
+  int lo = 0, hi = B - 1;  // largest b with pfx[b] * H <= x
   while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if ((int64_t)pfx[mid] * H <= x) lo = mid; else hi = mid - 1;
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)s.pfx[mid] * H <= x) lo = mid; else hi = mid - 1;
   }
-  e = lo;
-  int64_t rel = x - (int64_t)pfx[e] * H;
-  int32_t n = pfx[e + 1] - pfx[e];
-  h = (int)(rel / n);
-  k = (int)(rel - (int64_t)h * n);
+  Where w;
+  w.b = lo;
+  const int64_t rel = x - (int64_t)s.pfx[lo] * H;
+  const int32_t nb = s.pfx[lo + 1] - s.pfx[lo];
+  w.h = (int)(rel / nb);
+  w.k = (int)(rel - (int64_t)w.h * nb);
+  const int32_t n0 = s.n0[lo];
+  w.r = w.k < n0 ? 0 : 1;
+  w.kr = w.r ? w.k - n0 : w.k;
+  return w;
 }
 
 // The producer warp: block-table translation and TMA issue for the CTA's
@@ -163,27 +187,27 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
     prefetch_tmap(mv);
     if (a.mode == DA_MODE_FOLD) prefetch_tmap(ms);
   }
-  const int n_entries = 2 * a.B;
+  const bool fold = a.mode == DA_MODE_FOLD;
   uint32_t n = 0;
   for (int64_t base = xs; base < xe; base += 32) {
     const int64_t x = base + lane;
     int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0;
     if (x < xe) {
-      int e, k;
-      locate(s.pfx, n_entries, a.H_kv, x, e, h, k);
-      const int b = e >> 1, r = e & 1;
-      const Ranges rg = mode_ranges(a.mode, s.len[b], a.W, a.n_sink);
-      const int32_t k0 = r ? rg.k0[1] : rg.k0[0], k1 = r ? rg.k1[1] : rg.k1[0];
-      const int32_t P = k0 / kPage + k;
+      const Where w = locate(s, a.B, a.H_kv, x);
+      const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
+      const int32_t k0 = w.r ? rg.k0[1] : rg.k0[0], k1 = w.r ? rg.k1[1] : rg.k1[0];
+      const int32_t P = k0 / kPage + w.kr;
       const int32_t pk0 = P * kPage;
       const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;
-      const int32_t npg = s.pfx[e + 1] - s.pfx[e];
-      seq = e * a.H_kv + h;
+      const int32_t nb = s.pfx[w.b + 1] - s.pfx[w.b], n0 = s.n0[w.b];
+      h = w.h;
+      seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
       lohi = lo | (hi << 16);
-      phys = phys_page(a.block_table, b, P, a.max_pages, a.num_pages, a.status);
-      flags = ((x == xs || k == 0) ? kFirst : 0) | ((x == xe - 1 || k == npg - 1) ? kLast : 0) |
-              (phys >= 0 ? kValid : 0);
-      far = range_is_far(a.mode, r) ? 1 : 0;
+      phys = phys_page(a.block_table, w.b, P, a.max_pages, a.num_pages, a.status);
+      const bool first = x == xs || w.k == 0 || (fold && w.k == n0);
+      const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
+      flags = (first ? kFirst : 0) | (last ? kLast : 0) | (phys >= 0 ? kValid : 0);
+      far = (fold && w.r == 0) ? 1 : 0;
     }
     const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
     for (int j = 0; j < cnt; ++j) {
