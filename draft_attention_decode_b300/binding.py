@@ -65,7 +65,8 @@ class da_params(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("num_ctas", ctypes.c_int32),
         ("engine", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("min_pages_per_cta", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -133,7 +134,7 @@ def header_functions(path: str = HEADER) -> list:
 def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
-                page_size=64, engine=0) -> da_params:
+                page_size=64, engine=0, min_pages_per_cta=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -145,6 +146,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.alpha, p.far_mix, p.scale_slope = float(alpha), float(far_mix), float(scale_slope)
     p.scale_ref, p.softmax_scale, p.num_ctas = int(scale_ref), float(softmax_scale), int(num_ctas)
     p.engine = ENGINE_HINTS[engine] if isinstance(engine, str) else int(engine)
+    p.min_pages_per_cta = int(min_pages_per_cta)
     return p
 
 

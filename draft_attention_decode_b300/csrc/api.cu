@@ -98,6 +98,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->n_ref = p.scale_ref;
   a->scale_log2 = pl->scale_log2;
   a->n_cta = p.num_ctas;
+  a->min_pages = p.min_pages_per_cta > 0 ? p.min_pages_per_cta : da::kMinPagesPerCta;
   for (int i = 0; i < 64; ++i) a->inv_freq[i] = pl->inv_freq[i];
 }
 
@@ -147,7 +148,8 @@ int draft_attn_check_params(const da_params* p) {
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return DA_ERR_INVALID_ARG;
   if (p->num_ctas < 0 || p->num_ctas > 65535) return DA_ERR_INVALID_ARG;
   if (p->engine < 0 || p->engine > 2) return DA_ERR_INVALID_ARG;
-  for (int i = 0; i < 5; ++i)
+  if (p->min_pages_per_cta < 0 || p->min_pages_per_cta > (1 << 20)) return DA_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
     if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;

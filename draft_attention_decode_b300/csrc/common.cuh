@@ -51,6 +51,7 @@ struct DecodeArgs {
   int32_t n_ref;
   float scale_log2;     // softmax scale * log2(e)
   int32_t n_cta;
+  int32_t min_pages;    // split floor (pages per active CTA)
   double inv_freq[64];  // theta^(-2i/d), i < d/2
 };
 
@@ -171,7 +172,7 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 // Flat work partition.  The pages of every (b, kv head) are laid end to end
 // (b outer, then head, then range 0 before range 1); with TP pages in all and
 // n active CTAs, CTA i takes positions [floor(i*TP/n), floor((i+1)*TP/n)).
-// n = min(grid, ceil(TP / kMinPagesPerCta)): a small selection (a window)
+// n = min(grid, ceil(TP / min_pages)): a small selection (a window)
 // goes to fewer, fuller CTAs, so that each (b, head) has few pieces to merge.
 // A "piece" is the part of one (b, head, softmax segment) that one CTA covers
 // (the two ranges of window mode are one segment; FOLD's far and local ranges
@@ -179,7 +180,7 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 // the line, so slot = cta + seq is unique: every new piece advances the CTA,
 // the seq, or both.
 // ---------------------------------------------------------------------------
-constexpr int kMinPagesPerCta = 4;
+constexpr int kMinPagesPerCta = 4;   // default split floor (da_params.min_pages_per_cta = 0)
 
 __host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int64_t n) {
   return (i * TP) / n;
@@ -188,8 +189,9 @@ __host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int
 __host__ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t TP, int64_t n) {
   return ((x + 1) * n - 1) / TP;
 }
-__host__ __device__ __forceinline__ int64_t active_ctas(int64_t TP, int64_t grid) {
-  const int64_t want = (TP + kMinPagesPerCta - 1) / kMinPagesPerCta;
+__host__ __device__ __forceinline__ int64_t active_ctas(int64_t TP, int64_t grid,
+                                                       int64_t min_pages) {
+  const int64_t want = (TP + min_pages - 1) / min_pages;
   return want < 1 ? 1 : (want < grid ? want : grid);
 }
 // Piece id of (b, head, range); FOLD keeps its two ranges apart.

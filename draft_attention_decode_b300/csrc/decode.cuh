@@ -885,7 +885,7 @@ __device__ inline void merge_sequence(const DecodeArgs& a, const Smem& s, int b,
   constexpr int SPLIT = ITEMS >= NCT ? 1 : NCT / ITEMS;
   static_assert(SPLIT <= 32 && (SPLIT & (SPLIT - 1)) == 0, "split");
   const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
-  const int64_t n_act = active_ctas(TP, a.n_cta);
+  const int64_t n_act = active_ctas(TP, a.n_cta, a.min_pages);
   const bool dense = TP >= n_act;            // then no CTA's stretch is empty
   const bool fold = a.mode == DA_MODE_FOLD;
   // Pieces of (b, h): FOLD keeps the far range (seq even) and the local range
@@ -997,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem s = carve(smem_raw, L);
   prologue<D, ES, NCW>(a, s, L);
   const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
-  const int64_t n_act = active_ctas(TP, a.n_cta);
+  const int64_t n_act = active_ctas(TP, a.n_cta, a.min_pages);
   const int64_t xs = blockIdx.x < n_act ? cta_begin(blockIdx.x, TP, n_act) : 0;
   const int64_t xe = blockIdx.x < n_act ? cta_begin(blockIdx.x + 1, TP, n_act) : 0;
   const int warp = threadIdx.x >> 5;

@@ -115,7 +115,10 @@ typedef struct {
   int32_t num_ctas;          /* persistent CTAs; 0 = one per SM (tests vary this)  */
   int32_t engine;            /* 0 automatic, 1 CUDA cores (<= 8 rows), 2 tensor
                                 cores (bf16 only); see DA_ENGINE_*                */
-  int32_t reserved[5];       /* must be zero                                       */
+  int32_t min_pages_per_cta; /* split floor: a call whose selection has P pages
+                                (over all sequences and KV heads) runs on
+                                min(num_ctas, ceil(P / this)) CTAs; 0 = default   */
+  int32_t reserved[4];       /* must be zero                                       */
 } da_params;
 
 typedef struct {
