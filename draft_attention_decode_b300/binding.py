@@ -66,7 +66,8 @@ class da_params(ctypes.Structure):
         ("num_ctas", ctypes.c_int32),
         ("engine", ctypes.c_int32),
         ("min_pages_per_cta", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("stages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -110,6 +111,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
                                                    I64, VP, VP]),
         "draft_attn_get_status": (ctypes.c_int, [VP, VP, P(ctypes.c_uint32)]),
+        "draft_attn_ring_size": (ctypes.c_int, [I32, I32, P(I32), P(I32)]),
+        "draft_attn_ring_block_table": (ctypes.c_int, [P(I32), I64, P(I32), I32, I32]),
         "draft_attn_error_string": (ctypes.c_char_p, [ctypes.c_int]),
         "draft_attn_version": (ctypes.c_int, []),
     }
@@ -134,7 +137,7 @@ def header_functions(path: str = HEADER) -> list:
 def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
-                page_size=64, engine=0, min_pages_per_cta=0) -> da_params:
+                page_size=64, engine=0, min_pages_per_cta=0, stages=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -147,6 +150,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.scale_ref, p.softmax_scale, p.num_ctas = int(scale_ref), float(softmax_scale), int(num_ctas)
     p.engine = ENGINE_HINTS[engine] if isinstance(engine, str) else int(engine)
     p.min_pages_per_cta = int(min_pages_per_cta)
+    p.stages = int(stages)
     return p
 
 
@@ -270,6 +274,28 @@ def draft_attn_debug_gather(plan, q_pos, ctx_lens, block_table, b, t, capacity, 
     res = {k: v[: min(n, cap)] for k, v in out.items()}
     res["count"] = n
     return res
+
+
+def draft_attn_ring_size(window, n_sink):
+    """Returns (n_ring, n_sink_pages): the smallest ring of pages that holds a
+    window-mode draft KV with this window and sink count."""
+    n_ring, n_sink_pages = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().draft_attn_ring_size(int(window), int(n_sink), ctypes.byref(n_ring),
+                                               ctypes.byref(n_sink_pages)), "draft_attn_ring_size")
+    return n_ring.value, n_sink_pages.value
+
+
+def draft_attn_ring_block_table(max_pages, ring_pages, n_sink_pages):
+    """One block-table row (int32 numpy array of max_pages entries) mapping
+    logical pages onto the ring of physical pages `ring_pages`."""
+    import numpy as np
+    ring = np.ascontiguousarray(np.asarray(ring_pages, dtype=np.int32))
+    table = np.empty(int(max_pages), dtype=np.int32)
+    I32p = ctypes.POINTER(ctypes.c_int32)
+    _check(load_library().draft_attn_ring_block_table(
+        table.ctypes.data_as(I32p), int(max_pages), ring.ctypes.data_as(I32p), int(ring.size),
+        int(n_sink_pages)), "draft_attn_ring_block_table")
+    return table
 
 
 def draft_attn_get_status(plan, stream=None):

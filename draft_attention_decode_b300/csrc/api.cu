@@ -144,12 +144,13 @@ int draft_attn_check_params(const da_params* p) {
   if ((int64_t)p->max_pages_per_seq * da::kPage >= (int64_t)1 << 31) return DA_ERR_INVALID_ARG;
   if (p->dtype != DA_DTYPE_BF16 && p->dtype != DA_DTYPE_FP32) return DA_ERR_INVALID_ARG;
   if (p->mode < DA_MODE_FULL || p->mode > DA_MODE_SHARP) return DA_ERR_INVALID_ARG;
-  if (!(p->rope_theta > 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
+  if (!(p->rope_theta >= 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return DA_ERR_INVALID_ARG;
   if (p->num_ctas < 0 || p->num_ctas > 65535) return DA_ERR_INVALID_ARG;
   if (p->engine < 0 || p->engine > 2) return DA_ERR_INVALID_ARG;
   if (p->min_pages_per_cta < 0 || p->min_pages_per_cta > (1 << 20)) return DA_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  if (p->stages != 0 && (p->stages < 2 || p->stages > 8)) return DA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
     if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;
@@ -190,7 +191,7 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   pl->num_sms = sms;
   pl->rows = (params->num_q_heads / params->num_kv_heads) * params->n_q;
   if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, params->engine,
-                         max_smem, &pl->choice)) {
+                         params->stages, max_smem, &pl->choice)) {
     delete pl;
     return DA_ERR_UNSUPPORTED;
   }
@@ -201,7 +202,9 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   const size_t slots = (size_t)pl->p.num_ctas + (size_t)2 * params->batch * params->num_kv_heads;
   pl->ws_bytes = pl->cnt_bytes + slots * (size_t)da::slot_floats(pl->choice.rk, d) * sizeof(float);
   for (int i = 0; i < 64; ++i)
-    pl->inv_freq[i] = i < d / 2 ? std::pow(params->rope_theta, -2.0 * i / d) : 0.0;
+    pl->inv_freq[i] = (i < d / 2 && params->rope_theta > 0.0)
+                          ? std::pow(params->rope_theta, -2.0 * i / d)
+                          : 0.0;  // theta = 0: NoPE, every angle is zero
   const double c = params->softmax_scale > 0.f ? (double)params->softmax_scale
                                                : 1.0 / std::sqrt((double)d);
   pl->scale_log2 = (float)(c * 1.4426950408889634074);  // log2(e)
@@ -319,6 +322,26 @@ int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* c
   return da::launch_gather(a, b, t, o, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DA_OK
              : DA_ERR_CUDA;
+}
+
+int draft_attn_ring_size(int32_t window, int32_t n_sink, int32_t* n_ring, int32_t* n_sink_pages) {
+  if (window < 1 || n_sink < 0 || !n_ring || !n_sink_pages) return DA_ERR_INVALID_ARG;
+  const int64_t sp = ((int64_t)n_sink + da::kPage - 1) / da::kPage;
+  const int64_t wp = ((int64_t)window + da::kPage - 1) / da::kPage + 1;
+  if (sp + wp > INT32_MAX) return DA_ERR_INVALID_ARG;
+  *n_sink_pages = (int32_t)sp;
+  *n_ring = (int32_t)(sp + wp);
+  return DA_OK;
+}
+
+int draft_attn_ring_block_table(int32_t* table, int64_t max_pages, const int32_t* ring_pages,
+                                int32_t n_ring, int32_t n_sink_pages) {
+  if (!table || !ring_pages || max_pages < 1 || n_sink_pages < 0 || n_ring <= n_sink_pages)
+    return DA_ERR_INVALID_ARG;
+  const int64_t cycle = n_ring - n_sink_pages;
+  for (int64_t j = 0; j < max_pages; ++j)
+    table[j] = j < n_sink_pages ? ring_pages[j] : ring_pages[n_sink_pages + (j - n_sink_pages) % cycle];
+  return DA_OK;
 }
 
 int draft_attn_get_status(da_plan_t pl, void* stream, uint32_t* bits) {

@@ -6,8 +6,8 @@
 
 namespace da {
 
-bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int max_smem,
-                   Choice* c) {
+bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int stages,
+                   int max_smem, Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
   // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
   // from 5 on, QK^T and PV are dense enough for an n8 tensor-core tile
@@ -26,7 +26,9 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int m
     c->rk = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
     c->variant = kVariantCore;
   }
-  for (int s = 4; s >= 2; --s) {
+  // Deepest pipeline that fits (a requested depth must fit as it is).
+  const int s_hi = stages > 0 ? stages : kMaxAutoStages, s_lo = stages > 0 ? stages : 2;
+  for (int s = s_hi; s >= s_lo; --s) {
     const Layout L = make_layout(c->variant, es, d, c->rk, s, batch);
     if ((int)L.total <= max_smem) {
       c->stages = s;

@@ -36,8 +36,8 @@ struct Choice {
 // Picks the kernel instance for `rows` query rows per KV head (engine_hint:
 // 0 automatic, 1 CUDA cores, 2 tensor cores); false when none exists or it
 // does not fit in `max_smem` bytes of shared memory.
-bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int max_smem,
-                   Choice* c);
+bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int stages,
+                   int max_smem, Choice* c);
 
 cudaError_t prepare_decode(const Choice& c, int dtype, int d);
 cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,

@@ -94,7 +94,7 @@ typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP32 = 1 } da_dtype;
 #define DA_ENGINE_MMA       1  /* 5..32 rows, bf16: m16n8k16 tensor-core path     */
 
 typedef struct {
-  double  rope_theta;        /* RoPE base theta, > 0                               */
+  double  rope_theta;        /* RoPE base theta, > 0; 0 = NoPE (no rotation)      */
   int32_t batch;             /* sequences, 1..1024                                 */
   int32_t n_q;               /* query tokens per sequence (draft-tree width)       */
   int32_t num_q_heads;       /* H_q, a multiple of num_kv_heads                    */
@@ -118,7 +118,9 @@ typedef struct {
   int32_t min_pages_per_cta; /* split floor: a call whose selection has P pages
                                 (over all sequences and KV heads) runs on
                                 min(num_ctas, ceil(P / this)) CTAs; 0 = default   */
-  int32_t reserved[4];       /* must be zero                                       */
+  int32_t stages;            /* shared-memory pipeline depth in pages, 2..8;
+                                0 = as deep as shared memory allows (<= 4)       */
+  int32_t reserved[3];       /* must be zero                                       */
 } da_params;
 
 typedef struct {
@@ -182,6 +184,28 @@ int draft_attn_run(da_plan_t plan, const void* q, const int32_t* q_pos,
                    const int32_t* ctx_lens, const int32_t* block_table,
                    const void* k_cache, const void* v_cache, const void* k_side,
                    void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Ring-buffer draft KV for window mode ("Windowed-MTP ...", Abstract: the
+ * draft KV outside the window is never read and can be reclaimed into a
+ * compact ring).  Window mode reads only the sink positions and the last W
+ * positions, so its pages can live in a ring: the first n_sink_pages logical
+ * pages keep pages of their own, every later logical page j maps to ring slot
+ * (j - n_sink_pages) mod (n_ring - n_sink_pages).  Appending position p then
+ * overwrites a page that no window read will touch again, provided the ring
+ * has at least draft_attn_ring_size() pages.  Both calls are host-only.
+ *
+ * draft_attn_ring_size: the smallest ring for window W and n_sink sinks:
+ *   *n_sink_pages = ceil(n_sink / page_size), *n_ring = *n_sink_pages +
+ *   ceil(W / page_size) + 1.  DA_ERR_INVALID_ARG for W < 1 or n_sink < 0.
+ * draft_attn_ring_block_table: fills the HOST array table[0 .. max_pages-1]
+ *   (one block-table row) from the HOST array ring_pages[0 .. n_ring-1] of
+ *   physical page ids.  DA_ERR_INVALID_ARG for null pointers, max_pages < 1,
+ *   n_sink_pages < 0 or n_ring <= n_sink_pages.  The mapping is only valid for
+ *   window mode with the same W and n_sink (full, sharp and FOLD read every
+ *   position). */
+int draft_attn_ring_size(int32_t window, int32_t n_sink, int32_t* n_ring, int32_t* n_sink_pages);
+int draft_attn_ring_block_table(int32_t* table, int64_t max_pages, const int32_t* ring_pages,
+                                int32_t n_ring, int32_t n_sink_pages);
 
 /* Size of the library-owned workspace that draft_attn_run_static uses
  * (8 MiB): enough for every shape up to 16 sequences x 8 KV heads x 32 rows

@@ -47,6 +47,8 @@ silent (all listed again in the design notes):
    gamma * c * <RoPE(q, p), K_rot_j>.
 6. Grouped-query attention: query head h reads KV head h // (H_q / H_kv).
 7. An empty selection gives a zero output.
+8. NoPE: rope_theta = 0 means no rotation at all (keys and queries enter the
+   dot product as stored), for the NoPE draft the Windowed-MTP abstract names.
 
 Arithmetic: float64 throughout (numpy).  Softmax is exp(s - max) / sum.
 """
@@ -86,8 +88,12 @@ class Params:
 # --------------------------------------------------------------------------
 
 def rope_inv_freq(d: int, theta: float) -> np.ndarray:
-    """inv_freq_i = theta^(-2i/d) for i < d/2, in float64."""
+    """inv_freq_i = theta^(-2i/d) for i < d/2, in float64.  theta = 0 selects
+    NoPE (no positional rotation: every frequency is zero), the draft of the
+    Mamba2-hybrid NoPE model in the Windowed-MTP abstract (reading 8)."""
     i = np.arange(d // 2, dtype=np.float64)
+    if theta == 0:
+        return np.zeros(d // 2)
     return np.power(np.float64(theta), -2.0 * i / d)
 
 

@@ -305,7 +305,34 @@ def check_page_slot(orc):
         assert phys[j] == bt[j // P] and slot[j] == j % P and flat[j] == bt[j // P] * P + j % P
 
 
-ALL_CHECKS = [check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
+def check_nope(orc):
+    """rope_theta = 0 is NoPE: the plain softmax-attention definition with no
+    rotation, written out here per key (full, window, FOLD)."""
+    rng = np.random.default_rng(21)
+    d, L = 8, 40
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    q = rng.standard_normal(d)
+    c = 1.0 / math.sqrt(d)
+
+    def plain(js, mult):
+        s = [mult * c * sum(q[i] * K[j][i] for i in range(d)) for j in js]
+        mx = max(s)
+        e = [math.exp(x - mx) for x in s]
+        return np.array([sum(e[n] * V[j][i] for n, j in enumerate(js)) / sum(e) for i in range(d)])
+
+    got = orc.attend_group(q[None], 977, K, V, L, orc.Params("full", rope_theta=0.0))[0]
+    assert np.allclose(got, plain(range(L), 1.0), atol=1e-12)
+    got = orc.attend_group(q[None], 5, K, V, L,
+                           orc.Params("window", window=10, n_sink=2, rope_theta=0.0))[0]
+    assert np.allclose(got, plain(list(range(2)) + list(range(30, 40)), 1.0), atol=1e-12)
+    got = orc.attend_group(q[None], L, K, V, L,
+                           orc.Params("fold", window=10, alpha=2.0, far_mix=0.4, rope_theta=0.0))[0]
+    want = 0.6 * plain(range(30, 40), 1.0) + 0.4 * plain(range(30), 2.0)
+    assert np.allclose(got, want, atol=1e-12)
+
+
+ALL_CHECKS = [check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
               check_brute_force, check_closed_forms, check_weights_sum,
               check_mode_equivalences, check_fold_shared_position, check_gqa,
               check_page_slot]

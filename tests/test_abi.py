@@ -56,7 +56,8 @@ def _ok_params(**kw):
     (dict(mode="fold", window=16, alpha=2.0, n_sink=4), -1),
     (dict(mode="sharp", scale_slope=-1.0), -1),
     (dict(mode="sharp", scale_ref=0), -1),
-    (dict(rope_theta=0.0), -1),
+    (dict(rope_theta=0.0), 0),                         # NoPE
+    (dict(rope_theta=-1.0), -1),
     (dict(rope_theta=float("inf")), -1),
     (dict(mode=7), -1),
     (dict(num_ctas=-3), -1),

@@ -37,6 +37,8 @@ MUTATIONS = {
     "rope_pairing": ("rope", _rope_adjacent_pairs),
     "inv_freq_missing_2": ("rope_inv_freq",
                            lambda d, theta: np.power(float(theta), -np.arange(d // 2) / d)),
+    "nope_ignored": ("rope_inv_freq",
+                     lambda d, theta: np.power(float(theta or 1e4), -2.0 * np.arange(d // 2) / d)),
     "window_off_by_one": ("window_start", lambda L, W: max(0, L - W + 1)),
     "far_position_off_by_one": ("fold_far_position", lambda L, W: L - W),
     "gamma_no_clamp": ("sharp_gamma", lambda n, b, r: 1.0 + b * math.log(max(n, 1) / r)),
