@@ -50,6 +50,11 @@ import torch  # noqa: E402
 from draft_attention_decode_b300 import workloads as WL  # noqa: E402
 
 METRIC = "draft-step attention µs and KV GB/s (% of HBM peak) vs context, full vs window"
+HEADLINE = "mtp_draft_128k"
+FLUSH_BYTES = 256 << 20
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
 class L2Flush:
@@ -65,11 +70,6 @@ class L2Flush:
     def fill_(self, v):
         self.w.fill_(v)
         torch.amax(self.r, dim=0, out=self.sink)
-HEADLINE = "mtp_draft_128k"
-FLUSH_BYTES = 256 << 20
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
 # ---------------------------------------------------------------------------

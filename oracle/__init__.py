@@ -6,5 +6,5 @@ baseline use it; the product path never does.
 from .draft_attn_oracle import (  # noqa: F401
     MODES, SEG_FAR, SEG_LOCAL, Params, append_rotated_keys, attend, attend_group,
     fold_far_position, page_slot, rope, rope_angles, rope_inv_freq, round_to_bf16,
-    select_keys, selection_list, sharp_gamma, window_start,
+    select_keys, selection_list, sharp_gamma, tree_filter, window_start,
 )

@@ -49,6 +49,12 @@ silent (all listed again in the design notes):
 7. An empty selection gives a zero output.
 8. NoPE: rope_theta = 0 means no rotation at all (keys and queries enter the
    dot product as stored), for the NoPE draft the Windowed-MTP abstract names.
+9. Draft trees (EAGLE-style dynamic trees and DFlash blocks, which the FOLD
+   and SharpDraft pages name as drafters): the last n_tree keys of a context
+   are the tree's own tokens, key L-n_tree+i being tree token i at its own
+   slot position.  A query sees the mode's selection with the tree keys
+   restricted to those whose bit i is set in its mask (its ancestors and
+   itself); SharpDraft's |S| counts the keys the query actually sees.
 
 Arithmetic: float64 throughout (numpy).  Softmax is exp(s - max) / sum.
 """
@@ -80,6 +86,7 @@ class Params:
     scale_ref: int = 4096     # SharpDraft reference cardinality N_ref
     rope_theta: float = 10000.0
     softmax_scale: float = 0.0  # 0 => 1/sqrt(d)
+    n_tree: int = 0           # draft-tree tokens at the end of the context (reading 9)
     extra: dict = field(default_factory=dict)
 
 
@@ -169,15 +176,27 @@ def page_slot(positions, block_table_row, page_size: int = 64):
     return phys, slot, phys * page_size + slot
 
 
+def tree_filter(positions, L: int, n_tree: int, tree_mask):
+    """Drops the tree keys (positions >= L - n_tree) whose bit is clear in
+    tree_mask (an int; None keeps every key).  Reading 9."""
+    positions = np.asarray(positions, dtype=np.int64)
+    if tree_mask is None or n_tree <= 0:
+        return positions
+    base = L - n_tree
+    keep = [j < base or (int(tree_mask) >> int(j - base)) & 1 == 1 for j in positions]
+    return positions[np.asarray(keep, dtype=bool)] if positions.size else positions
+
+
 def selection_list(mode: str, L: int, p: int, prm: Params, block_table_row=None,
-                   page_size: int = 64) -> dict:
+                   page_size: int = 64, tree_mask=None) -> dict:
     """Per selected key: position, segment, the RoPE position its key is
     rotated at (j, or P_far for far keys), the position the query is rotated by
     when the key side is left as stored (p, or p - P_far for far keys, from
     <R(p)q, R(P)k> = <R(p-P)q, k>), and optionally the paged address.
     Sorted by position (positions are unique within one selection)."""
     sel = select_keys(mode, L, prm.window, prm.n_sink)
-    loc, far = sel["loc"], sel["far"]
+    loc = tree_filter(sel["loc"], L, prm.n_tree, tree_mask)
+    far = tree_filter(sel["far"], L, prm.n_tree, tree_mask)
     pos = np.concatenate([far, loc])
     seg = np.concatenate([np.full(far.size, SEG_FAR, np.int8),
                           np.full(loc.size, SEG_LOCAL, np.int8)])
@@ -242,13 +261,14 @@ def _weighted_sum(w: np.ndarray, v: np.ndarray, chunk: int) -> np.ndarray:
 
 
 def attend_group(q_rows, p: int, k_raw, v, L: int, prm: Params,
-                 chunk: int = 1 << 16, return_weights: bool = False):
+                 chunk: int = 1 << 16, return_weights: bool = False, tree_mask=None):
     """Attention of several query rows that share one query position p and one
     KV head.
 
     q_rows: [n_rows, d] un-rotated queries.  k_raw, v: [>= L, d] un-rotated keys
-    and values of that KV head, indexed by logical position.  Returns
-    o: [n_rows, d] float64 (and, optionally, the effective per-key weights).
+    and values of that KV head, indexed by logical position.  tree_mask: the
+    query's visible tree keys (reading 9; None: all).  Returns o: [n_rows, d]
+    float64 (and, optionally, the effective per-key weights).
     """
     q_rows = np.atleast_2d(np.asarray(q_rows, dtype=np.float64))
     n_rows, d = q_rows.shape
@@ -256,7 +276,8 @@ def attend_group(q_rows, p: int, k_raw, v, L: int, prm: Params,
     theta = prm.rope_theta
     q_rot = rope(q_rows, p, theta)
     sel = select_keys(prm.mode, L, prm.window, prm.n_sink)
-    loc, far = sel["loc"], sel["far"]
+    loc = tree_filter(sel["loc"], L, prm.n_tree, tree_mask)
+    far = tree_filter(sel["far"], L, prm.n_tree, tree_mask)
 
     gamma = 1.0
     if prm.mode == "sharp":
@@ -290,13 +311,14 @@ def attend_group(q_rows, p: int, k_raw, v, L: int, prm: Params,
 
 
 def attend(q, q_pos, k_raw, v, ctx_lens, prm: Params, rows=None,
-           chunk: int = 1 << 16) -> np.ndarray:
+           chunk: int = 1 << 16, tree_masks=None) -> np.ndarray:
     """Draft attention for a batch.
 
     q: [B, n_q, H_q, d]; q_pos: [B, n_q]; k_raw[b], v[b]: [>= L_b, H_kv, d]
     (un-rotated keys and values by logical position, any float dtype; a list or
     an array); ctx_lens: [B].  ``rows`` optionally restricts the computation to
-    a list of (b, t, h) query rows (others are left NaN).  Returns
+    a list of (b, t, h) query rows (others are left NaN).  tree_masks[b][t]:
+    the visible tree keys of query t (reading 9).  Returns
     [B, n_q, H_q, d] float64.
     """
     q = np.asarray(q)
@@ -316,7 +338,8 @@ def attend(q, q_pos, k_raw, v, ctx_lens, prm: Params, rows=None,
                     continue
                 kb = np.asarray(k_raw[b])[:, g, :]
                 vb = np.asarray(v[b])[:, g, :]
-                o = attend_group(q[b, t, heads, :], p, kb, vb, L, prm, chunk=chunk)
+                tm = None if tree_masks is None else int(tree_masks[b][t])
+                o = attend_group(q[b, t, heads, :], p, kb, vb, L, prm, chunk=chunk, tree_mask=tm)
                 out[b, t, heads, :] = o
     return out
 

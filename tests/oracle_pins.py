@@ -42,7 +42,7 @@ def bf_member(mode, j, L, W, n_sink):
 
 
 def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
-                  beta=0.0, n_ref=4096, theta=1e4):
+                  beta=0.0, n_ref=4096, theta=1e4, n_tree=0, tree_mask=None):
     """One query row by brute force: per-key loops, math.exp, Python floats."""
     d = len(q)
     c = 1.0 / math.sqrt(d)
@@ -50,6 +50,10 @@ def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
     segs = {"loc": [], "far": []}
     for j in range(L):
         m = bf_member(mode, j, L, W, n_sink)
+        # a draft-tree key counts only if the query's mask bit for it is set
+        if m is not None and tree_mask is not None and j >= L - n_tree:
+            if not (tree_mask >> (j - (L - n_tree))) & 1:
+                m = None
         if m is not None:
             segs[m].append(j)
     gamma = 1.0
@@ -305,6 +309,35 @@ def check_page_slot(orc):
         assert phys[j] == bt[j // P] and slot[j] == j % P and flat[j] == bt[j // P] * P + j % P
 
 
+def check_tree_masks(orc):
+    """Draft-tree masks: brute force per key, every mode; an all-ones mask is
+    no mask; a mask hiding every tree key is attention over the cache part."""
+    rng = np.random.default_rng(17)
+    d, L, nt = 8, 50, 6
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    q = rng.standard_normal(d)
+    for mode, kw, bkw in (("full", {}, {}), ("window", dict(window=12, n_sink=2), dict(W=12, n_sink=2)),
+                          ("fold", dict(window=10, alpha=2.0, far_mix=0.3),
+                           dict(W=10, alpha=2.0, lam=0.3)),
+                          ("sharp", dict(scale_slope=0.4, scale_ref=8), dict(beta=0.4, n_ref=8))):
+        for mask in (0b101001, 0b1, 0b111111, 0):
+            prm = orc.Params(mode=mode, n_tree=nt, rope_theta=1e4, **kw)
+            got = orc.attend_group(q[None], L + 1, K, V, L, prm, tree_mask=mask)[0]
+            want, _, _ = bf_attend_row(mode, list(q), L + 1, K.tolist(), V.tolist(), L,
+                                       n_tree=nt, tree_mask=mask, **bkw)
+            assert np.max(np.abs(got - np.array(want))) < 1e-12, (mode, mask)
+        prm = orc.Params(mode=mode, n_tree=nt, **kw)
+        allv = orc.attend_group(q[None], L, K, V, L, prm, tree_mask=(1 << nt) - 1)
+        assert np.array_equal(allv, orc.attend_group(q[None], L, K, V, L, prm))
+    prm = orc.Params("full", n_tree=nt)
+    none = orc.attend_group(q[None], L, K, V, L, prm, tree_mask=0)
+    assert np.allclose(none, orc.attend_group(q[None], L, K, V, L - nt, orc.Params("full")),
+                       atol=1e-14)
+    sl = orc.selection_list("full", L, L, prm, tree_mask=0b100)
+    assert list(sl["position"]) == list(range(L - nt)) + [L - nt + 2]
+
+
 def check_nope(orc):
     """rope_theta = 0 is NoPE: the plain softmax-attention definition with no
     rotation, written out here per key (full, window, FOLD)."""
@@ -332,7 +365,7 @@ def check_nope(orc):
     assert np.allclose(got, want, atol=1e-12)
 
 
-ALL_CHECKS = [check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
+ALL_CHECKS = [check_tree_masks, check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
               check_brute_force, check_closed_forms, check_weights_sum,
               check_mode_equivalences, check_fold_shared_position, check_gqa,
               check_page_slot]

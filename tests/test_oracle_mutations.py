@@ -40,6 +40,9 @@ MUTATIONS = {
     "nope_ignored": ("rope_inv_freq",
                      lambda d, theta: np.power(float(theta or 1e4), -2.0 * np.arange(d // 2) / d)),
     "window_off_by_one": ("window_start", lambda L, W: max(0, L - W + 1)),
+    "tree_bit_off_by_one": ("tree_filter", lambda pos, L, nt, m: (
+        np.asarray(pos, dtype=np.int64) if m is None or nt <= 0 else np.asarray(
+            [j for j in pos if j < L - nt or (int(m) >> int(j - (L - nt) + 1)) & 1], dtype=np.int64))),
     "far_position_off_by_one": ("fold_far_position", lambda L, W: L - W),
     "gamma_no_clamp": ("sharp_gamma", lambda n, b, r: 1.0 + b * math.log(max(n, 1) / r)),
     "gamma_log2": ("sharp_gamma", lambda n, b, r: max(1.0, 1 + b * math.log2(max(n, 1) / r))),
