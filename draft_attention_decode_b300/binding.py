@@ -67,7 +67,8 @@ class da_params(ctypes.Structure):
         ("engine", ctypes.c_int32),
         ("min_pages_per_cta", ctypes.c_int32),
         ("stages", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("tree_size", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -107,8 +108,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "draft_attn_plan_destroy": (None, [VP]),
         "draft_attn_append_kv": (ctypes.c_int, [VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP]),
         "draft_attn_run": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+        "draft_attn_run_tree": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ,
+                                               VP]),
         "draft_attn_run_static": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP]),
-        "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
+        "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
                                                    I64, VP, VP]),
         "draft_attn_get_status": (ctypes.c_int, [VP, VP, P(ctypes.c_uint32)]),
         "draft_attn_ring_size": (ctypes.c_int, [I32, I32, P(I32), P(I32)]),
@@ -137,7 +140,7 @@ def header_functions(path: str = HEADER) -> list:
 def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
-                page_size=64, engine=0, min_pages_per_cta=0, stages=0) -> da_params:
+                page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -151,6 +154,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.engine = ENGINE_HINTS[engine] if isinstance(engine, str) else int(engine)
     p.min_pages_per_cta = int(min_pages_per_cta)
     p.stages = int(stages)
+    p.tree_size = int(tree_size)
     return p
 
 
@@ -242,6 +246,23 @@ def draft_attn_run(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_si
         _stream(stream)), "draft_attn_run")
 
 
+def draft_attn_run_tree(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask,
+                        out, workspace, stream=None) -> None:
+    """tree_mask: int64 tensor [batch, n_q] holding each query's uint64 mask
+    of visible draft-tree keys (bit i: tree token i), or None (all visible)."""
+    for name, t in (("q_pos", q_pos), ("ctx_lens", ctx_lens), ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if tree_mask is not None and tree_mask.dtype not in (torch.int64, torch.uint64):
+        raise ValueError("tree_mask must be a 64-bit integer tensor")
+    if workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
+    _check(load_library().draft_attn_run_tree(
+        plan, _ptr(q), _ptr(q_pos), _ptr(ctx_lens), _ptr(block_table), _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_side), _ptr(tree_mask), _ptr(out), _ptr(workspace),
+        workspace.numel(), _stream(stream)), "draft_attn_run_tree")
+
+
 def draft_attn_run_static(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, out,
                           stream=None) -> None:
     """draft_attn_run with the library's own fixed device workspace: for
@@ -254,7 +275,8 @@ def draft_attn_run_static(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cach
         _ptr(v_cache), _ptr(k_side), _ptr(out), _stream(stream)), "draft_attn_run_static")
 
 
-def draft_attn_debug_gather(plan, q_pos, ctx_lens, block_table, b, t, capacity, stream=None) -> dict:
+def draft_attn_debug_gather(plan, q_pos, ctx_lens, block_table, b, t, capacity, stream=None,
+                            tree_mask=None) -> dict:
     dev = q_pos.device
     cap = int(capacity)
     out = {
@@ -266,7 +288,7 @@ def draft_attn_debug_gather(plan, q_pos, ctx_lens, block_table, b, t, capacity, 
     }
     count = torch.zeros(1, dtype=torch.int64, device=dev)
     _check(load_library().draft_attn_debug_gather(
-        plan, _ptr(q_pos), _ptr(ctx_lens), _ptr(block_table), int(b), int(t),
+        plan, _ptr(q_pos), _ptr(ctx_lens), _ptr(block_table), _ptr(tree_mask), int(b), int(t),
         _ptr(out["position"]), _ptr(out["phys_slot"]), _ptr(out["key_rope_pos"]),
         _ptr(out["q_rope_pos"]), _ptr(out["segment"]), cap, _ptr(count), _stream(stream)),
         "draft_attn_debug_gather")
@@ -330,11 +352,15 @@ class DraftAttention:
                              stream)
 
     def run(self, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side=None, out=None,
-            stream=None):
+            stream=None, tree_mask=None):
         if out is None:
             out = torch.empty_like(q)
-        draft_attn_run(self.plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, out,
-                       self.workspace, stream)
+        if tree_mask is None:
+            draft_attn_run(self.plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side,
+                           out, self.workspace, stream)
+        else:
+            draft_attn_run_tree(self.plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
+                                k_side, tree_mask, out, self.workspace, stream)
         return out
 
     def status(self, stream=None):

@@ -92,6 +92,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->mode = p.mode;
   a->W = p.window;
   a->n_sink = p.mode == DA_MODE_WINDOW ? p.n_sink : 0;
+  a->n_tree = p.tree_size;
   a->alpha = p.alpha;
   a->far_mix = p.far_mix;
   a->beta = p.scale_slope;
@@ -150,7 +151,11 @@ int draft_attn_check_params(const da_params* p) {
   if (p->engine < 0 || p->engine > 2) return DA_ERR_INVALID_ARG;
   if (p->min_pages_per_cta < 0 || p->min_pages_per_cta > (1 << 20)) return DA_ERR_INVALID_ARG;
   if (p->stages != 0 && (p->stages < 2 || p->stages > 8)) return DA_ERR_INVALID_ARG;
-  for (int i = 0; i < 3; ++i)
+  if (p->tree_size < 0 || p->tree_size > 64) return DA_ERR_INVALID_ARG;
+  if (p->tree_size > 0 && (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) &&
+      p->tree_size > p->window)
+    return DA_ERR_INVALID_ARG;
+  for (int i = 0; i < 2; ++i)
     if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;
@@ -269,6 +274,15 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
                    const int32_t* block_table, const void* k_cache, const void* v_cache,
                    const void* k_side, void* out, void* workspace, size_t workspace_bytes,
                    void* stream) {
+  return draft_attn_run_tree(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side,
+                             nullptr, out, workspace, workspace_bytes, stream);
+}
+
+int draft_attn_run_tree(da_plan_t pl, const void* q, const int32_t* q_pos,
+                        const int32_t* ctx_lens, const int32_t* block_table,
+                        const void* k_cache, const void* v_cache, const void* k_side,
+                        const uint64_t* tree_mask, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   if (!pl || !q || !q_pos || !ctx_lens || !block_table || !k_cache || !v_cache || !out ||
       !workspace)
     return DA_ERR_INVALID_ARG;
@@ -294,6 +308,7 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
   a.q_pos = q_pos;
   a.ctx_lens = ctx_lens;
   a.block_table = block_table;
+  a.tree_mask = pl->p.tree_size > 0 ? tree_mask : nullptr;
   a.out = out;
   a.cnt = static_cast<uint32_t*>(workspace);
   a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->cnt_bytes);
@@ -304,7 +319,8 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
 }
 
 int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* ctx_lens,
-                            const int32_t* block_table, int32_t b, int32_t t, int32_t* positions,
+                            const int32_t* block_table, const uint64_t* tree_mask, int32_t b,
+                            int32_t t, int32_t* positions,
                             int64_t* phys_slot, int32_t* key_rope_pos, int32_t* q_rope_pos,
                             int8_t* segment, int64_t capacity, int64_t* count, void* stream) {
   if (!pl || !q_pos || !ctx_lens || !block_table || !count || capacity < 0) return DA_ERR_INVALID_ARG;
@@ -318,6 +334,7 @@ int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* c
   a.q_pos = q_pos;
   a.ctx_lens = ctx_lens;
   a.block_table = block_table;
+  a.tree_mask = pl->p.tree_size > 0 ? tree_mask : nullptr;
   da::GatherOut o{positions, phys_slot, key_rope_pos, q_rope_pos, segment, capacity, count};
   return da::launch_gather(a, b, t, o, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DA_OK

@@ -91,22 +91,42 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Dec
   const Ranges rg = mode_ranges(a.mode, L, a.W, a.n_sink);
   const int64_t n0 = rg.k1[0] > rg.k0[0] ? rg.k1[0] - rg.k0[0] : 0;
   const int64_t n1 = rg.k1[1] > rg.k0[1] ? rg.k1[1] - rg.k0[1] : 0;
-  const int64_t total = n0 + n1;
+  const int64_t dense = n0 + n1;
+  // Draft-tree keys (the last `present` keys, all of them in the selection)
+  // are kept only where the query's mask bit is set; they come last, so the
+  // kept ones are compacted by a popcount of the lower bits.
+  const bool masked = a.tree_mask != nullptr && a.n_tree > 0;
+  const uint64_t m = masked ? (uint64_t)__ldg(reinterpret_cast<const unsigned long long*>(a.tree_mask) +
+                                              b * a.n_q + t)
+                            : ~0ull;
+  const int32_t present = masked ? min(a.n_tree, L) : 0;
+  const int32_t base = L - a.n_tree;              // position of tree token 0
+  const int32_t lo_bit = a.n_tree - present;
+  const uint64_t valid = present == 0 ? 0ull
+                         : ((present >= 64 ? ~0ull : ((1ull << present) - 1)) << lo_bit);
+  const int64_t n_before = dense - present;
+  const int64_t total = n_before + __popcll(m & valid);
   if (blockIdx.x == 0 && threadIdx.x == 0) *o.count = total;
-  const int64_t lim = total < o.capacity ? total : o.capacity;
   const int32_t pf = fold_far_pos(L, a.W);
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < lim;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < dense;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int rr = idx < n0 ? 0 : 1;
     const int32_t j = (rr ? rg.k0[1] : rg.k0[0]) + (int32_t)(idx < n0 ? idx : idx - n0);
+    int64_t out = idx;
+    if (idx >= n_before) {
+      const int i = j - base;
+      if (!((m >> i) & 1ull)) continue;
+      out = n_before + __popcll(m & valid & ((1ull << i) - 1));
+    }
+    if (out >= o.capacity) continue;
     const bool far = range_is_far(a.mode, rr);
     const int32_t pg = j / kPage;
     const int32_t phys = phys_page(a.block_table, b, pg, a.max_pages, a.num_pages, a.status);
-    o.positions[idx] = j;
-    o.phys_slot[idx] = phys < 0 ? -1 : (int64_t)phys * kPage + (j - pg * kPage);
-    o.key_rope_pos[idx] = far ? pf : j;
-    o.q_rope_pos[idx] = far ? p - pf : p;
-    o.segment[idx] = far ? 1 : 0;
+    o.positions[out] = j;
+    o.phys_slot[out] = phys < 0 ? -1 : (int64_t)phys * kPage + (j - pg * kPage);
+    o.key_rope_pos[out] = far ? pf : j;
+    o.q_rope_pos[out] = far ? p - pf : p;
+    o.segment[out] = far ? 1 : 0;
   }
 }
 

@@ -39,6 +39,7 @@ struct DecodeArgs {
   const int32_t* q_pos;
   const int32_t* ctx_lens;
   const int32_t* block_table;
+  const uint64_t* tree_mask;  // [B][n_q] visible tree keys per query, or null (all)
   void* out;
   float* part;          // partial (m, l, o) slots
   uint32_t* cnt;        // per-(b, kv head) count of pages finished; the CTA that
@@ -47,6 +48,7 @@ struct DecodeArgs {
   int32_t B, n_q, H_q, H_kv, G, R;  // R = G * n_q rows per KV head
   int32_t max_pages, num_pages;
   int32_t mode, W, n_sink;
+  int32_t n_tree;       // tree tokens at the end of each context
   float alpha, far_mix, beta;
   int32_t n_ref;
   float scale_log2;     // softmax scale * log2(e)

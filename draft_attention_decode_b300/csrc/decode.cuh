@@ -25,22 +25,39 @@ namespace da {
 // ---------------------------------------------------------------------------
 // Query preparation for a piece: RoPE at the query position (or at
 // q_pos - P_far for FOLD far memory, which equals rotating the keys at P_far:
-// <R(p)q, R(P)k> = <R(p-P)q, k>), times the logit multiplier, into s.q
-// [rk][d] as FP32.  Rows >= R are zero.  Consumer threads only.
+// <R(p)q, R(P)k> = <R(p-P)q, k>), times the row's logit multiplier, into s.q
+// [rk][d] as FP32, and each row's draft-tree mask into s.tmask.  Rows >= R
+// are zero.  Consumer threads only.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int RK, int NCT>
 __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
   const int tid = threadIdx.x;
   const int bh = seq >> 1, b = bh / a.H_kv, h = bh - b * a.H_kv;
   const int32_t L = s.len[b];
-  float mult = a.scale_log2;
-  int32_t shift = 0;
-  if (seq_is_far(a.mode, seq)) {
-    mult *= a.alpha;                     // "FOLD", abstract: concentration factor
-    shift = fold_far_pos(L, a.W);
-  } else if (a.mode == DA_MODE_SHARP) {  // "SharpDraft", Abstract: query scaling
-    const int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
-    if (n > 0) mult *= fmaxf(1.f, 1.f + a.beta * logf((float)n / (float)a.n_ref));
+  const bool far = seq_is_far(a.mode, seq);
+  const int32_t shift = far ? fold_far_pos(L, a.W) : 0;
+  // Row masks and multipliers.  A tree key hidden from a row also leaves that
+  // row's SharpDraft count |S| (every tree key lies in the main selection).
+  if (tid < RK) {
+    const int row = tid;
+    uint64_t m = ~0ull;
+    if (row < a.R && a.tree_mask && a.n_tree > 0)
+      m = __ldg(reinterpret_cast<const unsigned long long*>(a.tree_mask) + b * a.n_q + row / a.G);
+    s.tmask[row] = m;
+    float mult = a.scale_log2;
+    if (far) {
+      mult *= a.alpha;                       // "FOLD", abstract: concentration factor
+    } else if (a.mode == DA_MODE_SHARP) {    // "SharpDraft", Abstract: query scaling
+      int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
+      if (a.tree_mask && a.n_tree > 0) {
+        const int32_t present = min(a.n_tree, L);   // tree tokens that exist
+        const uint64_t bits = (present >= 64 ? ~0ull : ((1ull << present) - 1))
+                              << (a.n_tree - present);
+        n -= present - __popcll(m & bits);
+      }
+      if (n > 0) mult *= fmaxf(1.f, 1.f + a.beta * logf((float)n / (float)a.n_ref));
+    }
+    s.rmult[row] = mult;
   }
   // The query elements this thread rotates are loaded first, so that their
   // latency overlaps the position loads and the angle table.
@@ -76,6 +93,7 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
       float xr = 0.f, yr = 0.f;
       if (row < a.R) {
         const float2 c = cs[(row / a.G) * (D / 2) + f];
+        const float mult = s.rmult[row];
         xr = (qx[u] * c.x - qy[u] * c.y) * mult;
         yr = (qy[u] * c.x + qx[u] * c.y) * mult;
       }
@@ -87,6 +105,13 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// Whether a row with tree mask m sees key `key` of a page whose key k is tree
+// token k + toff (toff = kNoTree: no tree key under a mask in this page).
+__device__ __forceinline__ bool tree_visible(int key, int toff, uint64_t m) {
+  const int ti = key + toff;
+  return (unsigned)ti >= 64u || ((m >> ti) & 1ull) != 0;
+}
 
 // Reduce-scatter of RK per-lane partial sums over the W lanes of a key group
 // (lane bits below log2 W): afterwards lane ds holds the total for row
@@ -188,6 +213,7 @@ struct CoreEngine {
   float2 o2[RK][DQ / 2];
   float m_run, l_run;    // row ds & (RK-1): reference maximum, partial sum
   uint32_t off[2][NCH];  // swizzled byte offsets of the lane's chunks, pass 0/1
+  uint64_t tm;           // draft-tree mask of row ds & (RK-1)
   int lane, warp, kg, ds;
 
   __device__ __forceinline__ int chunk_of(int i) const {
@@ -229,14 +255,16 @@ struct CoreEngine {
           const int d0 = dim_of(i, 2 * e);
           q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0], s.q[r * D + d0 + 1]);
         }
+    tm = s.tmask[ds & (RK - 1)];
     reset();
   }
 
-  // NP consecutive pages of one piece: K/V stage addresses and valid key
-  // ranges [lo, hi) inside each page.
+  // NP consecutive pages of one piece: K/V stage addresses, valid key ranges
+  // [lo, hi) inside each page and tree offsets.
   template <int NP>
   __device__ __forceinline__ void pages(const uint32_t (&kb)[NP], const uint32_t (&vb)[NP],
-                                        const int (&lo)[NP], const int (&hi)[NP]) {
+                                        const int (&lo)[NP], const int (&hi)[NP],
+                                        const int (&toff)[NP]) {
     constexpr int NIT = 2 * NP;
     float sc[NIT];
     bool ok[NIT];
@@ -263,7 +291,7 @@ struct CoreEngine {
 #pragma unroll
       for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
       const float sr = reduce_scatter<RK, LPK>(v, ds);
-      sc[it] = ok[it] ? sr : -INFINITY;
+      sc[it] = (ok[it] && tree_visible(key, toff[pg], tm)) ? sr : -INFINITY;
     }
     // Row maximum over the warp's keys (lanes with the same ds).
     float mx = sc[0];
@@ -318,10 +346,11 @@ struct CoreEngine {
     }
   }
 
-  __device__ __forceinline__ void page(const Smem&, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+  __device__ __forceinline__ void page(const Smem&, uint32_t kbase, uint32_t vbase, int lo, int hi,
+                                       int toff) {
     const uint32_t kb[1] = {kbase}, vb[1] = {vbase};
-    const int l[1] = {lo}, h[1] = {hi};
-    pages<1>(kb, vb, l, h);
+    const int l[1] = {lo}, h[1] = {hi}, o[1] = {toff};
+    pages<1>(kb, vb, l, h, o);
   }
 
   // Sum the key groups, merge the consumer warps, write the piece's partial.
@@ -401,6 +430,7 @@ struct CoreEngineWide {
   float2 q2[RK][DQ / 2];
   float2 o2[RK][DPL / 2];
   float m_run, l_run;
+  uint64_t tm;           // draft-tree mask of row ds & (RK-1)
   int lane, warp, kg, ds;
 
   __device__ __forceinline__ void init() {
@@ -434,6 +464,7 @@ struct CoreEngineWide {
         for (int e = 0; e < EPC / 2; ++e)
           q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0 + 2 * e], s.q[r * D + d0 + 2 * e + 1]);
     }
+    tm = s.tmask[ds & (RK - 1)];
     reset();
   }
 
@@ -458,7 +489,8 @@ struct CoreEngineWide {
         o2[r][e] = ffma2(make_float2(pj[r], pj[r]), make_float2(v[2 * e], v[2 * e + 1]), o2[r][e]);
   }
 
-  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi,
+                                       int toff) {
     const int wk0 = warp * 8;
     float sc[2];
 #pragma unroll
@@ -483,7 +515,7 @@ struct CoreEngineWide {
 #pragma unroll
       for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
       const float sr = reduce_scatter8<RK>(v, ds);
-      sc[it] = (key >= lo && key < hi) ? sr : -INFINITY;
+      sc[it] = (key >= lo && key < hi && tree_visible(key, toff, tm)) ? sr : -INFINITY;
     }
     // Online softmax for row ds & (RK-1) over the warp's 8 keys.
     float mx = fmaxf(sc[0], sc[1]);
@@ -612,6 +644,7 @@ struct MmaEngine {
   uint32_t qf[KS][NT][2];
   float O[KS][NT][4];
   float m[NT][2], l[NT][2];
+  uint64_t tmr[NT][2];  // draft-tree masks of the lane's rows (8 nt + 2 t + cc)
   int lane, warp, kb, grp, g, t;
 
   __device__ __forceinline__ void init() {
@@ -650,10 +683,15 @@ struct MmaEngine {
         qf[ks][nt][0] = pack_bf16(qr[0], qr[1]);
         qf[ks][nt][1] = pack_bf16(qr[8], qr[9]);
       }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) tmr[nt][cc] = s.tmask[row0 + 8 * nt + 2 * t + cc];
     reset();
   }
 
-  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi) {
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi,
+                                       int toff) {
     const int key0 = 16 * kb;
     if (hi <= key0 || lo >= key0 + 16) return;
     float S[NT][4];
@@ -679,8 +717,9 @@ struct MmaEngine {
       float P[4];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const float v0 = oka ? S[nt][cc] : -INFINITY;
-        const float v1 = okb ? S[nt][cc + 2] : -INFINITY;
+        const float v0 = (oka && tree_visible(key0 + g, toff, tmr[nt][cc])) ? S[nt][cc] : -INFINITY;
+        const float v1 =
+            (okb && tree_visible(key0 + g + 8, toff, tmr[nt][cc])) ? S[nt][cc + 2] : -INFINITY;
         float mx = fmaxf(v0, v1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -1029,6 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kb0 = base + st * L.stage_bytes;
     const int lo0 = (inf.flags & kValid) ? (inf.lohi & 0xffff) : 0;
     const int hi0 = (inf.flags & kValid) ? (inf.lohi >> 16) : 0;
+    const int to0 = inf.toff;
     bool last = (inf.flags & kLast) != 0;
     uint32_t taken = 1;
     if constexpr (Engine::kPairs) {
@@ -1042,7 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vb[2] = {kb0 + NCB * kBoxBytes, kb1 + NCB * kBoxBytes};
         const int lo[2] = {lo0, (inf1.flags & kValid) ? (inf1.lohi & 0xffff) : 0};
         const int hi[2] = {hi0, (inf1.flags & kValid) ? (inf1.lohi >> 16) : 0};
-        eng.template pages<2>(kb, vb, lo, hi);
+        const int to[2] = {to0, inf1.toff};
+        eng.template pages<2>(kb, vb, lo, hi, to);
         __syncwarp();
         if ((threadIdx.x & 31) == 0) {
           mbar_arrive(&s.empty[st]);
@@ -1053,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (taken == 1) {
-      if (hi0 > lo0 && eng.owns(n)) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0);
+      if (hi0 > lo0 && eng.owns(n)) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
     }

@@ -16,18 +16,21 @@ namespace da {
 
 enum : int { kFirst = 1, kLast = 2, kValid = 4 };
 
+// Tree offset of a page with no draft-tree key under a mask.
+constexpr int32_t kNoTree = -(1 << 30);
+
 struct PageInfo {
   int32_t seq;    // piece id: piece_seq(mode, b, h, H_kv, range)
   int32_t lohi;   // first and one-past-last valid key in the page
   int32_t flags;
-  int32_t pad;
+  int32_t toff;   // key k of the page is tree token k + toff (when in [0, 64))
 };
 
 // Shared-memory layout (host and device agree on it).
 struct Layout {
   uint32_t stage_bytes, stages;
   uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
-      flag_off, total;
+      flag_off, tm_off, rm_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -54,6 +57,8 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.pfx_off = off;   off += align_up((uint32_t)(batch + 1) * 4, 128);
   L.n0_off = off;    off += align_up((uint32_t)batch * 4, 128);
   L.flag_off = off;  off += 128;
+  L.tm_off = off;    off += align_up((uint32_t)rk * 8, 128);
+  L.rm_off = off;    off += align_up((uint32_t)rk * 4, 128);
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
 }
@@ -72,6 +77,8 @@ struct Smem {
   int32_t* pfx;         // [B + 1] pages per head of sequences before b
   int32_t* n0;          // [B] pages per head of range 0
   int32_t* flag;        // broadcast of the merge ticket
+  uint64_t* tmask;      // [rk] visible tree keys of each row of the current piece
+  float* rmult;         // [rk] logit multiplier of each row of the current piece
 };
 
 __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
@@ -91,6 +98,8 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
   s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
   s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
+  s.tmask = reinterpret_cast<uint64_t*>(p + L.tm_off);
+  s.rmult = reinterpret_cast<float*>(p + L.rm_off);
   return s;
 }
 
@@ -191,7 +200,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
   uint32_t n = 0;
   for (int64_t base = xs; base < xe; base += 32) {
     const int64_t x = base + lane;
-    int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0;
+    int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree;
     if (x < xe) {
       const Where w = locate(s, a.B, a.H_kv, x);
       const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
@@ -208,6 +217,10 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
       flags = (first ? kFirst : 0) | (last ? kLast : 0) | (phys >= 0 ? kValid : 0);
       far = (fold && w.r == 0) ? 1 : 0;
+      if (a.tree_mask && a.n_tree > 0 && !far) {
+        const int32_t t0 = s.len[w.b] - a.n_tree;   // position of tree token 0
+        if (pk0 + kPage > t0) toff = pk0 - t0;
+      }
     }
     const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
     for (int j = 0; j < cnt; ++j) {
@@ -217,11 +230,12 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const int32_t jphys = __shfl_sync(0xffffffffu, phys, j);
       const int32_t jfar = __shfl_sync(0xffffffffu, far, j);
       const int32_t jh = __shfl_sync(0xffffffffu, h, j);
+      const int32_t jtoff = __shfl_sync(0xffffffffu, toff, j);
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
         if (mbar_wait(&s.empty[st], par ^ 1u, a.status)) {
-          s.info[st] = PageInfo{jseq, jlohi, jflags, 0};
+          s.info[st] = PageInfo{jseq, jlohi, jflags, jtoff};
           uint8_t* kdst = s.stage + st * L.stage_bytes;
           uint8_t* vdst = kdst + NCB * kBoxBytes;
           if (jflags & kValid) {

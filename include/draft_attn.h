@@ -120,7 +120,10 @@ typedef struct {
                                 min(num_ctas, ceil(P / this)) CTAs; 0 = default   */
   int32_t stages;            /* shared-memory pipeline depth in pages, 2..8;
                                 0 = as deep as shared memory allows (<= 4)       */
-  int32_t reserved[3];       /* must be zero                                       */
+  int32_t tree_size;         /* draft-tree tokens at the end of each context,
+                                0..64 (<= window in window and FOLD modes); the
+                                per-query masks go to draft_attn_run_tree        */
+  int32_t reserved[2];       /* must be zero                                       */
 } da_params;
 
 typedef struct {
@@ -185,6 +188,21 @@ int draft_attn_run(da_plan_t plan, const void* q, const int32_t* q_pos,
                    const void* k_cache, const void* v_cache, const void* k_side,
                    void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* draft_attn_run for a draft tree (EAGLE-style dynamic trees, DFlash blocks:
+ * drafters the FOLD and SharpDraft pages name).  The last params.tree_size
+ * keys of every context are the tree's own tokens: key L - tree_size + i is
+ * tree token i, appended at its slot position and rotated there.
+ * tree_mask: DEVICE uint64 [batch][n_q]; bit i of tree_mask[b][t] says whether
+ * query t of sequence b sees tree token i (its ancestors and itself).  Every
+ * other selected key is seen as in draft_attn_run; SharpDraft's |S| counts the
+ * keys the query sees.  tree_mask = NULL means every tree key is visible
+ * (draft_attn_run is exactly that).  Bits at or above tree_size are ignored. */
+int draft_attn_run_tree(da_plan_t plan, const void* q, const int32_t* q_pos,
+                        const int32_t* ctx_lens, const int32_t* block_table,
+                        const void* k_cache, const void* v_cache, const void* k_side,
+                        const uint64_t* tree_mask, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Ring-buffer draft KV for window mode ("Windowed-MTP ...", Abstract: the
  * draft KV outside the window is never read and can be reclaimed into a
  * compact ring).  Window mode reads only the sink positions and the last W
@@ -236,7 +254,8 @@ int draft_attn_run_static(da_plan_t plan, const void* q, const int32_t* q_pos,
                           void* out, void* stream);
 
 /* Test hook: the keys query token t of sequence b selects, computed by the
- * same device routines as draft_attn_run.  Per key, ascending by position:
+ * same device routines as draft_attn_run_tree (tree_mask: as there, may be
+ * NULL).  Per key, ascending by position:
  * positions (int32), phys_slot = physical_page * page_size + slot (int64, -1
  * for an invalid block-table entry), key_rope_pos (the position the key is
  * rotated at: its own, or P_far for FOLD far keys), q_rope_pos (the position
@@ -244,7 +263,8 @@ int draft_attn_run_static(da_plan_t plan, const void* q, const int32_t* q_pos,
  * segment (0 main/local, 1 FOLD far).  At most `capacity` entries are written;
  * *count (device int64) receives the total. */
 int draft_attn_debug_gather(da_plan_t plan, const int32_t* q_pos, const int32_t* ctx_lens,
-                            const int32_t* block_table, int32_t b, int32_t t,
+                            const int32_t* block_table, const uint64_t* tree_mask, int32_t b,
+                            int32_t t,
                             int32_t* positions, int64_t* phys_slot, int32_t* key_rope_pos,
                             int32_t* q_rope_pos, int8_t* segment, int64_t capacity,
                             int64_t* count, void* stream);

@@ -25,7 +25,7 @@ class Setup:
     def __init__(self, *, batch, n_q, num_q_heads, num_kv_heads, head_dim, dtype, ctx,
                  mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0, scale_slope=0.0,
                  scale_ref=4096, rope_theta=1e4, num_ctas=0, seed=0, extra_tokens=0,
-                 spare_pages=3, q_pos=None, fill=True, engine=0):
+                 spare_pages=3, q_pos=None, fill=True, engine=0, tree_size=0):
         self.dev = torch.device("cuda", 0)
         self.dtype = dtype
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -50,7 +50,7 @@ class Setup:
             head_dim=head_dim, num_pages=npg, max_pages_per_seq=bt.shape[1], dtype=dtype,
             mode=mode, window=window, n_sink=n_sink, alpha=alpha, far_mix=far_mix,
             scale_slope=scale_slope, scale_ref=scale_ref, rope_theta=rope_theta,
-            num_ctas=num_ctas, engine=engine)
+            num_ctas=num_ctas, engine=engine, tree_size=tree_size)
         shape = (npg, num_kv_heads, WL.PAGE, head_dim)
         # NaN-filled so that a read of a slot nobody wrote shows up in the output
         self.k_cache = torch.full(shape, float("nan"), dtype=tdt, device=self.dev)
@@ -59,7 +59,7 @@ class Setup:
                        if mode == "fold" else None)
         self.prm = orc.Params(mode=mode, window=window, n_sink=n_sink if mode == "window" else 0,
                               alpha=alpha, far_mix=far_mix, scale_slope=scale_slope,
-                              scale_ref=scale_ref, rope_theta=rope_theta)
+                              scale_ref=scale_ref, rope_theta=rope_theta, n_tree=tree_size)
         if fill:
             for b, c in enumerate(self.ctx):
                 self.append(b, 0, c)
@@ -74,19 +74,19 @@ class Setup:
         self.da.append_kv(k, v, pos, self.block_table[b:b + 1], self.k_cache, self.v_cache,
                           self.k_side)
 
-    def run(self, q=None, q_pos=None, ctx_lens=None):
+    def run(self, q=None, q_pos=None, ctx_lens=None, tree_mask=None):
         out = self.da.run(self.q if q is None else q, self.q_pos if q_pos is None else q_pos,
                           self.ctx_lens if ctx_lens is None else ctx_lens, self.block_table,
-                          self.k_cache, self.v_cache, self.k_side)
+                          self.k_cache, self.v_cache, self.k_side, tree_mask=tree_mask)
         torch.cuda.synchronize()
         return out
 
     def status(self):
         return self.da.status()
 
-    def oracle(self, groups=None, q=None, q_pos=None, ctx=None):
+    def oracle(self, groups=None, q=None, q_pos=None, ctx=None, tree_masks=None):
         """Float64 oracle output [B, n_q, H_q, d] (NaN outside `groups`, a list
-        of (b, t, kv_head))."""
+        of (b, t, kv_head)); tree_masks[b][t]: the query's visible tree keys."""
         q = (self.q if q is None else q).float().cpu().numpy().astype(np.float64)
         qp = (self.q_pos if q_pos is None else q_pos).cpu().numpy()
         ctx = self.ctx if ctx is None else ctx
@@ -106,8 +106,9 @@ class Setup:
                                  self.v[b][:n, g].float().cpu().numpy())
             kb, vb = cache[(b, g)]
             heads = slice(g * G, (g + 1) * G)
+            tm = None if tree_masks is None else int(tree_masks[b][t])
             out[b, t, heads] = orc.attend_group(q[b, t, heads], int(qp[b, t]), kb, vb, L,
-                                                self.prm)
+                                                self.prm, tree_mask=tm)
         return out
 
     def close(self):

@@ -69,6 +69,11 @@ def _ok_params(**kw):
     (dict(engine="cuda_core", num_q_heads=64), 0),     # 8 rows forced onto CUDA cores
     (dict(engine="mma", dtype="fp32"), -2),            # tensor-core path is bf16 only
     (dict(engine=3), -1),
+    (dict(tree_size=8), 0),
+    (dict(tree_size=65), -1),
+    (dict(tree_size=-1), -1),
+    (dict(mode="window", window=16, tree_size=32), -1),   # tree must fit in the window
+    (dict(mode="fold", window=64, alpha=2.0, far_mix=0.5, tree_size=64), 0),
 ])
 def test_check_params(kw, code):
     assert B.draft_attn_check_params(_ok_params(**kw)) == code
@@ -76,7 +81,7 @@ def test_check_params(kw, code):
 
 def test_reserved_must_be_zero():
     p = _ok_params()
-    p.reserved[2] = 1
+    p.reserved[1] = 1
     assert B.draft_attn_check_params(p) == -1
 
 
