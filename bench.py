@@ -8,8 +8,8 @@ Workload of the headline line: the MTP draft head decode at 128K context --
 batch 1, 32 query / 8 KV heads, head_dim 128, bf16 N(0,1) keys and values in a
 paged cache (64-token pages, shuffled block table), 4 sequential draft steps
 that each append one token (KV append + RoPE) and then attend with the query
-at that token.  One timed step is that 4-step draft loop, replayed from a CUDA
-graph; full and window (W = 2048) modes are timed separately, and `value` is
+at that token, each step one draft_attn_step launch.  One timed step is that
+4-step draft loop, replayed from a CUDA graph; full and window (W = 2048) modes are timed separately, and `value` is
 the full-mode KV GB/s (the KV bytes the mode must read, divided by the loop
 time).  The L2 cache is flushed between timed steps (a 256 MiB write, then a
 256 MiB read so no dirty lines are left for the timed step to write back).
@@ -235,7 +235,7 @@ class DraftLoop:
         self.out = torch.empty_like(self.q[0])
         self.plans = {m: self._plan(m) for m in modes}
 
-    def _plan(self, mode):
+    def _plan(self, mode, engine=0):
         wl = self.wl
         return self.B.DraftAttention(
             device=self.dev.index or 0, batch=wl.batch, n_q=wl.n_q,
@@ -243,20 +243,27 @@ class DraftLoop:
             num_pages=self.npg, max_pages_per_seq=self.bt.shape[1], dtype=wl.dtype, mode=mode,
             window=wl.window_for(mode), n_sink=wl.sinks_for(mode), alpha=wl.alpha,
             far_mix=wl.far_mix, scale_slope=wl.scale_slope, scale_ref=wl.scale_ref,
-            rope_theta=wl.rope_theta)
+            rope_theta=wl.rope_theta, engine=engine)
 
     # -- one draft loop through the C ABI --------------------------------
-    def loop(self, mode, lens=None):
+    def loop(self, mode, lens=None, fused=True):
+        """fused: each draft step is one draft_attn_step launch (append +
+        attend); otherwise draft_attn_append_kv then draft_attn_run."""
         da = self.plans[mode]
         for s in range(self.steps):
+            L = self.lens[s] if lens is None else lens
+            if self.wl.draft_steps and fused:
+                da.step(self.k_new[s], self.v_new[s], self.pos[s], self.q[s], self.qpos[s], L,
+                        self.bt, self.k_cache, self.v_cache, self.k_side, out=self.out)
+                continue
             if self.wl.draft_steps:
                 da.append_kv(self.k_new[s], self.v_new[s], self.pos[s], self.bt, self.k_cache,
                              self.v_cache, self.k_side)
-            da.run(self.q[s], self.qpos[s], self.lens[s] if lens is None else lens, self.bt,
-                   self.k_cache, self.v_cache, self.k_side, out=self.out)
+            da.run(self.q[s], self.qpos[s], L, self.bt, self.k_cache, self.v_cache, self.k_side,
+                   out=self.out)
 
-    def launches_per_loop(self):
-        per = 1 + (1 if self.wl.draft_steps else 0)   # decode (+ append)
+    def launches_per_loop(self, fused=True):
+        per = 1 + (1 if self.wl.draft_steps and not fused else 0)   # decode (+ append)
         return per * self.steps
 
     def kv_bytes(self, mode, lens=None):
@@ -272,16 +279,16 @@ class DraftLoop:
                 tot += selected_keys(mode, Lb, wl.window_for(mode), wl.sinks_for(mode)) * per_tok
         return tot
 
-    def capture(self, mode, lens=None):
+    def capture(self, mode, lens=None, fused=True):
         g = torch.cuda.CUDAGraph()
         st = torch.cuda.Stream()
         st.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(st):
-            self.loop(mode, lens)            # warm (plans, lazy module loads)
+            self.loop(mode, lens, fused)     # warm (plans, lazy module loads)
         torch.cuda.current_stream().wait_stream(st)
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
-            self.loop(mode, lens)
+            self.loop(mode, lens, fused)
         torch.cuda.synchronize()
         return g
 
@@ -478,8 +485,8 @@ def e2e_full(dl: DraftLoop, steps, warmup, dist):
             dq.copy_(hq[s], non_blocking=True); dk.copy_(hk[s], non_blocking=True)
             dv.copy_(hv[s], non_blocking=True); dp.copy_(hp[s], non_blocking=True)
             dqp.copy_(hqp[s], non_blocking=True); dln.copy_(hl[s], non_blocking=True)
-            da.append_kv(dk, dv, dp, dl.bt, dl.k_cache, dl.v_cache, dl.k_side)
-            da.run(dq, dqp, dln, dl.bt, dl.k_cache, dl.v_cache, dl.k_side, out=dl.out)
+            da.step(dk, dv, dp, dq, dqp, dln, dl.bt, dl.k_cache, dl.v_cache, dl.k_side,
+                    out=dl.out)
             hout.copy_(dl.out, non_blocking=True)
             torch.cuda.current_stream().synchronize()   # the draft head needs the output
     for _ in range(warmup):
@@ -522,6 +529,14 @@ def run_ours(args, dist):
                   "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
     torch.cuda.profiler.stop()
     clk = clocks.stop()
+    # the same loops with a separate append launch per draft step
+    two = {}
+    for m in ("full", "window"):
+        g2 = dl.capture(m, fused=False)
+        ms, _ = time_graph(g2, args.steps, args.warmup, flush, dist)
+        two[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 3),
+                  "kv_gbs": round(dl.kv_bytes(m) / (ms * 1e-3) / 1e9, 1)}
+        del g2
 
     # roofline of the dominant kernel: the full-mode attention call of the
     # last draft step, timed on its own launch stream
@@ -537,9 +552,19 @@ def run_ours(args, dist):
                 "bytes_per_launch": call_bytes, "us_per_launch": round(ms_call * 1e3, 2),
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs copy bandwidth)"}
 
+    # the 4-row shape on the tensor cores (an n8 tile half padding), for comparison
+    mma = dl._plan("full", engine="mma")
+    ms_mma = time_calls(lambda: mma.run(dl.q[-1], dl.qpos[-1], Lr, dl.bt, dl.k_cache, dl.v_cache,
+                                        None, out=dl.out), max(args.steps, 10), args.warmup,
+                        flush, dist)
+    mma.close()
+    engines = {"cuda_core_us": round(ms_call * 1e3, 2), "tensor_core_padded_us":
+               round(ms_mma * 1e3, 2), "note": "attention call alone, full mode; the default "
+               "keeps <= 4 rows per KV head on the CUDA cores"}
+
     e2e_s, h2d, d2h = e2e_full(dl, max(args.steps // 4, 5), args.warmup, dist)
     e2e_val = res["full"]["kv_bytes_per_loop"] / e2e_s / 1e9
-    launches = dl.launches_per_loop() * args.steps * 2
+    launches = dl.launches_per_loop(fused=True) * args.steps * 2
     dl.close()
     del dl, graphs
     torch.cuda.empty_cache()
@@ -559,6 +584,8 @@ def run_ours(args, dist):
         "modes": {m: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
                   for m, r in res.items()},
         "window_speedup_vs_full": round(res["full"]["ms_per_loop"] / res["window"]["ms_per_loop"], 2),
+        "modes_separate_append": two,
+        "engines": engines,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -110,6 +110,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "draft_attn_run": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
         "draft_attn_run_tree": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ,
                                                VP]),
+        "draft_attn_step": (ctypes.c_int, [VP, VP, VP, VP, I32, VP, VP, VP, VP, VP, VP, VP, VP, VP,
+                                           VP, SZ, VP]),
         "draft_attn_run_static": (ctypes.c_int, [VP, VP, VP, VP, VP, VP, VP, VP, VP, VP]),
         "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
                                                    I64, VP, VP]),
@@ -263,6 +265,24 @@ def draft_attn_run_tree(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
         workspace.numel(), _stream(stream)), "draft_attn_run_tree")
 
 
+def draft_attn_step(plan, k_new, v_new, pos, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
+                    k_side, out, workspace, tree_mask=None, stream=None) -> None:
+    """Append k_new / v_new [batch, n_new, H_kv, d] at pos [batch, n_new] and
+    attend, in one launch."""
+    n_new = int(k_new.shape[1]) if k_new is not None else 0
+    for name, t in (("q_pos", q_pos), ("ctx_lens", ctx_lens), ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if n_new and (pos.dtype != torch.int32 or tuple(pos.shape) != tuple(k_new.shape[:2])):
+        raise ValueError("pos must be int32 [batch, n_new]")
+    if workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
+    _check(load_library().draft_attn_step(
+        plan, _ptr(k_new), _ptr(v_new), _ptr(pos), n_new, _ptr(q), _ptr(q_pos), _ptr(ctx_lens),
+        _ptr(block_table), _ptr(k_cache), _ptr(v_cache), _ptr(k_side), _ptr(tree_mask), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "draft_attn_step")
+
+
 def draft_attn_run_static(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, out,
                           stream=None) -> None:
     """draft_attn_run with the library's own fixed device workspace: for
@@ -361,6 +381,14 @@ class DraftAttention:
         else:
             draft_attn_run_tree(self.plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
                                 k_side, tree_mask, out, self.workspace, stream)
+        return out
+
+    def step(self, k_new, v_new, pos, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
+             k_side=None, out=None, stream=None, tree_mask=None):
+        if out is None:
+            out = torch.empty_like(q)
+        draft_attn_step(self.plan, k_new, v_new, pos, q, q_pos, ctx_lens, block_table, k_cache,
+                        v_cache, k_side, out, self.workspace, tree_mask, stream)
         return out
 
     def status(self, stream=None):

@@ -278,11 +278,21 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
                              nullptr, out, workspace, workspace_bytes, stream);
 }
 
-int draft_attn_run_tree(da_plan_t pl, const void* q, const int32_t* q_pos,
-                        const int32_t* ctx_lens, const int32_t* block_table,
-                        const void* k_cache, const void* v_cache, const void* k_side,
-                        const uint64_t* tree_mask, void* out, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+struct AppendIn {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int32_t* pos = nullptr;
+  int32_t n_new = 0;
+};
+
+int run_impl(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
+             const int32_t* block_table, const void* k_cache, const void* v_cache,
+             const void* k_side, const uint64_t* tree_mask, void* out, void* workspace,
+             size_t workspace_bytes, void* stream, const AppendIn& app) {
   if (!pl || !q || !q_pos || !ctx_lens || !block_table || !k_cache || !v_cache || !out ||
       !workspace)
     return DA_ERR_INVALID_ARG;
@@ -312,10 +322,51 @@ int draft_attn_run_tree(da_plan_t pl, const void* q, const int32_t* q_pos,
   a.out = out;
   a.cnt = static_cast<uint32_t*>(workspace);
   a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->cnt_bytes);
+  if (app.n_new > 0) {
+    a.k_new = app.k_new;
+    a.v_new = app.v_new;
+    a.new_pos = app.pos;
+    a.n_new = app.n_new;
+    a.kc_w = const_cast<void*>(k_cache);
+    a.vc_w = const_cast<void*>(v_cache);
+    a.ks_w = const_cast<void*>(k_side);
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, a, mk, mv, ms, st) != cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int draft_attn_run_tree(da_plan_t pl, const void* q, const int32_t* q_pos,
+                        const int32_t* ctx_lens, const int32_t* block_table,
+                        const void* k_cache, const void* v_cache, const void* k_side,
+                        const uint64_t* tree_mask, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return run_impl(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask, out,
+                  workspace, workspace_bytes, stream, AppendIn{});
+}
+
+int draft_attn_step(da_plan_t pl, const void* k_new, const void* v_new, const int32_t* pos,
+                    int32_t n_new, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
+                    const int32_t* block_table, void* k_cache, void* v_cache, void* k_side,
+                    const uint64_t* tree_mask, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (n_new < 0) return DA_ERR_INVALID_ARG;
+  if (n_new > 32) return DA_ERR_UNSUPPORTED;
+  AppendIn app;
+  if (n_new > 0) {
+    if (!pl || !k_new || !v_new || !pos) return DA_ERR_INVALID_ARG;
+    app.k_new = k_new;
+    app.v_new = v_new;
+    app.pos = pos;
+    app.n_new = n_new;
+  }
+  return run_impl(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask, out,
+                  workspace, workspace_bytes, stream, app);
 }
 
 int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* ctx_lens,

@@ -54,6 +54,15 @@ struct DecodeArgs {
   float scale_log2;     // softmax scale * log2(e)
   int32_t n_cta;
   int32_t min_pages;    // split floor (pages per active CTA)
+  // Fused append (draft_attn_step): n_new tokens per sequence, written into the
+  // caches by the CTA that reads their page (or round-robin when none does).
+  const void* k_new;    // [B][n_new][H_kv][D]
+  const void* v_new;
+  const int32_t* new_pos;  // [B][n_new], < 0 skips the token
+  void* kc_w;           // K cache, V cache, FOLD side cache (may be null) to write
+  void* vc_w;
+  void* ks_w;
+  int32_t n_new;        // 0: no append
   double inv_freq[64];  // theta^(-2i/d), i < d/2
 };
 

@@ -203,6 +203,20 @@ int draft_attn_run_tree(da_plan_t plan, const void* q, const int32_t* q_pos,
                         const uint64_t* tree_mask, void* out, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* One draft step in one launch: exactly draft_attn_append_kv(k_new, v_new,
+ * pos, batch = params.batch, n_new) followed by draft_attn_run_tree, as the
+ * draft head hands over its query and its new key/value together.  Each new
+ * token is written (rotated K, side K when k_side is given, V) by the CTA that
+ * reads its page in this call, before that CTA loads the page; tokens no CTA
+ * reads are written by the others.  n_new in 0..32 (0: no append);
+ * ctx_lens already count the new tokens, as for draft_attn_run.  k_side is
+ * required in FOLD mode.  DA_ERR_UNSUPPORTED for n_new > 32. */
+int draft_attn_step(da_plan_t plan, const void* k_new, const void* v_new, const int32_t* pos,
+                    int32_t n_new, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
+                    const int32_t* block_table, void* k_cache, void* v_cache, void* k_side,
+                    const uint64_t* tree_mask, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Ring-buffer draft KV for window mode ("Windowed-MTP ...", Abstract: the
  * draft KV outside the window is never read and can be reclaimed into a
  * compact ring).  Window mode reads only the sink positions and the last W
