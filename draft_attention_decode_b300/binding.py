@@ -268,7 +268,7 @@ def draft_attn_run_tree(plan, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
 def draft_attn_step(plan, k_new, v_new, pos, q, q_pos, ctx_lens, block_table, k_cache, v_cache,
                     k_side, out, workspace, tree_mask=None, stream=None) -> None:
     """Append k_new / v_new [batch, n_new, H_kv, d] at pos [batch, n_new] and
-    attend, in one launch."""
+    attend, in one call (append kernel, then the attention kernel behind it)."""
     n_new = int(k_new.shape[1]) if k_new is not None else 0
     for name, t in (("q_pos", q_pos), ("ctx_lens", ctx_lens), ("block_table", block_table)):
         if t.dtype != torch.int32:

@@ -21,7 +21,7 @@ struct da_plan_s {
   size_t cnt_bytes;
   size_t ws_bytes;
   uint32_t* status;
-  double inv_freq[64];
+  float2 turn_freq[64];   // theta^(-2i/d) / 2pi, split into hi + lo floats
   float scale_log2;
 };
 
@@ -100,7 +100,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->scale_log2 = pl->scale_log2;
   a->n_cta = p.num_ctas;
   a->min_pages = p.min_pages_per_cta > 0 ? p.min_pages_per_cta : da::kMinPagesPerCta;
-  for (int i = 0; i < 64; ++i) a->inv_freq[i] = pl->inv_freq[i];
+  for (int i = 0; i < 64; ++i) a->turn_freq[i] = pl->turn_freq[i];
 }
 
 }  // namespace
@@ -142,7 +142,8 @@ int draft_attn_check_params(const da_params* p) {
   if (p->num_pages < 1 || p->max_pages_per_seq < 1) return DA_ERR_INVALID_ARG;
   if ((int64_t)p->num_pages * p->num_kv_heads * da::kPage >= (int64_t)1 << 31)
     return DA_ERR_INVALID_ARG;
-  if ((int64_t)p->max_pages_per_seq * da::kPage >= (int64_t)1 << 31) return DA_ERR_INVALID_ARG;
+  // positions must stay below 2^24 (exact in FP32 for the RoPE angle)
+  if ((int64_t)p->max_pages_per_seq * da::kPage > (int64_t)1 << 24) return DA_ERR_INVALID_ARG;
   if (p->dtype != DA_DTYPE_BF16 && p->dtype != DA_DTYPE_FP32) return DA_ERR_INVALID_ARG;
   if (p->mode < DA_MODE_FULL || p->mode > DA_MODE_SHARP) return DA_ERR_INVALID_ARG;
   if (!(p->rope_theta >= 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
@@ -206,10 +207,15 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   pl->cnt_bytes = ((size_t)params->batch * params->num_kv_heads * 4 + 255) / 256 * 256;
   const size_t slots = (size_t)pl->p.num_ctas + (size_t)2 * params->batch * params->num_kv_heads;
   pl->ws_bytes = pl->cnt_bytes + slots * (size_t)da::slot_floats(pl->choice.rk, d) * sizeof(float);
-  for (int i = 0; i < 64; ++i)
-    pl->inv_freq[i] = (i < d / 2 && params->rope_theta > 0.0)
-                          ? std::pow(params->rope_theta, -2.0 * i / d)
-                          : 0.0;  // theta = 0: NoPE, every angle is zero
+  for (int i = 0; i < 64; ++i) {
+    // turns per position, theta^(-2i/d) / 2pi, as hi + lo floats (rope_cos_sin);
+    // theta = 0: NoPE, every angle is zero
+    const double f = (i < d / 2 && params->rope_theta > 0.0)
+                         ? std::pow(params->rope_theta, -2.0 * i / d) / (2.0 * M_PI)
+                         : 0.0;
+    const float hi = (float)f;
+    pl->turn_freq[i] = make_float2(hi, (float)(f - (double)hi));
+  }
   const double c = params->softmax_scale > 0.f ? (double)params->softmax_scale
                                                : 1.0 / std::sqrt((double)d);
   pl->scale_log2 = (float)(c * 1.4426950408889634074);  // log2(e)
@@ -265,7 +271,7 @@ int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, con
   a.H_kv = pl->p.num_kv_heads;
   a.max_pages = pl->p.max_pages_per_seq;
   a.num_pages = pl->p.num_pages;
-  for (int i = 0; i < 64; ++i) a.inv_freq[i] = pl->inv_freq[i];
+  for (int i = 0; i < 64; ++i) a.turn_freq[i] = pl->turn_freq[i];
   cudaError_t e = da::launch_append(pl->p.dtype, pl->p.head_dim, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
@@ -282,17 +288,18 @@ int draft_attn_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int3
 
 namespace {
 
-struct AppendIn {
-  const void* k_new = nullptr;
-  const void* v_new = nullptr;
-  const int32_t* pos = nullptr;
-  int32_t n_new = 0;
+// Validation and argument set-up of an attention call, shared by the run and
+// step entry points: everything that can fail on the host fails here, before
+// any launch.
+struct RunPrep {
+  da::DecodeArgs a;
+  CUtensorMap mk, mv, ms;
 };
 
-int run_impl(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
-             const int32_t* block_table, const void* k_cache, const void* v_cache,
-             const void* k_side, const uint64_t* tree_mask, void* out, void* workspace,
-             size_t workspace_bytes, void* stream, const AppendIn& app) {
+int prepare_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
+                const int32_t* block_table, const void* k_cache, const void* v_cache,
+                const void* k_side, const uint64_t* tree_mask, void* out, void* workspace,
+                size_t workspace_bytes, RunPrep* r) {
   if (!pl || !q || !q_pos || !ctx_lens || !block_table || !k_cache || !v_cache || !out ||
       !workspace)
     return DA_ERR_INVALID_ARG;
@@ -302,17 +309,14 @@ int run_impl(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* c
       (k_side && !aligned(k_side, 16)))
     return DA_ERR_INVALID_ARG;
   if (workspace_bytes < pl->ws_bytes) return DA_ERR_WORKSPACE_TOO_SMALL;
-  DeviceGuard g(pl->device);
-  if (!g.ok) return DA_ERR_CUDA;
-  CUtensorMap mk, mv, ms;
-  if (!encode_cache_map(&mk, k_cache, pl->p) || !encode_cache_map(&mv, v_cache, pl->p))
+  if (!encode_cache_map(&r->mk, k_cache, pl->p) || !encode_cache_map(&r->mv, v_cache, pl->p))
     return DA_ERR_CUDA;
   if (fold) {
-    if (!encode_cache_map(&ms, k_side, pl->p)) return DA_ERR_CUDA;
+    if (!encode_cache_map(&r->ms, k_side, pl->p)) return DA_ERR_CUDA;
   } else {
-    ms = mk;
+    r->ms = r->mk;
   }
-  da::DecodeArgs a;
+  da::DecodeArgs& a = r->a;
   fill_args(pl, &a);
   a.q = q;
   a.q_pos = q_pos;
@@ -322,19 +326,14 @@ int run_impl(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t* c
   a.out = out;
   a.cnt = static_cast<uint32_t*>(workspace);
   a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl->cnt_bytes);
-  if (app.n_new > 0) {
-    a.k_new = app.k_new;
-    a.v_new = app.v_new;
-    a.new_pos = app.pos;
-    a.n_new = app.n_new;
-    a.kc_w = const_cast<void*>(k_cache);
-    a.vc_w = const_cast<void*>(v_cache);
-    a.ks_w = const_cast<void*>(k_side);
-  }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, a, mk, mv, ms, st) != cudaSuccess)
-    return DA_ERR_CUDA;
   return DA_OK;
+}
+
+int launch_run(da_plan_t pl, const RunPrep& r, void* stream) {
+  return da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, r.a, r.mk, r.mv, r.ms,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_CUDA;
 }
 
 }  // namespace
@@ -346,8 +345,13 @@ int draft_attn_run_tree(da_plan_t pl, const void* q, const int32_t* q_pos,
                         const void* k_cache, const void* v_cache, const void* k_side,
                         const uint64_t* tree_mask, void* out, void* workspace,
                         size_t workspace_bytes, void* stream) {
-  return run_impl(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask, out,
-                  workspace, workspace_bytes, stream, AppendIn{});
+  if (!pl) return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  RunPrep r;
+  const int rc = prepare_run(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side,
+                             tree_mask, out, workspace, workspace_bytes, &r);
+  return rc != DA_OK ? rc : launch_run(pl, r, stream);
 }
 
 int draft_attn_step(da_plan_t pl, const void* k_new, const void* v_new, const int32_t* pos,
@@ -357,16 +361,19 @@ int draft_attn_step(da_plan_t pl, const void* k_new, const void* v_new, const in
                     size_t workspace_bytes, void* stream) {
   if (n_new < 0) return DA_ERR_INVALID_ARG;
   if (n_new > 32) return DA_ERR_UNSUPPORTED;
-  AppendIn app;
-  if (n_new > 0) {
-    if (!pl || !k_new || !v_new || !pos) return DA_ERR_INVALID_ARG;
-    app.k_new = k_new;
-    app.v_new = v_new;
-    app.pos = pos;
-    app.n_new = n_new;
-  }
-  return run_impl(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask, out,
-                  workspace, workspace_bytes, stream, app);
+  if (!pl || (n_new > 0 && (!k_new || !v_new || !pos))) return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  RunPrep r;
+  int rc = prepare_run(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask,
+                       out, workspace, workspace_bytes, &r);
+  if (rc != DA_OK) return rc;
+  // The append runs first; the attention kernel is launched behind it with
+  // programmatic dependent launch, so its set-up overlaps the append and its
+  // first global read waits for the append to finish.
+  rc = draft_attn_append_kv(pl, k_new, v_new, pos, pl->p.batch, n_new, block_table, k_cache,
+                            v_cache, k_side, stream);
+  return rc != DA_OK ? rc : launch_run(pl, r, stream);
 }
 
 int draft_attn_debug_gather(da_plan_t pl, const int32_t* q_pos, const int32_t* ctx_lens,

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     const int f = lane + 32 * u;
     const float x = to_f32<T>(kx[u]), y = to_f32<T>(ky[u]);
     float c, s;
-    rope_cos_sin(pos, a.inv_freq[f], c, s);
+    rope_cos_sin(pos, a.turn_freq[f], c, s);
     kc[f] = from_f32<T>(x * c - y * s);
     kc[f + D / 2] = from_f32<T>(y * c + x * s);
     if (ks) {

@@ -54,16 +54,7 @@ struct DecodeArgs {
   float scale_log2;     // softmax scale * log2(e)
   int32_t n_cta;
   int32_t min_pages;    // split floor (pages per active CTA)
-  // Fused append (draft_attn_step): n_new tokens per sequence, written into the
-  // caches by the CTA that reads their page (or round-robin when none does).
-  const void* k_new;    // [B][n_new][H_kv][D]
-  const void* v_new;
-  const int32_t* new_pos;  // [B][n_new], < 0 skips the token
-  void* kc_w;           // K cache, V cache, FOLD side cache (may be null) to write
-  void* vc_w;
-  void* ks_w;
-  int32_t n_new;        // 0: no append
-  double inv_freq[64];  // theta^(-2i/d), i < d/2
+  float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 
 // Partial slot of one piece: m[RK], l[RK], padding to a 16-byte boundary,
@@ -133,21 +124,23 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int mode, int32_t L, in
 }
 
 // ---------------------------------------------------------------------------
-// RoPE angle.  angle = pos * inv_freq is formed in double precision (positions
-// reach ~1M, where a float product would be off by ~0.06 rad), reduced modulo
-// 2*pi with Cody and Waite's two-constant additive reduction (2*pi split into
-// a double and its double-rounded remainder), and only then narrowed to float
-// for the library sincosf, which is accurate on [-pi, pi].
+// RoPE angle, in FP32 only.  Each frequency is kept as f = theta^(-2i/d) / 2pi
+// (turns per position) split into two floats hi + lo (formed on the host in
+// double: hi = f rounded, lo = f - hi rounded), so that pos * f is the angle in
+// turns.  pos * hi is formed without error as the float pair th + te by an FMA
+// (Dekker's TwoProduct: te = fma(pos, hi, -th)); the whole turns of th are
+// dropped exactly, te and pos * lo are added, and CUDA's sincospif (which
+// works in units of pi) takes twice the remaining fraction of a turn.  With
+// |pos| < 2^24 (exact in float) the angle is within a few 1e-7 rad at every
+// position, where a plain float product pos * inv_freq would be off by
+// ~0.06 rad near 1M.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void rope_cos_sin(int32_t pos, double inv_freq, float& c, float& s) {
-  const double kInvTwoPi = 0.15915494309189533577;    // 1 / (2 pi)
-  const double kTwoPiHi = 6.28318530717958623200;     // 2 pi rounded to double
-  const double kTwoPiLo = 2.44929359829470635445e-16; // 2 pi - kTwoPiHi
-  double a = (double)pos * inv_freq;
-  double k = rint(a * kInvTwoPi);
-  double r = fma(-k, kTwoPiHi, a);
-  r = fma(-k, kTwoPiLo, r);
-  sincosf((float)r, &s, &c);
+__device__ __forceinline__ void rope_cos_sin(int32_t pos, float2 f, float& c, float& s) {
+  const float p = (float)pos;
+  const float th = __fmul_rn(p, f.x);
+  const float te = __fmaf_rn(p, f.x, -th);
+  const float t = __fadd_rn(th, -rintf(th)) + (te + p * f.y);
+  sincospif(2.f * t, &s, &c);
 }
 
 // ---------------------------------------------------------------------------

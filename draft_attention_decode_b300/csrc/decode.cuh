@@ -213,7 +213,6 @@ struct CoreEngine {
   float2 o2[RK][DQ / 2];
   float m_run, l_run;    // row ds & (RK-1): reference maximum, partial sum
   uint32_t off[2][NCH];  // swizzled byte offsets of the lane's chunks, pass 0/1
-  uint64_t tm;           // draft-tree mask of row ds & (RK-1)
   int lane, warp, kg, ds;
 
   __device__ __forceinline__ int chunk_of(int i) const {
@@ -255,16 +254,15 @@ struct CoreEngine {
           const int d0 = dim_of(i, 2 * e);
           q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0], s.q[r * D + d0 + 1]);
         }
-    tm = s.tmask[ds & (RK - 1)];
     reset();
   }
 
   // NP consecutive pages of one piece: K/V stage addresses, valid key ranges
   // [lo, hi) inside each page and tree offsets.
   template <int NP>
-  __device__ __forceinline__ void pages(const uint32_t (&kb)[NP], const uint32_t (&vb)[NP],
-                                        const int (&lo)[NP], const int (&hi)[NP],
-                                        const int (&toff)[NP]) {
+  __device__ __forceinline__ void pages(const Smem& s, const uint32_t (&kb)[NP],
+                                        const uint32_t (&vb)[NP], const int (&lo)[NP],
+                                        const int (&hi)[NP], const int (&toff)[NP]) {
     constexpr int NIT = 2 * NP;
     float sc[NIT];
     bool ok[NIT];
@@ -291,7 +289,19 @@ struct CoreEngine {
 #pragma unroll
       for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
       const float sr = reduce_scatter<RK, LPK>(v, ds);
-      sc[it] = (ok[it] && tree_visible(key, toff[pg], tm)) ? sr : -INFINITY;
+      sc[it] = ok[it] ? sr : -INFINITY;
+    }
+    // Draft-tree keys the row does not see (only pages that hold tree keys).
+    bool has_tree = false;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) has_tree |= toff[pg] != kNoTree;
+    if (has_tree) {
+      const uint64_t tm = s.tmask[ds & (RK - 1)];
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int key = warp * KPW + kg + KG * (it & 1);
+        if (!tree_visible(key, toff[it >> 1], tm)) sc[it] = -INFINITY;
+      }
     }
     // Row maximum over the warp's keys (lanes with the same ds).
     float mx = sc[0];
@@ -346,11 +356,11 @@ struct CoreEngine {
     }
   }
 
-  __device__ __forceinline__ void page(const Smem&, uint32_t kbase, uint32_t vbase, int lo, int hi,
+  __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi,
                                        int toff) {
     const uint32_t kb[1] = {kbase}, vb[1] = {vbase};
     const int l[1] = {lo}, h[1] = {hi}, o[1] = {toff};
-    pages<1>(kb, vb, l, h, o);
+    pages<1>(s, kb, vb, l, h, o);
   }
 
   // Sum the key groups, merge the consumer warps, write the piece's partial.
@@ -430,7 +440,6 @@ struct CoreEngineWide {
   float2 q2[RK][DQ / 2];
   float2 o2[RK][DPL / 2];
   float m_run, l_run;
-  uint64_t tm;           // draft-tree mask of row ds & (RK-1)
   int lane, warp, kg, ds;
 
   __device__ __forceinline__ void init() {
@@ -464,7 +473,6 @@ struct CoreEngineWide {
         for (int e = 0; e < EPC / 2; ++e)
           q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0 + 2 * e], s.q[r * D + d0 + 2 * e + 1]);
     }
-    tm = s.tmask[ds & (RK - 1)];
     reset();
   }
 
@@ -515,7 +523,13 @@ struct CoreEngineWide {
 #pragma unroll
       for (int r = 0; r < RK; ++r) v[r] = acc[r].x + acc[r].y;
       const float sr = reduce_scatter8<RK>(v, ds);
-      sc[it] = (key >= lo && key < hi && tree_visible(key, toff, tm)) ? sr : -INFINITY;
+      sc[it] = (key >= lo && key < hi) ? sr : -INFINITY;
+    }
+    if (toff != kNoTree) {   // draft-tree keys the row does not see
+      const uint64_t tm = s.tmask[ds & (RK - 1)];
+#pragma unroll
+      for (int it = 0; it < 2; ++it)
+        if (!tree_visible(wk0 + kg + 4 * it, toff, tm)) sc[it] = -INFINITY;
     }
     // Online softmax for row ds & (RK-1) over the warp's 8 keys.
     float mx = fmaxf(sc[0], sc[1]);
@@ -644,7 +658,6 @@ struct MmaEngine {
   uint32_t qf[KS][NT][2];
   float O[KS][NT][4];
   float m[NT][2], l[NT][2];
-  uint64_t tmr[NT][2];  // draft-tree masks of the lane's rows (8 nt + 2 t + cc)
   int lane, warp, kb, grp, g, t;
 
   __device__ __forceinline__ void init() {
@@ -683,10 +696,6 @@ struct MmaEngine {
         qf[ks][nt][0] = pack_bf16(qr[0], qr[1]);
         qf[ks][nt][1] = pack_bf16(qr[8], qr[9]);
       }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tmr[nt][cc] = s.tmask[row0 + 8 * nt + 2 * t + cc];
     reset();
   }
 
@@ -707,6 +716,17 @@ struct MmaEngine {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_bf16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
     }
+    if (toff != kNoTree) {   // draft-tree keys a row does not see
+      const int row0 = SPLIT_PAGES ? 0 : grp * RW;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint64_t m = s.tmask[row0 + 8 * nt + 2 * t + cc];
+          if (!tree_visible(key0 + g, toff, m)) S[nt][cc] = -INFINITY;
+          if (!tree_visible(key0 + g + 8, toff, m)) S[nt][cc + 2] = -INFINITY;
+        }
+    }
     const bool oka = (key0 + g >= lo) && (key0 + g < hi);
     const bool okb = (key0 + g + 8 >= lo) && (key0 + g + 8 < hi);
     float alpha[NT][2];
@@ -717,9 +737,8 @@ struct MmaEngine {
       float P[4];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const float v0 = (oka && tree_visible(key0 + g, toff, tmr[nt][cc])) ? S[nt][cc] : -INFINITY;
-        const float v1 =
-            (okb && tree_visible(key0 + g + 8, toff, tmr[nt][cc])) ? S[nt][cc + 2] : -INFINITY;
+        const float v0 = oka ? S[nt][cc] : -INFINITY;
+        const float v1 = okb ? S[nt][cc + 2] : -INFINITY;
         float mx = fmaxf(v0, v1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -1083,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo[2] = {lo0, (inf1.flags & kValid) ? (inf1.lohi & 0xffff) : 0};
         const int hi[2] = {hi0, (inf1.flags & kValid) ? (inf1.lohi >> 16) : 0};
         const int to[2] = {to0, inf1.toff};
-        eng.template pages<2>(kb, vb, lo, hi, to);
+        eng.template pages<2>(s, kb, vb, lo, hi, to);
         __syncwarp();
         if ((threadIdx.x & 31) == 0) {
           mbar_arrive(&s.empty[st]);

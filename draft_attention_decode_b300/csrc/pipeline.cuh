@@ -28,6 +28,7 @@ struct PageInfo {
   int32_t toff;   // key k of the page is tree token k + toff (when in [0, 64))
 };
 
+
 // Shared-memory layout (host and device agree on it).
 struct Layout {
   uint32_t stage_bytes, stages;
@@ -54,13 +55,14 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.p_off = off;     off += variant == kVariantCore ? align_up(ncw * 9 * rk * 4, 128) : 0;
   L.info_off = off;  off += align_up((uint32_t)stages * sizeof(PageInfo), 128);
   L.bar_off = off;   off += align_up((uint32_t)stages * 16, 128);
-  L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);
+  L.invf_off = off;  off += align_up((uint32_t)(d / 2) * 8, 128);   // float2 per pair
   L.len_off = off;   off += align_up((uint32_t)batch * 4, 128);
   L.pfx_off = off;   off += align_up((uint32_t)(batch + 1) * 4, 128);
   L.n0_off = off;    off += align_up((uint32_t)batch * 4, 128);
   L.flag_off = off;  off += 128;
   L.tm_off = off;    off += align_up((uint32_t)rk * 8, 128);
   L.rm_off = off;    off += align_up((uint32_t)rk * 4, 128);
+
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
 }
@@ -74,7 +76,7 @@ struct Smem {
   PageInfo* info;
   uint64_t* full;
   uint64_t* empty;
-  double* invf;
+  float2* invf;         // turn frequencies (rope_cos_sin)
   int32_t* len;
   int32_t* pfx;         // [B + 1] pages per head of sequences before b
   int32_t* n0;          // [B] pages per head of range 0
@@ -95,7 +97,7 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.info = reinterpret_cast<PageInfo*>(p + L.info_off);
   s.full = reinterpret_cast<uint64_t*>(p + L.bar_off);
   s.empty = s.full + L.stages;
-  s.invf = reinterpret_cast<double*>(p + L.invf_off);
+  s.invf = reinterpret_cast<float2*>(p + L.invf_off);
   s.len = reinterpret_cast<int32_t*>(p + L.len_off);
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
   s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
@@ -111,7 +113,7 @@ template <int D, int ES, int NCW>
 __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
   grid_dep_launch_dependents();
-  for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.inv_freq[i];
+  for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.turn_freq[i];
   if (tid == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
       mbar_init(&s.full[i], 1);
@@ -184,85 +186,6 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
   return w;
 }
 
-// ---------------------------------------------------------------------------
-// Fused append: one new token of one KV head, written by a whole warp (lane f
-// takes the rotate-half pairs (f, f + D/2), f = lane, lane + 32): the rotated
-// key into the K cache, the raw key into the side cache (when given), the
-// value into the V cache -- the same arithmetic as the append kernel.  Then a
-// proxy fence, so that a TMA load this thread issues later sees the writes.
-// ---------------------------------------------------------------------------
-template <int ES, int D>
-__device__ inline void append_token(const DecodeArgs& a, const Smem& s, int b, int j, int h,
-                                    int32_t pos, int32_t phys) {
-  using T = std::conditional_t<ES == 2, __nv_bfloat16, float>;
-  const int lane = threadIdx.x & 31;
-  const int64_t src = (((int64_t)b * a.n_new + j) * a.H_kv + h) * D;
-  const int64_t dst = (((int64_t)phys * a.H_kv + h) * kPage + (pos % kPage)) * D;
-  const T* k = static_cast<const T*>(a.k_new) + src;
-  const T* v = static_cast<const T*>(a.v_new) + src;
-  T* kc = static_cast<T*>(a.kc_w) + dst;
-  T* vc = static_cast<T*>(a.vc_w) + dst;
-  T* ks = a.ks_w ? static_cast<T*>(a.ks_w) + dst : nullptr;
-#pragma unroll
-  for (int u = 0; u < D / 64; ++u) {
-    const int f = lane + 32 * u;
-    const T xr = k[f], yr = k[f + D / 2];
-    const float x = to_f32<T>(xr), y = to_f32<T>(yr);
-    float c, sn;
-    rope_cos_sin(pos, s.invf[f], c, sn);
-    kc[f] = from_f32<T>(x * c - y * sn);
-    kc[f + D / 2] = from_f32<T>(y * c + x * sn);
-    if (ks) {
-      ks[f] = xr;
-      ks[f + D / 2] = yr;
-    }
-    vc[f] = v[f];
-    vc[f + D / 2] = v[f + D / 2];
-  }
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Whether new token position p of sequence b is read by some CTA in this
-// call (it lies in one of the mode's key ranges): then the CTA that loads its
-// page writes it; otherwise the round-robin pass does.
-__device__ __forceinline__ bool read_this_call(const DecodeArgs& a, const Smem& s, int b,
-                                               int32_t p) {
-  const Ranges rg = mode_ranges(a.mode, s.len[b], a.W, a.n_sink);
-  return (p >= rg.k0[0] && p < rg.k1[0]) || (p >= rg.k0[1] && p < rg.k1[1]);
-}
-
-// Tokens no CTA reads in this call, spread over the grid; whole warp, one
-// (token, head) per lane to look up, then the warp writes the ones it owns.
-template <int ES, int D>
-__device__ inline void append_unread(const DecodeArgs& a, const Smem& s) {
-  const int lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)a.B * a.n_new * a.H_kv;
-  for (int64_t base = (int64_t)blockIdx.x * 32; base < total; base += (int64_t)gridDim.x * 32) {
-    const int64_t i = base + lane;
-    int32_t p = -1, phys = -1;
-    if (i < total) {
-      const int64_t bj = i / a.H_kv;
-      const int b = (int)(bj / a.n_new);
-      p = __ldg(a.new_pos + bj);
-      if (p >= 0 && !read_this_call(a, s, b, p)) {
-        if (p / kPage >= a.max_pages) atomicOr(a.status, DA_STATUS_BAD_POSITION);
-        else phys = phys_page(a.block_table, b, p / kPage, a.max_pages, a.num_pages, a.status);
-      }
-    }
-    uint32_t todo = __ballot_sync(0xffffffffu, phys >= 0);
-    while (todo) {
-      const int l = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int64_t il = base + l;
-      const int h = (int)(il % a.H_kv);
-      const int64_t bj = il / a.H_kv;
-      const int b = (int)(bj / a.n_new), j = (int)(bj - (int64_t)b * a.n_new);
-      append_token<ES, D>(a, s, b, j, h, __shfl_sync(0xffffffffu, p, l),
-                          __shfl_sync(0xffffffffu, phys, l));
-    }
-  }
-}
-
 // The producer warp: block-table translation and TMA issue for the CTA's
 // stretch [xs, xe) of the page line.  ES = element bytes, NCB = 128-byte
 // column boxes per row (head_dim * ES / 128).
@@ -270,7 +193,6 @@ template <int ES, int NCB>
 __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
                                 int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
                                 const CUtensorMap* ms) {
-  constexpr int D = NCB * kSwizzleRow / ES;
   const int lane = threadIdx.x & 31;
   const uint64_t pol = policy_evict_first();
   if (lane == 0) {
@@ -282,8 +204,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
   uint32_t n = 0;
   for (int64_t base = xs; base < xe; base += 32) {
     const int64_t x = base + lane;
-    int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree, pb = 0;
-    uint32_t app = 0;   // new tokens of this page that this CTA writes first
+    int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree;
     if (x < xe) {
       const Where w = locate(s, a.B, a.H_kv, x);
       const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
@@ -304,12 +225,6 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
         const int32_t t0 = s.len[w.b] - a.n_tree;   // position of tree token 0
         if (pk0 + kPage > t0) toff = pk0 - t0;
       }
-      pb = w.b;
-      if (a.n_new > 0 && phys >= 0)
-        for (int j = 0; j < a.n_new; ++j) {
-          const int32_t p = __ldg(a.new_pos + w.b * a.n_new + j);
-          if (p >= pk0 + lo && p < pk0 + hi) app |= 1u << j;
-        }
     }
     const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
     for (int j = 0; j < cnt; ++j) {
@@ -320,16 +235,6 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const int32_t jfar = __shfl_sync(0xffffffffu, far, j);
       const int32_t jh = __shfl_sync(0xffffffffu, h, j);
       const int32_t jtoff = __shfl_sync(0xffffffffu, toff, j);
-      uint32_t japp = __shfl_sync(0xffffffffu, app, j);
-      if (japp) {   // the page holds new tokens: write them before loading it
-        const int32_t jb = __shfl_sync(0xffffffffu, pb, j);
-        while (japp) {
-          const int t = __ffs(japp) - 1;
-          japp &= japp - 1;
-          append_token<ES, D>(a, s, jb, t, jh, __ldg(a.new_pos + jb * a.n_new + t), jphys);
-        }
-        __syncwarp();
-      }
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
@@ -355,7 +260,6 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       __syncwarp();
     }
   }
-  if (a.n_new > 0) append_unread<ES, D>(a, s);
 }
 
 }  // namespace da

@@ -102,7 +102,8 @@ typedef struct {
   int32_t head_dim;          /* 64 or 128                                          */
   int32_t page_size;         /* tokens per page; must be 64                        */
   int32_t num_pages;         /* physical pages in each cache array                 */
-  int32_t max_pages_per_seq; /* row length of the block table                      */
+  int32_t max_pages_per_seq; /* row length of the block table; at most 2^24 /
+                                page_size, so every position is below 2^24       */
   int32_t dtype;             /* da_dtype of q, caches and out                      */
   int32_t mode;              /* da_mode                                            */
   int32_t window;            /* W (window, fold), >= 1                             */
@@ -161,8 +162,9 @@ void draft_attn_plan_destroy(da_plan_t plan);
  * writes RoPE(k_new, pos) to k_cache, k_new unchanged to k_side (when
  * k_side != NULL) and v_new to v_cache, at page
  * block_table[b][pos / page_size], slot pos % page_size.  Angles are formed
- * in double precision, the rotation in FP32, the store rounds to nearest
- * even.  A negative position skips the token (padding for ragged batches).
+ * in FP32 from an exact product of the position and a two-float frequency
+ * (error a few 1e-7 rad below 2^24), the rotation in FP32, the store rounds
+ * to nearest even.  A negative position skips the token (padding for ragged batches).
  * batch may be below params.batch (pass a block_table offset by rows to
  * append to a subset).  k_side is required when params.mode is FOLD.
  * "FOLD ...", review (the unrotated side cache); Windowed-MTP, Abstract (the
@@ -203,14 +205,15 @@ int draft_attn_run_tree(da_plan_t plan, const void* q, const int32_t* q_pos,
                         const uint64_t* tree_mask, void* out, void* workspace,
                         size_t workspace_bytes, void* stream);
 
-/* One draft step in one launch: exactly draft_attn_append_kv(k_new, v_new,
+/* One draft step in one call: exactly draft_attn_append_kv(k_new, v_new,
  * pos, batch = params.batch, n_new) followed by draft_attn_run_tree, as the
- * draft head hands over its query and its new key/value together.  Each new
- * token is written (rotated K, side K when k_side is given, V) by the CTA that
- * reads its page in this call, before that CTA loads the page; tokens no CTA
- * reads are written by the others.  n_new in 0..32 (0: no append);
- * ctx_lens already count the new tokens, as for draft_attn_run.  k_side is
- * required in FOLD mode.  DA_ERR_UNSUPPORTED for n_new > 32. */
+ * draft head hands over its query and its new key/value together.  Every
+ * argument of the attention is checked before anything is launched, so an
+ * error leaves the caches untouched.  The attention kernel is launched behind
+ * the append with programmatic dependent launch: its set-up overlaps the
+ * append and its first global read waits for it.  n_new in 0..32 (0: no
+ * append); ctx_lens already count the new tokens, as for draft_attn_run.
+ * k_side is required in FOLD mode.  DA_ERR_UNSUPPORTED for n_new > 32. */
 int draft_attn_step(da_plan_t plan, const void* k_new, const void* v_new, const int32_t* pos,
                     int32_t n_new, const void* q, const int32_t* q_pos, const int32_t* ctx_lens,
                     const int32_t* block_table, void* k_cache, void* v_cache, void* k_side,

@@ -1,4 +1,4 @@
-"""draft_attn_step (append + attend in one launch) on the GPU: the output and
+"""draft_attn_step (append + attend in one call) on the GPU: the output and
 every cache it writes are bit-identical to draft_attn_append_kv followed by
 draft_attn_run(_tree), for every mode and engine, for tokens that the call
 reads and tokens it does not, and a draft loop matches the oracle."""
@@ -53,7 +53,7 @@ def test_step_equals_append_then_run(mode, kw, shape, n_new, visible, dtype):
     # reference: separate append and run
     s.da.append_kv(k_new, v_new, pos, s.block_table, s.k_cache, s.v_cache, s.k_side)
     want = s.run(ctx_lens=lens).clone()
-    # one launch
+    # one call
     got = s.da.step(k_new, v_new, pos, s.q, s.q_pos, lens, s.block_table, kc, vc, ks)
     torch.cuda.synchronize()
     assert torch.equal(got, want)
@@ -90,7 +90,7 @@ def test_step_with_tree_mask(mode, kw):
 
 @pytest.mark.parametrize("mode", ["full", "window"])
 def test_step_draft_loop_matches_oracle(mode):
-    """Four draft steps at 20K context, each one launch, against the oracle."""
+    """Four draft steps at 20K context, each one call, against the oracle."""
     wl = WL.resized(WL.WORKLOADS["mtp_draft_128k"], 20000)
     s = Setup(batch=1, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
               ctx=list(wl.ctx), mode=mode, window=2048, extra_tokens=4, seed=1)
@@ -118,4 +118,23 @@ def test_step_rejects_too_many_tokens():
     with pytest.raises(B.DraftAttnError) as e:
         s.da.step(k, k, pos, s.q, s.q_pos, s.ctx_lens, s.block_table, s.k_cache, s.v_cache)
     assert e.value.code == B.DA_ERR_UNSUPPORTED
+    s.close()
+
+
+def test_step_error_leaves_cache_untouched():
+    """A step whose attention arguments are invalid fails before the append
+    is launched."""
+    s = Setup(batch=1, n_q=1, num_q_heads=8, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=[100], extra_tokens=1)
+    kc = s.k_cache.clone()
+    k = s.k_raw[0][None, 100:101].contiguous()
+    pos = torch.tensor([[100]], dtype=torch.int32, device=s.dev)
+    lens = torch.tensor([101], dtype=torch.int32, device=s.dev)
+    out = torch.empty_like(s.q)
+    with pytest.raises(B.DraftAttnError) as e:
+        B.draft_attn_step(s.da.plan, k, k, pos, s.q, s.q_pos, lens, s.block_table, s.k_cache,
+                          s.v_cache, None, out, s.da.workspace[:16], None, None)
+    assert e.value.code == B.DA_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert _same(kc, s.k_cache)          # unwritten slots hold NaN
     s.close()
