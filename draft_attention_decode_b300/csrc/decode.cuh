@@ -140,21 +140,40 @@ __device__ __forceinline__ float reduce_scatter8(float (&v)[RK], int ds) {
 
 template <typename T>
 struct Chunk;  // one 16-byte shared-memory chunk as floats
+// raw(): the 16 bytes as loaded; cvt(): those bytes as floats.
 template <>
 struct Chunk<__nv_bfloat16> {
-  __device__ __forceinline__ static void load(uint32_t addr, float (&f)[8]) {
-    uint32_t w0, w1, w2, w3;
+  __device__ __forceinline__ static void raw(uint32_t addr, uint32_t (&w)[4]) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
-    f[0] = bf16lo(w0); f[1] = bf16hi(w0); f[2] = bf16lo(w1); f[3] = bf16hi(w1);
-    f[4] = bf16lo(w2); f[5] = bf16hi(w2); f[6] = bf16lo(w3); f[7] = bf16hi(w3);
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+  }
+  __device__ __forceinline__ static void cvt(const uint32_t (&w)[4], float (&f)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16lo(w[i]);
+      f[2 * i + 1] = bf16hi(w[i]);
+    }
+  }
+  __device__ __forceinline__ static void load(uint32_t addr, float (&f)[8]) {
+    uint32_t w[4];
+    raw(addr, w);
+    cvt(w, f);
   }
 };
 template <>
 struct Chunk<float> {
+  __device__ __forceinline__ static void raw(uint32_t addr, uint32_t (&w)[4]) {
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+  }
+  __device__ __forceinline__ static void cvt(const uint32_t (&w)[4], float (&f)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(w[i]);
+  }
   __device__ __forceinline__ static void load(uint32_t addr, float (&f)[4]) {
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(addr));
+    uint32_t w[4];
+    raw(addr, w);
+    cvt(w, f);
   }
 };
 
@@ -291,6 +310,16 @@ struct CoreEngine {
       const float sr = reduce_scatter<RK, LPK>(v, ds);
       sc[it] = ok[it] ? sr : -INFINITY;
     }
+    // The V chunks of every key, loaded now so that their latency overlaps the
+    // softmax.  A key outside [lo, hi) may hold anything, NaN included: it reads
+    // the zeroed chunk instead (its probability is 0).
+    uint32_t vw[NIT][NCH][4];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int pg = it >> 1, ps = it & 1;
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) Chunk<T>::raw(ok[it] ? vb[pg] + off[ps][i] : s.zero16, vw[it][i]);
+    }
     // Draft-tree keys the row does not see (only pages that hold tree keys).
     bool has_tree = false;
 #pragma unroll
@@ -334,23 +363,20 @@ struct CoreEngine {
     // PV in the QK^T layout.
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
-      const int pg = it >> 1, ps = it & 1;
       float pr[RK];
 #pragma unroll
       for (int r = 0; r < RK; ++r)
         pr[r] = __shfl_sync(0xffffffffu, p[it], (lane & ~(LPK - 1)) | r);
-      if (ok[it]) {   // keys outside [lo, hi) may hold anything, NaN included
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) {
-          float f[EPC];
-          Chunk<T>::load(vb[pg] + off[ps][i], f);
+      for (int i = 0; i < NCH; ++i) {
+        float f[EPC];
+        Chunk<T>::cvt(vw[it][i], f);
 #pragma unroll
-          for (int e = 0; e < EPC / 2; ++e) {
-            const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
+        for (int e = 0; e < EPC / 2; ++e) {
+          const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
 #pragma unroll
-            for (int r = 0; r < RK; ++r)
-              o2[r][i * (EPC / 2) + e] = ffma2(make_float2(pr[r], pr[r]), vv, o2[r][i * (EPC / 2) + e]);
-          }
+          for (int r = 0; r < RK; ++r)
+            o2[r][i * (EPC / 2) + e] = ffma2(make_float2(pr[r], pr[r]), vv, o2[r][i * (EPC / 2) + e]);
         }
       }
     }

@@ -80,7 +80,8 @@ struct Smem {
   int32_t* len;
   int32_t* pfx;         // [B + 1] pages per head of sequences before b
   int32_t* n0;          // [B] pages per head of range 0
-  int32_t* flag;        // broadcast of the merge ticket
+  int32_t* flag;        // broadcast of the merge ticket (word 0)
+  uint32_t zero16;      // shared address of 16 zero bytes (words 16..19 of the flag block)
   uint64_t* tmask;      // [rk] visible tree keys of each row of the current piece
   float* rmult;         // [rk] logit multiplier of each row of the current piece
 };
@@ -102,6 +103,7 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
   s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
   s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
+  s.zero16 = smem_u32(p + L.flag_off + 64);
   s.tmask = reinterpret_cast<uint64_t*>(p + L.tm_off);
   s.rmult = reinterpret_cast<float*>(p + L.rm_off);
   return s;
@@ -114,6 +116,7 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
   grid_dep_launch_dependents();
   for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.turn_freq[i];
+  if (tid < 4) s.flag[16 + tid] = 0;
   if (tid == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
       mbar_init(&s.full[i], 1);
