@@ -368,9 +368,11 @@ int draft_attn_step(da_plan_t pl, const void* k_new, const void* v_new, const in
   int rc = prepare_run(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask,
                        out, workspace, workspace_bytes, &r);
   if (rc != DA_OK) return rc;
+  r.a.inputs_ready = n_new > 0 && pl->p.batch > 0;
   // The append runs first; the attention kernel is launched behind it with
-  // programmatic dependent launch, so its set-up overlaps the append and its
-  // first global read waits for the append to finish.
+  // programmatic dependent launch.  Its set-up, the block-table reads and the
+  // query preparation overlap the append; only its first cache load waits
+  // for the append to finish.
   rc = draft_attn_append_kv(pl, k_new, v_new, pos, pl->p.batch, n_new, block_table, k_cache,
                             v_cache, k_side, stream);
   return rc != DA_OK ? rc : launch_run(pl, r, stream);

@@ -11,8 +11,11 @@ namespace da {
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
-  grid_dep_launch_dependents();
+  // Wait for the predecessor first, then let the dependent start: a
+  // dependent attention kernel (draft_attn_step) reads its inputs before its
+  // own griddepcontrol.wait, relying on this order.
   grid_dep_wait();
+  grid_dep_launch_dependents();
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t total = (int64_t)a.B * a.n_new * a.H_kv;

@@ -54,6 +54,11 @@ struct DecodeArgs {
   float scale_log2;     // softmax scale * log2(e)
   int32_t n_cta;
   int32_t min_pages;    // split floor (pages per active CTA)
+  // Nonzero when the previous kernel in the stream is this library's append
+  // kernel (draft_attn_step): it waits for its own predecessor before it lets
+  // this kernel start, so every input but the caches it writes may be read
+  // before griddepcontrol.wait; only the producer's first cache load waits.
+  int32_t inputs_ready;
   float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 
@@ -185,7 +190,7 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 // the seq, or both.
 // ---------------------------------------------------------------------------
 constexpr int kMaxAutoStages = 4;   // pipeline depth chosen when da_params.stages = 0
-constexpr int kMinPagesPerCta = 4;   // default split floor (da_params.min_pages_per_cta = 0)
+constexpr int kMinPagesPerCta = 2;   // default split floor (da_params.min_pages_per_cta = 0)
 
 __host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int64_t n) {
   return (i * TP) / n;
@@ -304,6 +309,11 @@ __device__ __forceinline__ void grid_dep_wait() {
 }
 __device__ __forceinline__ void grid_dep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+// Orders global writes made visible to this thread (by the previous grid)
+// before the TMA loads it issues next.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {

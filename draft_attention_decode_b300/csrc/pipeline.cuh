@@ -124,7 +124,9 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
     }
     fence_barrier_init();
   }
-  grid_dep_wait();   // global memory from here on
+  // global memory from here on (the caches only after the producer's wait
+  // when the inputs are known to be ready)
+  if (!a.inputs_ready) grid_dep_wait();
   for (int b = tid; b < a.B; b += blockDim.x)
     s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
   // Small query tensors are pulled into L2 now, while the lengths load: the
@@ -241,6 +243,10 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
+        if (n == 0 && a.inputs_ready) {   // the append kernel's writes land first
+          grid_dep_wait();
+          fence_proxy_async_global();
+        }
         if (mbar_wait(&s.empty[st], par ^ 1u, a.status)) {
           s.info[st] = PageInfo{jseq, jlohi, jflags, jtoff};
           uint8_t* kdst = s.stage + st * L.stage_bytes;

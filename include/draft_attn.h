@@ -118,7 +118,8 @@ typedef struct {
                                 cores (bf16 only); see DA_ENGINE_*                */
   int32_t min_pages_per_cta; /* split floor: a call whose selection has P pages
                                 (over all sequences and KV heads) runs on
-                                min(num_ctas, ceil(P / this)) CTAs; 0 = default   */
+                                min(num_ctas, ceil(P / this)) CTAs; 0 = default
+                                (2)                                               */
   int32_t stages;            /* shared-memory pipeline depth in pages, 2..8;
                                 0 = as deep as shared memory allows (<= 4)       */
   int32_t tree_size;         /* draft-tree tokens at the end of each context,
