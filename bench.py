@@ -572,6 +572,8 @@ def run_ours(args, dist):
     sweep = None if args.no_sweep else context_sweep(dev, args, flush, dist, peak)
     others = None if args.no_workloads else all_workloads(
         dev, args, flush, dist, peak, ("fold_4x256k", "ragged_tree_16x8"))
+    if others is not None:
+        others.append(fold_ring_row(dev, args, flush, dist, peak))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -686,6 +688,48 @@ def all_workloads(dev, args, flush, dist, peak, names):
         del dl
         torch.cuda.empty_cache()
     return table
+
+
+def fold_ring_row(dev, args, flush, dist, peak):
+    """FOLD 4 x 256K with the rotated keys kept in a ring of ceil(W/64) + 1
+    pages per sequence (da_params.k_ring_pages): the attention call timed as in
+    all_workloads, with the rotated K cache's bytes beside the paged one's."""
+    wl = WL.WORKLOADS["fold_4x256k"]
+    dl = DraftLoop(wl, dev, ("fold",))
+    R = (wl.window + WL.PAGE - 1) // WL.PAGE + 1
+    ring = dl.B.DraftAttention(
+        device=dev.index or 0, batch=wl.batch, n_q=wl.n_q, num_q_heads=wl.num_q_heads,
+        num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_pages=dl.npg,
+        max_pages_per_seq=dl.bt.shape[1], dtype=wl.dtype, mode="fold", window=wl.window,
+        alpha=wl.alpha, far_mix=wl.far_mix, rope_theta=wl.rope_theta, k_ring_pages=R)
+    kr = torch.empty((wl.batch * R,) + tuple(dl.k_cache.shape[1:]), dtype=dl.k_cache.dtype,
+                     device=dev)
+    for b in range(wl.batch):           # set-up: the window's rotated pages into the ring
+        L = int(dl.lens[0][b])
+        for P in range(max(L - wl.window, 0) // WL.PAGE, (L - 1) // WL.PAGE + 1):
+            kr[b * R + P % R] = dl.k_cache[int(dl.bt[b, P])]
+    torch.cuda.synchronize()
+
+    def call():
+        ring.run(dl.q[0], dl.qpos[0], dl.lens[0], dl.bt, kr, dl.v_cache, dl.k_side, out=dl.out)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+    nb = dl.kv_bytes("fold")
+    row = {"workload": "fold_4x256k", "mode": "fold, rotated K in a ring", "us": round(ms * 1e3, 2),
+           "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+           "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+           "k_cache_bytes": kr.numel() * kr.element_size(),
+           "k_cache_bytes_paged": dl.k_cache.numel() * dl.k_cache.element_size()}
+    assert ring.status() == (dl.B.DA_OK, 0)
+    ring.close()
+    dl.close()
+    del dl
+    torch.cuda.empty_cache()
+    return row
 
 
 def profile_loop(args):

@@ -68,7 +68,8 @@ class da_params(ctypes.Structure):
         ("min_pages_per_cta", ctypes.c_int32),
         ("stages", ctypes.c_int32),
         ("tree_size", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("k_ring_pages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 
@@ -142,7 +143,8 @@ def header_functions(path: str = HEADER) -> list:
 def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
-                page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0) -> da_params:
+                page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0,
+                k_ring_pages=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -157,6 +159,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.min_pages_per_cta = int(min_pages_per_cta)
     p.stages = int(stages)
     p.tree_size = int(tree_size)
+    p.k_ring_pages = int(k_ring_pages)
     return p
 
 

@@ -58,12 +58,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D view of a cache array: rows = num_pages * H_kv * 64 tokens, columns =
 // head_dim elements; box = 64 rows x 128 bytes with the 128-byte swizzle.
-bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p) {
+// pages: the cache array's page count (num_pages, or batch * k_ring_pages for
+// FOLD's ring of rotated keys).
+bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p, int64_t pages) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int es = p.dtype == DA_DTYPE_BF16 ? 2 : 4;
-  cuuint64_t gdim[2] = {(cuuint64_t)p.head_dim,
-                        (cuuint64_t)p.num_pages * p.num_kv_heads * da::kPage};
+  cuuint64_t gdim[2] = {(cuuint64_t)p.head_dim, (cuuint64_t)pages * p.num_kv_heads * da::kPage};
   cuuint64_t gstride[1] = {(cuuint64_t)p.head_dim * es};
   cuuint32_t box[2] = {(cuuint32_t)(da::kSwizzleRow / es), (cuuint32_t)da::kPage};
   cuuint32_t estr[2] = {1, 1};
@@ -100,6 +101,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->scale_log2 = pl->scale_log2;
   a->n_cta = p.num_ctas;
   a->min_pages = p.min_pages_per_cta > 0 ? p.min_pages_per_cta : da::kMinPagesPerCta;
+  a->k_ring = p.k_ring_pages;
   for (int i = 0; i < 64; ++i) a->turn_freq[i] = pl->turn_freq[i];
 }
 
@@ -156,8 +158,13 @@ int draft_attn_check_params(const da_params* p) {
   if (p->tree_size > 0 && (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) &&
       p->tree_size > p->window)
     return DA_ERR_INVALID_ARG;
-  for (int i = 0; i < 2; ++i)
-    if (p->reserved[i] != 0) return DA_ERR_INVALID_ARG;
+  if (p->reserved[0] != 0) return DA_ERR_INVALID_ARG;
+  if (p->k_ring_pages != 0) {   // FOLD's rotated K kept for the local window only
+    if (p->mode != DA_MODE_FOLD || p->window < 1) return DA_ERR_INVALID_ARG;
+    if (p->k_ring_pages < (p->window + da::kPage - 1) / da::kPage + 1) return DA_ERR_INVALID_ARG;
+    if ((int64_t)p->k_ring_pages * p->batch * p->num_kv_heads * da::kPage >= (int64_t)1 << 31)
+      return DA_ERR_INVALID_ARG;
+  }
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;
   }
@@ -251,6 +258,7 @@ int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, con
                          int32_t batch, int32_t n_new, const int32_t* block_table, void* k_cache,
                          void* v_cache, void* k_side, void* stream) {
   if (!pl || batch < 0 || batch > pl->p.batch || n_new < 0) return DA_ERR_INVALID_ARG;
+  if (pl->p.k_ring_pages > 0 && batch != pl->p.batch) return DA_ERR_INVALID_ARG;
   if (batch == 0 || n_new == 0) return DA_OK;
   if (!k_new || !v_new || !pos || !block_table || !k_cache || !v_cache) return DA_ERR_INVALID_ARG;
   if (pl->p.mode == DA_MODE_FOLD && !k_side) return DA_ERR_INVALID_ARG;
@@ -271,6 +279,7 @@ int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, con
   a.H_kv = pl->p.num_kv_heads;
   a.max_pages = pl->p.max_pages_per_seq;
   a.num_pages = pl->p.num_pages;
+  a.k_ring = pl->p.k_ring_pages;
   for (int i = 0; i < 64; ++i) a.turn_freq[i] = pl->turn_freq[i];
   cudaError_t e = da::launch_append(pl->p.dtype, pl->p.head_dim, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
@@ -309,10 +318,13 @@ int prepare_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t
       (k_side && !aligned(k_side, 16)))
     return DA_ERR_INVALID_ARG;
   if (workspace_bytes < pl->ws_bytes) return DA_ERR_WORKSPACE_TOO_SMALL;
-  if (!encode_cache_map(&r->mk, k_cache, pl->p) || !encode_cache_map(&r->mv, v_cache, pl->p))
+  const int64_t k_pages = pl->p.k_ring_pages > 0 ? (int64_t)pl->p.k_ring_pages * pl->p.batch
+                                                 : (int64_t)pl->p.num_pages;
+  if (!encode_cache_map(&r->mk, k_cache, pl->p, k_pages) ||
+      !encode_cache_map(&r->mv, v_cache, pl->p, pl->p.num_pages))
     return DA_ERR_CUDA;
   if (fold) {
-    if (!encode_cache_map(&r->ms, k_side, pl->p)) return DA_ERR_CUDA;
+    if (!encode_cache_map(&r->ms, k_side, pl->p, pl->p.num_pages)) return DA_ERR_CUDA;
   } else {
     r->ms = r->mk;
   }

@@ -59,6 +59,7 @@ struct DecodeArgs {
   // this kernel start, so every input but the caches it writes may be read
   // before griddepcontrol.wait; only the producer's first cache load waits.
   int32_t inputs_ready;
+  int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + P mod k_ring
   float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 

@@ -54,6 +54,7 @@ struct AppendArgs {
   void* k_side;
   uint32_t* status;
   int32_t B, n_new, H_kv, max_pages, num_pages;
+  int32_t k_ring;   // rotated K of page P of sequence b at b * k_ring + P mod k_ring (0: paged)
   float2 turn_freq[64];
 };
 cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st);

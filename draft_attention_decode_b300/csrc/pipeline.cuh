@@ -210,6 +210,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
   for (int64_t base = xs; base < xe; base += 32) {
     const int64_t x = base + lane;
     int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree;
+    int32_t kphys = -1;   // page of the K array (the ring slot of a FOLD local page)
     if (x < xe) {
       const Where w = locate(s, a.B, a.H_kv, x);
       const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
@@ -226,6 +227,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
       flags = (first ? kFirst : 0) | (last ? kLast : 0) | (phys >= 0 ? kValid : 0);
       far = (fold && w.r == 0) ? 1 : 0;
+      kphys = (a.k_ring > 0 && !far) ? w.b * a.k_ring + P % a.k_ring : phys;
       if (a.tree_mask && a.n_tree > 0 && !far) {
         const int32_t t0 = s.len[w.b] - a.n_tree;   // position of tree token 0
         if (pk0 + kPage > t0) toff = pk0 - t0;
@@ -240,6 +242,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const int32_t jfar = __shfl_sync(0xffffffffu, far, j);
       const int32_t jh = __shfl_sync(0xffffffffu, h, j);
       const int32_t jtoff = __shfl_sync(0xffffffffu, toff, j);
+      const int32_t jkphys = __shfl_sync(0xffffffffu, kphys, j);
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
@@ -254,10 +257,11 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
           if (jflags & kValid) {
             mbar_arrive_expect_tx(&s.full[st], L.stage_bytes);
             const int32_t y = (jphys * a.H_kv + jh) * kPage;
+            const int32_t yk = (jkphys * a.H_kv + jh) * kPage;
             const CUtensorMap* km = jfar ? ms : mk;
 #pragma unroll
             for (int cb = 0; cb < NCB; ++cb) {
-              tma_load_2d(kdst + cb * kBoxBytes, km, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+              tma_load_2d(kdst + cb * kBoxBytes, km, cb * (kSwizzleRow / ES), yk, &s.full[st], pol);
               tma_load_2d(vdst + cb * kBoxBytes, mv, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
             }
           } else {

@@ -125,7 +125,18 @@ typedef struct {
   int32_t tree_size;         /* draft-tree tokens at the end of each context,
                                 0..64 (<= window in window and FOLD modes); the
                                 per-query masks go to draft_attn_run_tree        */
-  int32_t reserved[2];       /* must be zero                                       */
+  int32_t k_ring_pages;      /* FOLD only: 0, or R >= ceil(window / 64) + 1.  The
+                                rotated K cache then keeps only the local window:
+                                logical page P of sequence b lives at page
+                                b * R + (P mod R) of k_cache (batch * R pages),
+                                while the side cache and the V cache stay paged
+                                by the block table.  The far memory reads the
+                                side cache only, so the unrotated keys are the
+                                one full-length copy of K.  Appends then cover
+                                every sequence (batch = params.batch), and one
+                                call must not hold two positions R * 64 apart
+                                (they would share a slot).                       */
+  int32_t reserved[1];       /* must be zero                                       */
 } da_params;
 
 typedef struct {
@@ -167,7 +178,9 @@ void draft_attn_plan_destroy(da_plan_t plan);
  * (error a few 1e-7 rad below 2^24), the rotation in FP32, the store rounds
  * to nearest even.  A negative position skips the token (padding for ragged batches).
  * batch may be below params.batch (pass a block_table offset by rows to
- * append to a subset).  k_side is required when params.mode is FOLD.
+ * append to a subset), except with params.k_ring_pages, where row b of the
+ * call is sequence b of the ring (batch must equal params.batch; pad with
+ * negative positions).  k_side is required when params.mode is FOLD.
  * "FOLD ...", review (the unrotated side cache); Windowed-MTP, Abstract (the
  * draft KV grows by one token per draft step). */
 int draft_attn_append_kv(da_plan_t plan, const void* k_new, const void* v_new,
@@ -275,7 +288,9 @@ int draft_attn_run_static(da_plan_t plan, const void* q, const int32_t* q_pos,
  * same device routines as draft_attn_run_tree (tree_mask: as there, may be
  * NULL).  Per key, ascending by position:
  * positions (int32), phys_slot = physical_page * page_size + slot (int64, -1
- * for an invalid block-table entry), key_rope_pos (the position the key is
+ * for an invalid block-table entry; the block table's page, where V and the
+ * side cache live: with k_ring_pages a local key's rotated K sits in the
+ * ring page given there), key_rope_pos (the position the key is
  * rotated at: its own, or P_far for FOLD far keys), q_rope_pos (the position
  * the kernel rotates the query by: q_pos, or q_pos - P_far for far keys) and
  * segment (0 main/local, 1 FOLD far).  At most `capacity` entries are written;

@@ -74,6 +74,12 @@ def _ok_params(**kw):
     (dict(tree_size=-1), -1),
     (dict(mode="window", window=16, tree_size=32), -1),   # tree must fit in the window
     (dict(mode="fold", window=64, alpha=2.0, far_mix=0.5, tree_size=64), 0),
+    # FOLD's rotated keys in a ring of R >= ceil(W / 64) + 1 pages per sequence
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, k_ring_pages=5), 0),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, k_ring_pages=4), -1),
+    (dict(mode="fold", window=128, alpha=2.0, far_mix=0.5, k_ring_pages=3), 0),
+    (dict(mode="full", k_ring_pages=5), -1),
+    (dict(mode="window", window=200, k_ring_pages=5), -1),
 ])
 def test_check_params(kw, code):
     assert B.draft_attn_check_params(_ok_params(**kw)) == code
@@ -81,7 +87,7 @@ def test_check_params(kw, code):
 
 def test_reserved_must_be_zero():
     p = _ok_params()
-    p.reserved[1] = 1
+    p.reserved[0] = 1
     assert B.draft_attn_check_params(p) == -1
 
 
