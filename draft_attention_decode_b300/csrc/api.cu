@@ -203,8 +203,8 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   pl->device = device;
   pl->num_sms = sms;
   pl->rows = (params->num_q_heads / params->num_kv_heads) * params->n_q;
-  if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, params->engine,
-                         params->stages, max_smem, &pl->choice)) {
+  if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, params->mode,
+                         params->engine, params->stages, max_smem, &pl->choice)) {
     delete pl;
     return DA_ERR_UNSUPPORTED;
   }

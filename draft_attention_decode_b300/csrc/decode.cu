@@ -6,7 +6,7 @@
 
 namespace da {
 
-bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int stages,
+bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
                    int max_smem, Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
   // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
@@ -15,6 +15,7 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int s
   bool mma = dtype == DA_DTYPE_BF16 && rows > 4;
   if (engine_hint == 1) mma = false;
   if (engine_hint == 2) mma = true;
+  c->pingpong = false;
   if (mma) {
     if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
     c->engine = DA_ENGINE_MMA;
@@ -25,9 +26,13 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int s
     c->engine = DA_ENGINE_CUDA_CORE;
     c->rk = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
     c->variant = kVariantCore;
+    // Turn-taking warp groups pay off on long selections (full, FOLD,
+    // SharpDraft); a window's few pages per CTA keep all eight warps together.
+    c->pingpong = c->rk <= 4 && mode != DA_MODE_WINDOW;
   }
   // Deepest pipeline that fits (a requested depth must fit as it is).
-  const int s_hi = stages > 0 ? stages : kMaxAutoStages, s_lo = stages > 0 ? stages : 2;
+  const int s_hi = stages > 0 ? stages : (c->pingpong ? kMaxAutoStagesCore : kMaxAutoStages);
+  const int s_lo = stages > 0 ? stages : 2;
   for (int s = s_hi; s >= s_lo; --s) {
     const Layout L = make_layout(c->variant, es, d, c->rk, s, batch);
     if ((int)L.total <= max_smem) {
@@ -53,11 +58,15 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
     return cudaErrorInvalidValue;
   }
 #define DA_CORE(T, D, RK)                                                                     \
-  if (dtype == (sizeof(T) == 2 ? DA_DTYPE_BF16 : DA_DTYPE_FP32) && d == D && c.rk == RK)         \
-    return f(decode_kernel<T, D,                                                               \
-                           std::conditional_t<(RK <= 4), CoreEngine<T, D, RK>,                  \
-                                              CoreEngineWide<T, D, RK>>,                        \
-                           kVariantCore, RK>);
+  if (dtype == (sizeof(T) == 2 ? DA_DTYPE_BF16 : DA_DTYPE_FP32) && d == D && c.rk == RK) {       \
+    if constexpr (RK <= 4) {                                                                     \
+      if (c.pingpong)                                                                            \
+        return f(decode_kernel<T, D, CoreEngine<T, D, RK, true>, kVariantCore, RK>);             \
+      return f(decode_kernel<T, D, CoreEngine<T, D, RK, false>, kVariantCore, RK>);              \
+    } else {                                                                                     \
+      return f(decode_kernel<T, D, CoreEngineWide<T, D, RK>, kVariantCore, RK>);                 \
+    }                                                                                            \
+  }
   DA_CORE(bf, 128, 1) DA_CORE(bf, 128, 2) DA_CORE(bf, 128, 4) DA_CORE(bf, 128, 8)
   DA_CORE(bf, 64, 1) DA_CORE(bf, 64, 2) DA_CORE(bf, 64, 4) DA_CORE(bf, 64, 8)
   DA_CORE(float, 128, 1) DA_CORE(float, 128, 2) DA_CORE(float, 128, 4) DA_CORE(float, 128, 8)

@@ -198,28 +198,36 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core engine, 1..4 rows.  Warp w owns keys 8w .. 8w+7 of each page; the
-// eight lanes of key group kg (lane bits 3, 4) share key 8w + kg (+4 on the
-// second pass) and lane ds (bits 0..2) owns D/8 of its dimensions, read as
-// 16-byte chunks whose order is rotated by ds (no bank conflicts under the
-// 128-byte swizzle).  QK^T: per-lane partial dots, then a reduce-scatter
-// leaves lane ds with row ds's score.  PV runs in the same layout: the row
-// probabilities of the lane's key come back by shuffle, the lane accumulates
-// p * V over its own dimensions, and the key groups are summed only at the
-// end of a piece.  Two consecutive pages of a piece are processed together
-// (one softmax step, twice the independent work in flight per warp).  The
-// running maximum is raised lazily (only when a score exceeds it by more than
-// 2^8): the result is exact for any reference value, and the accumulators are
-// rescaled only a handful of times.
+// CUDA-core engine, 1..4 rows.  Without PINGPONG the eight consumer warps
+// share every step (two consecutive pages of a piece, or one) and warp w owns
+// keys 8w .. 8w+7 of each page.  With PINGPONG (the long selections of full,
+// FOLD and SharpDraft) they form two groups of four that take turns: a group
+// takes a whole step, the other group the next one, so each scheduler holds
+// one warp of each group and one group's reductions and shuffles overlap the
+// other's dot products; warp w of a group owns keys 16w .. 16w+15.  The eight
+// lanes of key group kg (lane bits 3, 4) share key KPW w + kg + 4 ps on pass
+// ps and lane ds (bits 0..2) owns D/8 of its
+// dimensions, read as 16-byte chunks whose order is rotated by ds (no bank
+// conflicts under the 128-byte swizzle).  QK^T: per-lane partial dots, then a
+// reduce-scatter leaves lane ds with row ds's score.  PV runs in the same
+// layout: the row probabilities of the lane's key come back by shuffle, the
+// lane accumulates p * V over its own dimensions, and the key groups are
+// summed only at the end of a piece.  The running maximum is raised lazily
+// (only when a score exceeds it by more than 2^8): the result is exact for
+// any reference value, and the accumulators are rescaled only a handful of
+// times.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int RK>
+template <typename T, int D, int RK, bool PINGPONG>
 struct CoreEngine {
   static constexpr int NCW = kConsumerWarps;
   static constexpr int NCT = NCW * 32;
   static constexpr bool kPairs = true;         // takes two pages per step
+  static constexpr bool kPingPong = PINGPONG;  // the two warp groups alternate steps
+  static constexpr int GW = PINGPONG ? NCW / 2 : NCW;   // warps sharing a step
   static constexpr int LPK = 8;                // lanes per key
   static constexpr int KG = 32 / LPK;          // key groups per pass
-  static constexpr int KPW = 64 / NCW;         // keys per warp and page (= 2 KG)
+  static constexpr int KPW = 64 / GW;          // keys per warp and page
+  static constexpr int PP = KPW / KG;          // passes per page
   static constexpr int ES = sizeof(T);
   static constexpr int DQ = D / LPK;           // dimensions per lane
   static constexpr int NCH = DQ * ES / 16;     // 16-byte chunks per lane (1, 2 or 4)
@@ -231,8 +239,14 @@ struct CoreEngine {
   float2 q2[RK][DQ / 2];
   float2 o2[RK][DQ / 2];
   float m_run, l_run;    // row ds & (RK-1): reference maximum, partial sum
-  uint32_t off[2][NCH];  // swizzled byte offsets of the lane's chunks, pass 0/1
+  // Swizzled byte offsets of the lane's chunks on passes 0 and 1; pass ps adds
+  // 1024 (ps / 2) bytes: its row is 8 further on and has the same swizzle.
+  uint32_t off[2][NCH];
   int lane, warp, kg, ds;
+  static_assert(KG == 4, "rows of passes ps and ps + 2 differ by 8");
+  __device__ __forceinline__ uint32_t off_of(int ps, int i) const {
+    return off[ps & 1][i] + (uint32_t)(ps >> 1) * (8 * kSwizzleRow);
+  }
 
   __device__ __forceinline__ int chunk_of(int i) const {
     return ds * NCH + ((i + ((ds * NCH) >> 3)) & (NCH - 1));
@@ -249,10 +263,13 @@ struct CoreEngine {
     for (int it = 0; it < 2; ++it)
 #pragma unroll
       for (int i = 0; i < NCH; ++i)
-        off[it][i] = swz_addr(0u, warp * KPW + kg + KG * it, chunk_of(i) * 16);
+        off[it][i] = swz_addr(0u, (warp & (GW - 1)) * KPW + kg + KG * it, chunk_of(i) * 16);
   }
 
-  __device__ __forceinline__ bool owns(uint32_t) const { return true; }
+  // Step u (a pair or a single page) belongs to warp group u mod 2.
+  __device__ __forceinline__ bool owns(uint32_t u) const {
+    return !PINGPONG || (int)(u & 1u) == warp / GW;
+  }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -282,13 +299,14 @@ struct CoreEngine {
   __device__ __forceinline__ void pages(const Smem& s, const uint32_t (&kb)[NP],
                                         const uint32_t (&vb)[NP], const int (&lo)[NP],
                                         const int (&hi)[NP], const int (&toff)[NP]) {
-    constexpr int NIT = 2 * NP;
+    constexpr int NIT = PP * NP;
+    const int kw = (warp & (GW - 1)) * KPW + kg;   // the lane's key on pass 0
     float sc[NIT];
     bool ok[NIT];
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
-      const int pg = it >> 1, ps = it & 1;
-      const int key = warp * KPW + kg + KG * ps;
+      const int pg = it / PP, ps = it % PP;
+      const int key = kw + KG * ps;
       ok[it] = key >= lo[pg] && key < hi[pg];
       float2 acc[RK];
 #pragma unroll
@@ -296,7 +314,7 @@ struct CoreEngine {
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         float f[EPC];
-        Chunk<T>::load(kb[pg] + off[ps][i], f);
+        Chunk<T>::load(kb[pg] + off_of(ps, i), f);
 #pragma unroll
         for (int e = 0; e < EPC / 2; ++e) {
           const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
@@ -310,16 +328,6 @@ struct CoreEngine {
       const float sr = reduce_scatter<RK, LPK>(v, ds);
       sc[it] = ok[it] ? sr : -INFINITY;
     }
-    // The V chunks of every key, loaded now so that their latency overlaps the
-    // softmax.  A key outside [lo, hi) may hold anything, NaN included: it reads
-    // the zeroed chunk instead (its probability is 0).
-    uint32_t vw[NIT][NCH][4];
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-      const int pg = it >> 1, ps = it & 1;
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) Chunk<T>::raw(ok[it] ? vb[pg] + off[ps][i] : s.zero16, vw[it][i]);
-    }
     // Draft-tree keys the row does not see (only pages that hold tree keys).
     bool has_tree = false;
 #pragma unroll
@@ -327,10 +335,8 @@ struct CoreEngine {
     if (has_tree) {
       const uint64_t tm = s.tmask[ds & (RK - 1)];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int key = warp * KPW + kg + KG * (it & 1);
-        if (!tree_visible(key, toff[it >> 1], tm)) sc[it] = -INFINITY;
-      }
+      for (int it = 0; it < NIT; ++it)
+        if (!tree_visible(kw + KG * (it % PP), toff[it / PP], tm)) sc[it] = -INFINITY;
     }
     // Row maximum over the warp's keys (lanes with the same ds).
     float mx = sc[0];
@@ -360,9 +366,11 @@ struct CoreEngine {
       p[it] = sc[it] > -INFINITY ? fast_exp2(sc[it] - m_run) : 0.f;
       l_run += p[it];
     }
-    // PV in the QK^T layout.
+    // PV in the QK^T layout.  A key outside [lo, hi) may hold anything, NaN
+    // included: it reads the zeroed chunk instead (its probability is 0).
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
+      const int pg = it / PP, ps = it % PP;
       float pr[RK];
 #pragma unroll
       for (int r = 0; r < RK; ++r)
@@ -370,7 +378,7 @@ struct CoreEngine {
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         float f[EPC];
-        Chunk<T>::cvt(vw[it][i], f);
+        Chunk<T>::load(ok[it] ? vb[pg] + off_of(ps, i) : s.zero16, f);
 #pragma unroll
         for (int e = 0; e < EPC / 2; ++e) {
           const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
@@ -453,6 +461,7 @@ struct CoreEngine {
 template <typename T, int D, int RK>
 struct CoreEngineWide {
   static constexpr bool kPairs = false;
+  static constexpr bool kPingPong = false;
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int ES = sizeof(T);
@@ -675,6 +684,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <int D, int NT, bool SPLIT_PAGES>
 struct MmaEngine {
   static constexpr bool kPairs = false;
+  static constexpr bool kPingPong = false;
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
@@ -1102,6 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t base = smem_u32(s.stage);
   uint32_t n = 0, pages = 0;
+  uint32_t unit = 0;   // steps taken (a pair or a single page): the ping-pong turn
+  const bool long_stretch = !Engine::kPingPong || xe - xs >= 4;
   for (int64_t x = xs; x < xe;) {
     const uint32_t st = n % L.stages;
     if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status)) break;
@@ -1117,8 +1129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool last = (inf.flags & kLast) != 0;
     uint32_t taken = 1;
     if constexpr (Engine::kPairs) {
-      // the next page belongs to the same piece unless this one ends it
-      if (!last) {
+      // the next page belongs to the same piece unless this one ends it; a
+      // short stretch goes page by page, so that both warp groups work
+      if (!last && long_stretch) {
         const uint32_t st1 = (n + 1) % L.stages;
         if (!mbar_wait(&s.full[st1], ((n + 1) / L.stages) & 1u, a.status)) break;
         const PageInfo inf1 = s.info[st1];
@@ -1128,7 +1141,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo[2] = {lo0, (inf1.flags & kValid) ? (inf1.lohi & 0xffff) : 0};
         const int hi[2] = {hi0, (inf1.flags & kValid) ? (inf1.lohi >> 16) : 0};
         const int to[2] = {to0, inf1.toff};
-        eng.template pages<2>(s, kb, vb, lo, hi, to);
+        if (eng.owns(unit)) {
+          if constexpr (Engine::kPingPong && sizeof(T) == 4) {   // fp32: a step per page
+            const uint32_t k1[1] = {kb[0]}, v1[1] = {vb[0]}, k2[1] = {kb[1]}, v2[1] = {vb[1]};
+            const int l1[1] = {lo[0]}, h1[1] = {hi[0]}, t1[1] = {to[0]};
+            const int l2[1] = {lo[1]}, h2[1] = {hi[1]}, t2[1] = {to[1]};
+            eng.template pages<1>(s, k1, v1, l1, h1, t1);
+            eng.template pages<1>(s, k2, v2, l2, h2, t2);
+          } else {
+            eng.template pages<2>(s, kb, vb, lo, hi, to);
+          }
+        }
         __syncwarp();
         if ((threadIdx.x & 31) == 0) {
           mbar_arrive(&s.empty[st]);
@@ -1139,13 +1162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (taken == 1) {
-      if (hi0 > lo0 && eng.owns(n)) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
+      const bool mine = Engine::kPingPong ? eng.owns(unit) : eng.owns(n);
+      if (hi0 > lo0 && mine) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
     }
     pages += taken;
     x += taken;
     n += taken;
+    ++unit;
     if (last) {
       eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
       ticket<T, D, RK, NCT>(a, s, inf.seq, pages);

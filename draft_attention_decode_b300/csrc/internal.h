@@ -29,14 +29,15 @@ struct Choice {
   int engine;      // DA_ENGINE_CUDA_CORE or DA_ENGINE_MMA
   int variant;     // kVariantCore or kVariantMma (shared-memory layout)
   int rk;          // rows the kernel instance computes
+  bool pingpong;   // CUDA cores, <= 4 rows: the two consumer warp groups take turns
   int stages;      // pipeline depth
   uint32_t smem;   // dynamic shared memory bytes
 };
 
 // Picks the kernel instance for `rows` query rows per KV head (engine_hint:
-// 0 automatic, 1 CUDA cores, 2 tensor cores); false when none exists or it
-// does not fit in `max_smem` bytes of shared memory.
-bool choose_kernel(int dtype, int d, int rows, int batch, int engine_hint, int stages,
+// 0 automatic, 1 CUDA cores, 2 tensor cores) in `mode`; false when none
+// exists or it does not fit in `max_smem` bytes of shared memory.
+bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
                    int max_smem, Choice* c);
 
 cudaError_t prepare_decode(const Choice& c, int dtype, int d);

@@ -121,7 +121,9 @@ typedef struct {
                                 min(num_ctas, ceil(P / this)) CTAs; 0 = default
                                 (2)                                               */
   int32_t stages;            /* shared-memory pipeline depth in pages, 2..8;
-                                0 = as deep as shared memory allows (<= 4)       */
+                                0 = as deep as shared memory allows (<= 6 for
+                                the CUDA-core engine outside window mode, <= 4
+                                otherwise)                                       */
   int32_t tree_size;         /* draft-tree tokens at the end of each context,
                                 0..64 (<= window in window and FOLD modes); the
                                 per-query masks go to draft_attn_run_tree        */

@@ -136,6 +136,16 @@ def sample_groups(batch, n_q, H_kv, k, seed):
     return [allg[i] for i in sorted(idx)]
 
 
+def equal_up_to_one_rounding(a, b):
+    """Element-wise |a - b| <= one bf16 ulp of the larger magnitude: two
+    kernels that compute the same attention with a different summation order
+    (the CUDA-core engine with or without turn-taking warp groups) round to
+    the same or an adjacent bf16 value."""
+    x = a.float().cpu().numpy().astype(np.float64)
+    y = b.float().cpu().numpy().astype(np.float64)
+    return bool((np.abs(x - y) <= bf16_ulp(np.maximum(np.abs(x), np.abs(y)))).all())
+
+
 def bf16_ulp(x):
     """Spacing of bfloat16 at |x| (normal range)."""
     ax = np.maximum(np.abs(x), 2.0 ** -126)
