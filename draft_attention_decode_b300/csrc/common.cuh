@@ -193,7 +193,7 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 constexpr int kMaxAutoStages = 4;       // pipeline depth chosen when da_params.stages = 0
 constexpr int kMaxAutoStagesCore = 6;   // the same for the CUDA-core engines (two warp
                                         // groups hold two steps, the producer fills more)
-constexpr int kMinPagesPerCta = 2;   // default split floor (da_params.min_pages_per_cta = 0)
+constexpr int kMinPagesPerCta = 1;   // default split floor (da_params.min_pages_per_cta = 0)
 
 __host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t TP, int64_t n) {
   return (i * TP) / n;

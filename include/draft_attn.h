@@ -119,7 +119,7 @@ typedef struct {
   int32_t min_pages_per_cta; /* split floor: a call whose selection has P pages
                                 (over all sequences and KV heads) runs on
                                 min(num_ctas, ceil(P / this)) CTAs; 0 = default
-                                (2)                                               */
+                                (1)                                               */
   int32_t stages;            /* shared-memory pipeline depth in pages, 2..8;
                                 0 = as deep as shared memory allows (<= 6 for
                                 the CUDA-core engine outside window mode, <= 4
