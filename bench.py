@@ -675,9 +675,23 @@ def context_sweep(dev, args, flush, dist, peak):
     dl.close()
     del dl
     torch.cuda.empty_cache()
+    # the configuration's own draft loop: 6 steps (append + attend) at 1M context
+    dl = DraftLoop(base, dev, ("full", "window"))
+    loop = {"context": base.ctx[0], "draft_steps": dl.steps}
+    for m in ("full", "window"):
+        g = dl.capture(m)
+        ms, _ = time_graph(g, max(args.steps // 4, 10), args.warmup, flush, dist)
+        nb = dl.kv_bytes(m)
+        loop[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 2),
+                   "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                   "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+    dl.close()
+    del dl
+    torch.cuda.empty_cache()
     w = [r["window"]["us"] for r in rows]
     return {"shape": "64/8 heads, d128, bf16, theta 1e6, W=4096 + 4 sinks, 1 query",
-            "rows": rows, "window_max_over_min": round(max(w) / min(w), 3)}
+            "rows": rows, "window_max_over_min": round(max(w) / min(w), 3),
+            "draft_loop_1m": loop}
 
 
 def all_workloads(dev, args, flush, dist, peak, names):
