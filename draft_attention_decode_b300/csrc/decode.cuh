@@ -1,19 +1,22 @@
-// Split-KV decode kernel: the pipeline of pipeline.cuh driving one of two
+// Split-KV decode kernel: the pipeline of pipeline.cuh driving one of three
 // compute engines.
 //
-//  * CoreEngine (<= 4 query rows per KV head by default, <= 8 on request:
-//    one draft token over a small GQA group).  QK^T and PV on the FP32 pipes with packed two-wide FMAs; no
+//  * CoreEngine (<= 4 query rows per KV head: one draft token over a small GQA
+//    group).  QK^T and PV on the FP32 pipes with packed two-wide FMAs; no
 //    tensor cores, since with this few rows the page read, not arithmetic, is
-//    the bound.  Each warp owns 8 of the page's 64 keys: for QK^T eight lanes
-//    share one key (16 dimensions each at d = 128) and a reduce-scatter
-//    butterfly leaves lane i with row i's score; for PV every lane owns d/32
-//    dimensions of all rows.
+//    the bound.  Eight lanes share a key (16 dimensions each at d = 128), a
+//    reduce-scatter butterfly leaves lane i with row i's score, and PV runs in
+//    the same layout.  With PINGPONG (long selections) the consumer warps form
+//    two groups that take alternate steps.
+//  * CoreEngineWide (5..8 rows on the FP32 pipes: fp32 caches, or on
+//    request).  QK^T as in CoreEngine; for PV every lane owns d/32 dimensions
+//    of all rows.
 //  * MmaEngine (5..32 rows: a GQA group of 8, or draft trees).  QK^T and PV as
 //    bf16 m16n8k16 tensor-core MMAs with FP32 accumulation, keys on the M side
 //    of QK^T (S^T = K Q^T) so that 8-row query tiles need no padding, P^T
 //    moved into the PV operand layout with movmatrix.
 //
-// Both keep one online softmax (m, l, o) per warp and query row, in the log2
+// All keep an online softmax (m, l, o) per warp and query row, in the log2
 // domain (the query is pre-scaled by softmax_scale * log2 e and by alpha or
 // gamma), and merge the eight warps only at the end of a piece.
 #pragma once
