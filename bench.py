@@ -462,42 +462,44 @@ def workload_config(wl, mode_note):
 # ---------------------------------------------------------------------------
 
 def e2e_full(dl: DraftLoop, steps, warmup, dist):
-    """The headline metric through the public API with host buffers: every
-    draft step copies its query, new K/V token, positions and lengths from
-    pinned host memory (packed in one buffer, so one copy), appends, attends
-    and reads the output back."""
+    """The headline metric through the public API with host buffers.  One step
+    is one draft loop: the inputs of all its draft steps (queries, new K/V
+    tokens, positions, lengths) go to the device in one copy from pinned host
+    memory, each draft step is one draft_attn_step call, and the outputs of all
+    draft steps come back in one copy, read by the host before the next loop."""
     da = dl.plans["full"]
     parts = [dl.q, dl.k_new, dl.v_new, dl.pos, dl.qpos, dl.lens]
     offs, nb = [], 0
-    for p in parts:                      # 256-byte aligned slots of one staging buffer
-        offs.append(nb)
-        nb += (p[0].numel() * p[0].element_size() + 255) // 256 * 256
-    host = []
-    for s in range(dl.steps):
-        h = torch.empty(nb, dtype=torch.uint8).pin_memory()
-        for p, o in zip(parts, offs):
-            x = p[s].contiguous()
-            n = x.numel() * x.element_size()
-            h[o:o + n].copy_(x.view(-1).view(torch.uint8).cpu())
-        host.append(h)
+    for s in range(dl.steps):            # 256-byte aligned slots of one staging buffer
+        row = []
+        for p in parts:
+            row.append(nb)
+            nb += (p[s].numel() * p[s].element_size() + 255) // 256 * 256
+        offs.append(row)
+    host = torch.empty(nb, dtype=torch.uint8).pin_memory()
     dbuf = torch.empty(nb, dtype=torch.uint8, device=dl.dev)
     views = []
-    for p, o in zip(parts, offs):
-        x = p[0]
-        n = x.numel() * x.element_size()
-        views.append(dbuf[o:o + n].view(x.dtype).view(x.shape))
-    dq, dk, dv, dp, dqp, dln = views
-    hout = torch.empty(tuple(dl.out.shape), dtype=dl.out.dtype).pin_memory()
+    for s in range(dl.steps):
+        vs = []
+        for p, o in zip(parts, offs[s]):
+            x = p[s].contiguous()
+            n = x.numel() * x.element_size()
+            host[o:o + n].copy_(x.view(-1).view(torch.uint8).cpu())
+            vs.append(dbuf[o:o + n].view(x.dtype).view(x.shape))
+        views.append(vs)
+    outs = torch.empty((dl.steps,) + tuple(dl.out.shape), dtype=dl.out.dtype, device=dl.dev)
+    hout = torch.empty(tuple(outs.shape), dtype=outs.dtype).pin_memory()
     h2d = nb
     d2h = hout.numel() * hout.element_size()
 
     def one():
+        dbuf.copy_(host, non_blocking=True)
         for s in range(dl.steps):
-            dbuf.copy_(host[s], non_blocking=True)
+            dq, dk, dv, dp, dqp, dln = views[s]
             da.step(dk, dv, dp, dq, dqp, dln, dl.bt, dl.k_cache, dl.v_cache, dl.k_side,
-                    out=dl.out)
-            hout.copy_(dl.out, non_blocking=True)
-            torch.cuda.current_stream().synchronize()   # the draft head needs the output
+                    out=outs[s])
+        hout.copy_(outs, non_blocking=True)
+        torch.cuda.current_stream().synchronize()   # the host reads the loop's outputs
     for _ in range(warmup):
         one()
     torch.cuda.synchronize(); dist.barrier(); torch.cuda.synchronize()
@@ -506,7 +508,7 @@ def e2e_full(dl: DraftLoop, steps, warmup, dist):
         one()
     torch.cuda.synchronize(); dist.barrier(); torch.cuda.synchronize()
     dt = dist.max((time.perf_counter() - t0) / steps)
-    return dt, h2d * dl.steps, d2h * dl.steps
+    return dt, h2d, d2h
 
 
 def run_ours(args, dist):
@@ -601,9 +603,9 @@ def run_ours(args, dist):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "full mode, pinned host buffers, one H2D copy of each draft step's "
-                        "packed inputs and a D2H of its output inside the timed region, stream "
-                        "sync per draft step"},
+                "note": "full mode, pinned host buffers; per step (one 4-draft-step loop) one "
+                        "H2D copy of all its inputs, four draft_attn_step calls, one D2H copy "
+                        "of the four outputs and a host sync, inside the timed region"},
         "gpu_launches": launches,
         "clocks": clk,
         "sweep": sweep,
