@@ -39,7 +39,10 @@ silent (all listed again in the design notes):
    at j.  The query position p is an explicit input.
 3. window: S = {0 <= j < min(n_sink, L)} union {max(0, L-W) <= j < L}.
 4. fold: Loc = {max(0, L-W) <= j < L}, Far = {0 <= j < L-W}, shared far
-   position P_far = L-W-1 (the newest far token).  Far logits are
+   position P_far = L-W-1 (the newest far token).  With n_sink > 0 (FOLD
+   combined with StreamingLLM-style sinks) the first n_sink keys join the
+   local softmax at their exact positions: Loc = {j < min(n_sink, L)} union
+   {max(0, L-W) <= j < L}, Far = {n_sink <= j < L-W}.  Far logits are
    alpha * c * <RoPE(q, p), RoPE(k_raw_j, P_far)>; two independent softmaxes;
    o = (1-lam_eff) o_loc + lam_eff o_far with lam_eff = lam if Far is non-empty
    else 0.  V is never rotated; far V comes from the main V cache.
@@ -79,7 +82,7 @@ class Params:
 
     mode: str = "full"
     window: int = 0          # W (window, fold)
-    n_sink: int = 0          # attention-sink tokens (window)
+    n_sink: int = 0          # attention-sink tokens (window, fold)
     alpha: float = 1.0       # FOLD concentration factor
     far_mix: float = 0.0     # FOLD far-memory weight lambda
     scale_slope: float = 0.0  # SharpDraft slope beta
@@ -152,9 +155,10 @@ def select_keys(mode: str, L: int, W: int = 0, n_sink: int = 0) -> dict:
         sinks = np.arange(min(n_sink, L), dtype=np.int64)
         recent = np.arange(ws, L, dtype=np.int64)
         return {"loc": np.union1d(sinks, recent).astype(np.int64), "far": empty}
-    # fold
-    return {"loc": np.arange(ws, L, dtype=np.int64),
-            "far": np.arange(0, max(0, L - W), dtype=np.int64)}
+    # fold: sinks, when given, join the local softmax (reading 4)
+    sinks = np.arange(min(n_sink, L), dtype=np.int64)
+    return {"loc": np.union1d(sinks, np.arange(ws, L, dtype=np.int64)).astype(np.int64),
+            "far": np.arange(min(n_sink, max(0, L - W)), max(0, L - W), dtype=np.int64)}
 
 
 def sharp_gamma(n_keys: int, beta: float, n_ref: int) -> float:

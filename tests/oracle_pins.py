@@ -38,7 +38,8 @@ def bf_member(mode, j, L, W, n_sink):
         return "loc"
     if mode == "window":
         return "loc" if (j < n_sink or j >= L - W) else None
-    return "loc" if j >= L - W else "far"
+    # fold: the window and the sinks are local, every other older key is far
+    return "loc" if (j >= L - W or j < n_sink) else "far"
 
 
 def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
@@ -120,7 +121,7 @@ def check_selection(orc):
              (10, 12, 0), (64, 16, 4), (65, 64, 4), (200, 63, 5), (7, 3, 10)]
     for L, W, ns in cases:
         for mode in ("full", "window", "fold", "sharp"):
-            sel = orc.select_keys(mode, L, W, ns if mode == "window" else 0)
+            sel = orc.select_keys(mode, L, W, ns if mode in ("window", "fold") else 0)
             want_loc = [j for j in range(L)
                         if bf_member(mode, j, L, W, ns) == "loc"]
             want_far = [j for j in range(L)
@@ -139,6 +140,8 @@ def check_brute_force(orc):
         dict(mode="fold", L=45, W=12, alpha=2.0, lam=0.5),
         dict(mode="fold", L=30, W=7, alpha=0.7, lam=0.25),
         dict(mode="fold", L=9, W=12, alpha=2.0, lam=0.5),
+        dict(mode="fold", L=45, W=12, n_sink=4, alpha=2.0, lam=0.5),
+        dict(mode="fold", L=15, W=12, n_sink=4, alpha=1.5, lam=0.5),
         dict(mode="sharp", L=60, beta=0.4, n_ref=8),
         dict(mode="sharp", L=5, beta=0.4, n_ref=8),
     ]
@@ -238,9 +241,16 @@ def check_mode_equivalences(orc):
         o = orc.attend_group(q, L, K, V, L, orc.Params("fold", window=W, alpha=3.0, far_mix=0.5))
         w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=W, n_sink=0))
         assert np.allclose(o, w, atol=1e-13)
-    # fold with lambda = 0 is window attention over the last W keys
-    o = orc.attend_group(q, L, K, V, L, orc.Params("fold", window=30, alpha=3.0, far_mix=0.0))
-    w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=30, n_sink=0))
+    # fold with lambda = 0 is window attention over the last W keys (and the
+    # same sinks); with sinks and an empty far memory it is that window too
+    for ns in (0, 4):
+        o = orc.attend_group(q, L, K, V, L,
+                             orc.Params("fold", window=30, n_sink=ns, alpha=3.0, far_mix=0.0))
+        w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=30, n_sink=ns))
+        assert np.allclose(o, w, atol=1e-13), ns
+    o = orc.attend_group(q, L, K, V, L, orc.Params("fold", window=L - 4, n_sink=4, alpha=3.0,
+                                                   far_mix=0.7))
+    w = orc.attend_group(q, L, K, V, L, orc.Params("window", window=L - 4, n_sink=4))
     assert np.allclose(o, w, atol=1e-13)
     # sharp with slope 0, or with |S| <= N_ref (clamp), is plain attention
     o = orc.attend_group(q, L, K, V, L, orc.Params("sharp", scale_slope=0.0, scale_ref=4))

@@ -32,6 +32,20 @@ def _rope_adjacent_pairs(x, pos, theta):
     return out
 
 
+def _fold_sinks_also_far(mode, L, W=0, n_sink=0):
+    # FOLD with sinks, the sinks counted twice: local and far
+    sel = _select_keys(mode, L, W, n_sink)
+    if mode == "fold":
+        sel = dict(sel, far=np.arange(0, max(0, L - W), dtype=np.int64))
+    return sel
+
+
+def _fold_sinks_ignored(mode, L, W=0, n_sink=0):
+    return _select_keys(mode, L, W, 0 if mode == "fold" else n_sink)
+
+
+_select_keys = orc.select_keys
+
 MUTATIONS = {
     "rope_sign": ("rope", _rope_sign),
     "rope_pairing": ("rope", _rope_adjacent_pairs),
@@ -43,6 +57,8 @@ MUTATIONS = {
     "tree_bit_off_by_one": ("tree_filter", lambda pos, L, nt, m: (
         np.asarray(pos, dtype=np.int64) if m is None or nt <= 0 else np.asarray(
             [j for j in pos if j < L - nt or (int(m) >> int(j - (L - nt) + 1)) & 1], dtype=np.int64))),
+    "fold_sinks_also_far": ("select_keys", _fold_sinks_also_far),
+    "fold_sinks_ignored": ("select_keys", _fold_sinks_ignored),
     "far_position_off_by_one": ("fold_far_position", lambda L, W: L - W),
     "gamma_no_clamp": ("sharp_gamma", lambda n, b, r: 1.0 + b * math.log(max(n, 1) / r)),
     "gamma_log2": ("sharp_gamma", lambda n, b, r: max(1.0, 1 + b * math.log2(max(n, 1) / r))),
