@@ -92,7 +92,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->num_pages = p.num_pages;
   a->mode = p.mode;
   a->W = p.window;
-  a->n_sink = p.mode == DA_MODE_WINDOW ? p.n_sink : 0;
+  a->n_sink = (p.mode == DA_MODE_WINDOW || p.mode == DA_MODE_FOLD) ? p.n_sink : 0;
   a->n_tree = p.tree_size;
   a->alpha = p.alpha;
   a->far_mix = p.far_mix;
@@ -168,9 +168,11 @@ int draft_attn_check_params(const da_params* p) {
   if (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) {
     if (p->window < 1) return DA_ERR_INVALID_ARG;
   }
-  if (p->mode == DA_MODE_WINDOW && p->n_sink < 0) return DA_ERR_INVALID_ARG;
+  if ((p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) && p->n_sink < 0)
+    return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_FOLD) {
-    if (p->n_sink != 0) return DA_ERR_INVALID_ARG;
+    // the ring keeps rotated K for the local window only, not for sinks
+    if (p->k_ring_pages != 0 && p->n_sink != 0) return DA_ERR_INVALID_ARG;
     if (!(p->alpha > 0.f) || !std::isfinite(p->alpha)) return DA_ERR_INVALID_ARG;
     if (!(p->far_mix >= 0.f && p->far_mix <= 1.f)) return DA_ERR_INVALID_ARG;
   }

@@ -93,9 +93,18 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Dec
   const int32_t L = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
   const int32_t p = __ldg(a.q_pos + b * a.n_q + t);
   const Ranges rg = mode_ranges(a.mode, L, a.W, a.n_sink);
-  const int64_t n0 = rg.k1[0] > rg.k0[0] ? rg.k1[0] - rg.k0[0] : 0;
-  const int64_t n1 = rg.k1[1] > rg.k0[1] ? rg.k1[1] - rg.k0[1] : 0;
-  const int64_t dense = n0 + n1;
+  // the ranges in position order (they are disjoint): ord[0] < ord[1] < ord[2]
+  int ord[kRanges] = {0, 1, 2};
+  for (int i = 1; i < kRanges; ++i)
+    for (int j = i; j > 0 && rg.lo(ord[j]) < rg.lo(ord[j - 1]); --j) {
+      const int t = ord[j]; ord[j] = ord[j - 1]; ord[j - 1] = t;
+    }
+  int64_t cnt[kRanges];
+  for (int i = 0; i < kRanges; ++i) {
+    const int32_t k0 = rg.lo(ord[i]), k1 = rg.hi(ord[i]);
+    cnt[i] = k1 > k0 ? k1 - k0 : 0;
+  }
+  const int64_t dense = cnt[0] + cnt[1] + cnt[2];
   // Draft-tree keys (the last `present` keys, all of them in the selection)
   // are kept only where the query's mask bit is set; they come last, so the
   // kept ones are compacted by a popcount of the lower bits.
@@ -114,8 +123,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Dec
   const int32_t pf = fold_far_pos(L, a.W);
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < dense;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int rr = idx < n0 ? 0 : 1;
-    const int32_t j = (rr ? rg.k0[1] : rg.k0[0]) + (int32_t)(idx < n0 ? idx : idx - n0);
+    const int oi = idx < cnt[0] ? 0 : (idx < cnt[0] + cnt[1] ? 1 : 2);
+    const int rr = ord[oi];
+    const int64_t before = oi == 0 ? 0 : (oi == 1 ? cnt[0] : cnt[0] + cnt[1]);
+    const int32_t j = rg.lo(rr) + (int32_t)(idx - before);
     int64_t out = idx;
     if (idx >= n_before) {
       const int i = j - base;

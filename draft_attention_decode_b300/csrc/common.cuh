@@ -69,22 +69,32 @@ __host__ __device__ constexpr int slot_o_off(int rk) { return (2 * rk + 3) / 4 *
 __host__ __device__ constexpr int slot_floats(int rk, int d) { return slot_o_off(rk) + rk * d; }
 
 // ---------------------------------------------------------------------------
-// Mode -> key ranges.  Two half-open ranges per sequence, in ascending
-// position order; range 0 of FOLD is the far memory, everything else belongs
-// to the main (local) softmax.
+// Mode -> key ranges.  Three half-open ranges per sequence (empty ones are
+// [x, x)); range 0 of FOLD is the far memory, everything else belongs to the
+// main (local) softmax.
 //   full / sharp : [0, L)                              "Windowed-MTP", Abstract
 //   window       : [0, n_sink) u [L-W, L)  (merged into [0, L) when they touch)
-//   fold         : far [0, L-W), local [L-W, L)        "FOLD", abstract
+//   fold         : far [s, L-W), local [0, s) u [L-W, L), s = min(n_sink, L-W)
+//                  ("FOLD", abstract; the sinks, when given, are exact local
+//                  keys, as in window mode)
+// Ranges are disjoint; only FOLD with sinks lists them out of position order.
 // ---------------------------------------------------------------------------
+constexpr int kRanges = 3;
 struct Ranges {
-  int32_t k0[2], k1[2];
+  int32_t k0[kRanges], k1[kRanges];
+  __host__ __device__ __forceinline__ int32_t lo(int r) const {
+    return r == 0 ? k0[0] : (r == 1 ? k0[1] : k0[2]);
+  }
+  __host__ __device__ __forceinline__ int32_t hi(int r) const {
+    return r == 0 ? k1[0] : (r == 1 ? k1[1] : k1[2]);
+  }
 };
 
 __host__ __device__ __forceinline__ Ranges mode_ranges(int mode, int32_t L, int32_t W,
                                                        int32_t n_sink) {
   Ranges r;
-  r.k0[0] = 0; r.k1[0] = 0; r.k0[1] = L; r.k1[1] = L;
-  if (L <= 0) { r.k0[1] = r.k1[1] = 0; return r; }
+  r.k0[0] = 0; r.k1[0] = 0; r.k0[1] = L; r.k1[1] = L; r.k0[2] = L; r.k1[2] = L;
+  if (L <= 0) { r.k0[1] = r.k1[1] = r.k0[2] = r.k1[2] = 0; return r; }
   int32_t ws = L - W > 0 ? L - W : 0;
   switch (mode) {
     case DA_MODE_WINDOW:
@@ -96,9 +106,11 @@ __host__ __device__ __forceinline__ Ranges mode_ranges(int mode, int32_t L, int3
         r.k0[0] = ws; r.k1[0] = L;
       }
       break;
-    case DA_MODE_FOLD:
-      r.k0[0] = 0; r.k1[0] = ws; r.k0[1] = ws; r.k1[1] = L;
+    case DA_MODE_FOLD: {
+      const int32_t sk = n_sink < ws ? n_sink : ws;
+      r.k0[0] = sk; r.k1[0] = ws; r.k0[1] = 0; r.k1[1] = sk; r.k0[2] = ws; r.k1[2] = L;
       break;
+    }
     default:  // full, sharp
       r.k0[0] = 0; r.k1[0] = L;
       break;
@@ -124,7 +136,7 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int mode, int32_t L, in
                                                         int32_t n_sink) {
   Ranges r = mode_ranges(mode, L, W, n_sink);
   int32_t n = 0;
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < kRanges; ++i)
     if (!range_is_far(mode, i) && r.k1[i] > r.k0[i]) n += r.k1[i] - r.k0[i];
   return n;
 }
@@ -180,13 +192,13 @@ __device__ __forceinline__ int32_t clamp_ctx(int32_t L, int32_t max_pages, uint3
 
 // ---------------------------------------------------------------------------
 // Flat work partition.  The pages of every (b, kv head) are laid end to end
-// (b outer, then head, then range 0 before range 1); with TP pages in all and
+// (b outer, then head, then ranges 0, 1, 2 in turn); with TP pages in all and
 // n active CTAs, CTA i takes positions [floor(i*TP/n), floor((i+1)*TP/n)).
 // n = min(grid, ceil(TP / min_pages)): a small selection (a window)
 // goes to fewer, fuller CTAs, so that each (b, head) has few pieces to merge.
 // A "piece" is the part of one (b, head, softmax segment) that one CTA covers
-// (the two ranges of window mode are one segment; FOLD's far and local ranges
-// are two).  Its seq = (b * H_kv + head) * 2 + segment never decreases along
+// (the ranges of window mode are one segment; FOLD's far range is one segment
+// and its local ranges the other).  Its seq = (b * H_kv + head) * 2 + segment never decreases along
 // the line, so slot = cta + seq is unique: every new piece advances the CTA,
 // the seq, or both.
 // ---------------------------------------------------------------------------
@@ -207,9 +219,9 @@ __host__ __device__ __forceinline__ int64_t active_ctas(int64_t TP, int64_t grid
   const int64_t want = (TP + min_pages - 1) / min_pages;
   return want < 1 ? 1 : (want < grid ? want : grid);
 }
-// Piece id of (b, head, range); FOLD keeps its two ranges apart.
+// Piece id of (b, head, range); FOLD keeps its far range apart from the rest.
 __host__ __device__ __forceinline__ int32_t piece_seq(int mode, int b, int h, int H, int range) {
-  return (b * H + h) * 2 + (mode == DA_MODE_FOLD ? range : 0);
+  return (b * H + h) * 2 + (mode == DA_MODE_FOLD && range != 0 ? 1 : 0);
 }
 __host__ __device__ __forceinline__ bool seq_is_far(int mode, int32_t seq) {
   return mode == DA_MODE_FOLD && (seq & 1) == 0;

@@ -33,7 +33,7 @@ struct PageInfo {
 struct Layout {
   uint32_t stage_bytes, stages;
   uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
-      flag_off, tm_off, rm_off, total;
+      n01_off, flag_off, tm_off, rm_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -59,6 +59,7 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.len_off = off;   off += align_up((uint32_t)batch * 4, 128);
   L.pfx_off = off;   off += align_up((uint32_t)(batch + 1) * 4, 128);
   L.n0_off = off;    off += align_up((uint32_t)batch * 4, 128);
+  L.n01_off = off;   off += align_up((uint32_t)batch * 4, 128);
   L.flag_off = off;  off += 128;
   L.tm_off = off;    off += align_up((uint32_t)rk * 8, 128);
   L.rm_off = off;    off += align_up((uint32_t)rk * 4, 128);
@@ -80,6 +81,7 @@ struct Smem {
   int32_t* len;
   int32_t* pfx;         // [B + 1] pages per head of sequences before b
   int32_t* n0;          // [B] pages per head of range 0
+  int32_t* n01;         // [B] pages per head of ranges 0 and 1
   int32_t* flag;        // broadcast of the merge ticket (word 0)
   uint32_t zero16;      // shared address of 16 zero bytes (words 16..19 of the flag block)
   uint64_t* tmask;      // [rk] visible tree keys of each row of the current piece
@@ -102,6 +104,7 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.len = reinterpret_cast<int32_t*>(p + L.len_off);
   s.pfx = reinterpret_cast<int32_t*>(p + L.pfx_off);
   s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
+  s.n01 = reinterpret_cast<int32_t*>(p + L.n01_off);
   s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
   s.zero16 = smem_u32(p + L.flag_off + 64);
   s.tmask = reinterpret_cast<uint64_t*>(p + L.tm_off);
@@ -151,8 +154,10 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
       if (b < a.B) {
         const Ranges r = mode_ranges(a.mode, s.len[b], a.W, a.n_sink);
         const int32_t n0 = range_pages(r.k0[0], r.k1[0]);
-        v = n0 + range_pages(r.k0[1], r.k1[1]);
+        const int32_t n01 = n0 + range_pages(r.k0[1], r.k1[1]);
+        v = n01 + range_pages(r.k0[2], r.k1[2]);
         s.n0[b] = n0;
+        s.n01[b] = n01;
       }
       int32_t inc = v;
 #pragma unroll
@@ -185,9 +190,9 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
   const int32_t nb = s.pfx[lo + 1] - s.pfx[lo];
   w.h = (int)(rel / nb);
   w.k = (int)(rel - (int64_t)w.h * nb);
-  const int32_t n0 = s.n0[lo];
-  w.r = w.k < n0 ? 0 : 1;
-  w.kr = w.r ? w.k - n0 : w.k;
+  const int32_t n0 = s.n0[lo], n01 = s.n01[lo];
+  w.r = w.k < n0 ? 0 : (w.k < n01 ? 1 : 2);
+  w.kr = w.k - (w.r == 0 ? 0 : (w.r == 1 ? n0 : n01));
   return w;
 }
 
@@ -214,7 +219,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
     if (x < xe) {
       const Where w = locate(s, a.B, a.H_kv, x);
       const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
-      const int32_t k0 = w.r ? rg.k0[1] : rg.k0[0], k1 = w.r ? rg.k1[1] : rg.k1[0];
+      const int32_t k0 = rg.lo(w.r), k1 = rg.hi(w.r);
       const int32_t P = k0 / kPage + w.kr;
       const int32_t pk0 = P * kPage;
       const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;

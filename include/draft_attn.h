@@ -16,6 +16,10 @@
  *                   P_far = L - W - 1, its logits sharpened by alpha; the two
  *                   are mixed as (1 - far_mix) * local + far_mix * far
  *                   (far_mix counts only when the far memory is non-empty).
+ *                   With n_sink > 0 the first n_sink keys join the local
+ *                   softmax at their own positions, as the sinks of window
+ *                   mode do, and the far memory starts after them (the
+ *                   library's reading: the FOLD page names no sinks).
  *                   "FOLD: Position-Free Far Memory with Local Order for
  *                   Long-Context Speculative Decoding", summary and abstract.
  *   DA_MODE_SHARP   all keys, logits scaled by
@@ -107,7 +111,9 @@ typedef struct {
   int32_t dtype;             /* da_dtype of q, caches and out                      */
   int32_t mode;              /* da_mode                                            */
   int32_t window;            /* W (window, fold), >= 1                             */
-  int32_t n_sink;            /* sink tokens (window only), >= 0                    */
+  int32_t n_sink;            /* sink tokens (window, fold), >= 0; in FOLD the
+                                first n_sink keys stay exact local keys and
+                                leave the far memory (not with k_ring_pages)     */
   float   alpha;             /* FOLD far-logit concentration factor, > 0           */
   float   far_mix;           /* FOLD far-memory weight lambda in [0, 1]            */
   float   scale_slope;       /* SharpDraft slope beta, >= 0                        */

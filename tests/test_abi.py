@@ -53,7 +53,9 @@ def _ok_params(**kw):
     (dict(mode="window", window=16, n_sink=-1), -1),
     (dict(mode="fold", window=16, alpha=0.0), -1),
     (dict(mode="fold", window=16, alpha=2.0, far_mix=1.5), -1),
-    (dict(mode="fold", window=16, alpha=2.0, n_sink=4), -1),
+    (dict(mode="fold", window=16, alpha=2.0, n_sink=4), 0),       # sinks join the local softmax
+    (dict(mode="fold", window=16, alpha=2.0, n_sink=-1), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=4, k_ring_pages=5), -1),
     (dict(mode="sharp", scale_slope=-1.0), -1),
     (dict(mode="sharp", scale_ref=0), -1),
     (dict(rope_theta=0.0), 0),                         # NoPE

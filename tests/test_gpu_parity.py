@@ -111,6 +111,10 @@ GATHER_CASES = [
     ("window", 100, 512, 4), ("window", 130, 64, 0), ("window", 3, 1, 10), ("window", 200, 1, 0),
     ("fold", 5000, 2048), ("fold", 2049, 2048), ("fold", 2048, 2048), ("fold", 70, 2048),
     ("fold", 1, 1),
+    # FOLD with sinks: sinks, far memory and window apart; sinks touching the
+    # window (no far memory); sinks past a page; a sink page shared with the window
+    ("fold", 5000, 2048, 4), ("fold", 2052, 2048, 4), ("fold", 2050, 2048, 4),
+    ("fold", 700, 300, 100), ("fold", 60, 40, 4), ("fold", 1, 1, 4),
     ("sharp", 777, 0),
 ]
 
@@ -148,6 +152,7 @@ MODES = [
     dict(mode="window", window=300, n_sink=4),
     dict(mode="window", window=129, n_sink=0),
     dict(mode="fold", window=200, alpha=2.0, far_mix=0.5),
+    dict(mode="fold", window=200, n_sink=70, alpha=2.0, far_mix=0.5),
     dict(mode="sharp", scale_slope=0.05, scale_ref=256),
 ]
 
@@ -156,8 +161,12 @@ def _rows(h, hk, nq):
     return (h // hk) * nq
 
 
+def _mid(m):
+    return m["mode"] + str(m.get("window", "")) + ("s%d" % m["n_sink"] if m.get("n_sink") else "")
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "h%d_%d_q%d" % s)
-@pytest.mark.parametrize("mp", MODES, ids=lambda m: m["mode"] + str(m.get("window", "")))
+@pytest.mark.parametrize("mp", MODES, ids=_mid)
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp32", 64), ("fp32", 128)])
 def test_parity_small(shape, mp, dtype, d):
     h, hk, nq = shape
@@ -176,12 +185,14 @@ def test_parity_small(shape, mp, dtype, d):
                                           ((32, 8, 1), "mma"), ((8, 8, 1), "mma"),
                                           ((16, 8, 1), "mma")],
                          ids=lambda x: str(x))
-@pytest.mark.parametrize("mode", ["full", "fold", "window", "sharp"])
+@pytest.mark.parametrize("mode", ["full", "fold", "window", "sharp", "fold_sinks"])
 def test_engine_forced(shape, engine, mode):
     """Either engine, forced, computes the same attention for 1..8 rows."""
     h, hk, nq = shape
+    ns = 4 if mode in ("window", "fold_sinks") else 0
+    mode = "fold" if mode == "fold_sinks" else mode
     s = Setup(batch=2, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
-              ctx=[2500, 700], mode=mode, window=600, n_sink=4 if mode == "window" else 0,
+              ctx=[2500, 700], mode=mode, window=600, n_sink=ns,
               alpha=2.0, far_mix=0.5, scale_slope=0.05, scale_ref=256, seed=12, engine=engine)
     assert s.da.info()["engine_name"] == engine
     compare(s.run(), s.oracle(), "bf16", f"{mode} {shape} {engine}")
@@ -189,12 +200,14 @@ def test_engine_forced(shape, engine, mode):
 
 
 @pytest.mark.parametrize("num_ctas", [1, 2, 7, 148, 600])
-@pytest.mark.parametrize("mode", ["full", "fold", "window"])
+@pytest.mark.parametrize("mode", ["full", "fold", "window", "fold_sinks"])
 def test_split_count(num_ctas, mode):
     """Any number of persistent CTAs (hence of split pieces per sequence)
     gives the oracle's result."""
+    ns = 4 if mode in ("window", "fold_sinks") else 0
+    mode = "fold" if mode == "fold_sinks" else mode
     s = Setup(batch=3, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
-              ctx=[5000, 130, 2047], mode=mode, window=1000, n_sink=4 if mode == "window" else 0,
+              ctx=[5000, 130, 2047], mode=mode, window=1000, n_sink=ns,
               alpha=2.0, far_mix=0.5, num_ctas=num_ctas, seed=3)
     compare(s.run(), s.oracle(), "bf16", f"{mode} ctas={num_ctas}")
     s.close()
@@ -272,6 +285,37 @@ def test_fold_without_far_memory_equals_window():
     assert equal_up_to_one_rounding(fold.run(), win.run())
     fold.close()
     win.close()
+
+
+def test_fold_sinks_reduce_to_window_with_sinks():
+    """FOLD with sinks is window attention with the same sinks when lambda = 0,
+    and when the sinks reach the window (no far memory) at any lambda."""
+    kw = dict(batch=2, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=[3000, 700], seed=16)
+    for W, ns, lam in ((512, 4, 0.0), (512, 100, 0.0), (600, 2400, 0.7)):
+        fold = Setup(mode="fold", window=W, n_sink=ns, alpha=2.0, far_mix=lam, **kw)
+        win = Setup(mode="window", window=W, n_sink=ns, **kw)
+        fo, wo = fold.run(), win.run()
+        diff = (fo.float() - wo.float()).abs().max().item()
+        assert equal_up_to_one_rounding(fo, wo), (W, ns, lam, diff)
+        compare(fo, fold.oracle(), "bf16", f"fold W={W} sinks={ns} lambda={lam}")
+        fold.close()
+        win.close()
+
+
+def test_fold_sinks_differ_from_fold():
+    """The sinks move keys from the far memory into the local softmax: the
+    output changes, and each one matches its own oracle."""
+    kw = dict(batch=1, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=[4000], seed=17, mode="fold", window=256, alpha=2.0, far_mix=0.5)
+    a = Setup(n_sink=0, **kw)
+    b = Setup(n_sink=16, **kw)
+    oa, ob = a.run(), b.run()
+    compare(oa, a.oracle(), "bf16", "fold")
+    compare(ob, b.oracle(), "bf16", "fold sinks")
+    assert (oa.float() - ob.float()).abs().max().item() > 1e-3
+    a.close()
+    b.close()
 
 
 def test_sharp_slope_zero_equals_full():

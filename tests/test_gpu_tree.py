@@ -42,6 +42,7 @@ def _setup(shape, dtype, mode, kw, L0, seed=19, **extra):
 
 MODES = [("full", {}), ("window", dict(window=300, n_sink=4)),
          ("fold", dict(window=200, alpha=2.0, far_mix=0.5)),
+         ("fold_sinks", dict(window=200, n_sink=4, alpha=2.0, far_mix=0.5)),
          ("sharp", dict(scale_slope=0.05, scale_ref=256))]
 
 
@@ -52,7 +53,7 @@ MODES = [("full", {}), ("window", dict(window=300, n_sink=4)),
                          ids=["r32", "r8", "r4", "r2", "r4f32", "r8f32"])
 def test_tree_parity(mode, kw, shape, dtype):
     L0 = [2500, 40, 777]
-    s = _setup(shape, dtype, mode, kw, L0)
+    s = _setup(shape, dtype, mode.split("_")[0], kw, L0)
     masks = random_tree_masks(len(L0), shape[2], 5)
     tm = torch.tensor(masks.view(np.int64), device=s.dev)
     out = s.run(tree_mask=tm)
@@ -62,7 +63,7 @@ def test_tree_parity(mode, kw, shape, dtype):
     for t in range(shape[2]):
         g = B.draft_attn_debug_gather(s.da.plan, s.q_pos, s.ctx_lens, s.block_table, 0, t,
                                       capacity=L0[0] + shape[2] + 8, tree_mask=tm)
-        want = orc.selection_list(mode, L0[0] + shape[2], int(s.q_pos[0, t]), s.prm, bt[0], 64,
+        want = orc.selection_list(s.prm.mode, L0[0] + shape[2], int(s.q_pos[0, t]), s.prm, bt[0], 64,
                                   tree_mask=int(masks[0, t]))
         assert g["count"] == want["position"].size
         for k in ("position", "phys_slot", "key_rope_pos", "q_rope_pos", "segment"):
@@ -74,7 +75,7 @@ def test_tree_parity(mode, kw, shape, dtype):
 
 @pytest.mark.parametrize("mode,kw", MODES, ids=[m for m, _ in MODES])
 def test_all_ones_mask_is_no_mask(mode, kw):
-    s = _setup((32, 8, 8), "bf16", mode, kw, [3000, 100])
+    s = _setup((32, 8, 8), "bf16", mode.split("_")[0], kw, [3000, 100])
     ones = torch.full((2, 8), -1, dtype=torch.int64, device=s.dev)
     a = s.run(tree_mask=ones).clone()
     b = s.run()
