@@ -58,6 +58,15 @@ silent (all listed again in the design notes):
    slot position.  A query sees the mode's selection with the tree keys
    restricted to those whose bit i is set in its mask (its ancestors and
    itself); SharpDraft's |S| counts the keys the query actually sees.
+10. FP8 side cache (the FOLD page puts the side cache's size at up to 6 GiB
+   and fixes no format; this is the library's option for shrinking it): the
+   side cache may hold the unrotated keys as FP8 E4M3 codes of k_raw / s, s a
+   positive per-tensor scale.  The quotient is formed in IEEE float32 (the
+   precision the kernel decides the code in), then rounded to the nearest
+   E4M3 value, ties to the even code, magnitudes at or above 448 saturating
+   to 448.  Far keys are then code value * s.  E4M3 (the OCP 8-bit floating
+   point format): 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0 is
+   subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinities.
 
 Arithmetic: float64 throughout (numpy).  Softmax is exp(s - max) / sum.
 """
@@ -90,6 +99,7 @@ class Params:
     rope_theta: float = 10000.0
     softmax_scale: float = 0.0  # 0 => 1/sqrt(d)
     n_tree: int = 0           # draft-tree tokens at the end of the context (reading 9)
+    side_fp8_scale: float = 0.0  # > 0: FOLD side cache as E4M3 codes of k / s (reading 10)
     extra: dict = field(default_factory=dict)
 
 
@@ -300,7 +310,10 @@ def attend_group(q_rows, p: int, k_raw, v, L: int, prm: Params,
     # position, logits sharpened by alpha, softmax normalised on its own.
     if far.size:
         pf = fold_far_position(L, prm.window)
-        f_far = prm.alpha * c * _logits(q_rot, _take(k_raw, far), pf, theta, chunk)
+        k_far = _take(k_raw, far)
+        if prm.side_fp8_scale > 0:
+            k_far = side_fp8_keys(k_far, prm.side_fp8_scale)
+        f_far = prm.alpha * c * _logits(q_rot, k_far, pf, theta, chunk)
         w_far = _softmax(f_far)
         o_far = _weighted_sum(w_far, _take(v, far), chunk)
         lam = prm.far_mix
@@ -358,6 +371,60 @@ def append_rotated_keys(k_new, pos, theta: float) -> np.ndarray:
     k = np.asarray(k_new, dtype=np.float64)
     pos = np.asarray(pos, dtype=np.int64)
     return rope(k, pos[..., None], theta)
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 side cache (reading 10)
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code: int) -> float:
+    """The value of one E4M3 code (0..255) from the format's fields."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 15 and m == 7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Codes of float32 values: nearest E4M3 value, ties to the even code,
+    |x| >= 448 saturating to 448, the sign kept (so -0 and small negatives that
+    round to zero give 0x80)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    mags = np.array([e4m3_value(c) for c in range(0x7F)])     # codes 0..126, ascending
+    a = np.minimum(np.abs(x), E4M3_MAX).ravel()
+    hi = np.searchsorted(mags, a, side="left")                # first magnitude >= a
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - mags[lo], mags[hi] - a
+    code = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    code = np.where(tie, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(mags[hi] == a, hi, code)                  # exact values
+    sign = np.signbit(x.ravel()).astype(np.int64) << 7
+    return (code.astype(np.int64) | sign).astype(np.uint8).reshape(x.shape)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    table = np.array([e4m3_value(c) for c in range(256)])
+    return table[np.asarray(codes, dtype=np.int64)]
+
+
+def side_fp8_codes(k_raw, scale: float) -> np.ndarray:
+    """The side cache's bytes for un-rotated keys k_raw: E4M3 codes of the
+    float32 quotient k_raw / scale."""
+    q = np.asarray(k_raw, dtype=np.float32) / np.float32(scale)
+    return e4m3_encode(q)
+
+
+def side_fp8_keys(k_raw, scale: float) -> np.ndarray:
+    """Far keys as the FP8 side cache gives them back: code value * scale."""
+    return e4m3_decode(side_fp8_codes(k_raw, scale)) * np.float64(np.float32(scale))
 
 
 def round_to_bf16(x) -> np.ndarray:

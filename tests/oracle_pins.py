@@ -42,9 +42,29 @@ def bf_member(mode, j, L, W, n_sink):
     return "loc" if (j >= L - W or j < n_sink) else "far"
 
 
+def bf_e4m3(x):
+    """Nearest E4M3 value of a Python float by its binade: spacing 2^(E-3) in
+    [2^E, 2^(E+1)), E >= -6 (2^-9 in the subnormal range), Python's round()
+    (half to even on the multiple of the spacing, which is the code's last
+    mantissa bit), magnitudes saturating at 448."""
+    sign = math.copysign(1.0, x)
+    a = min(abs(x), 448.0)
+    if a == 0.0:
+        return sign * 0.0
+    _, e = math.frexp(a)                 # a in [2^(e-1), 2^e)
+    spacing = 2.0 ** (max(e - 1, -6) - 3)
+    return sign * min(round(a / spacing) * spacing, 448.0)
+
+
+def bf_side_fp8(k, s):
+    """Far key as an FP8 side cache with scale s returns it."""
+    return [bf_e4m3(float(np.float32(x) / np.float32(s))) * float(np.float32(s)) for x in k]
+
+
 def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
-                  beta=0.0, n_ref=4096, theta=1e4, n_tree=0, tree_mask=None):
-    """One query row by brute force: per-key loops, math.exp, Python floats."""
+                  beta=0.0, n_ref=4096, theta=1e4, n_tree=0, tree_mask=None, far_key=None):
+    """One query row by brute force: per-key loops, math.exp, Python floats.
+    far_key optionally maps a raw key to the key the far memory sees."""
     d = len(q)
     c = 1.0 / math.sqrt(d)
     qr = bf_rope(q, p, theta)
@@ -61,12 +81,12 @@ def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
     if mode == "sharp" and segs["loc"]:
         gamma = max(1.0, 1.0 + beta * math.log(len(segs["loc"]) / n_ref))
 
-    def seg_out(js, key_pos, mult):
+    def seg_out(js, key_pos, mult, kmap=None):
         if not js:
             return [0.0] * d, []
         logits = []
         for j in js:
-            kr = bf_rope(K[j], key_pos(j), theta)
+            kr = bf_rope(kmap(K[j]) if kmap else K[j], key_pos(j), theta)
             logits.append(mult * c * sum(a * b for a, b in zip(qr, kr)))
         mx = max(logits)
         e = [math.exp(s - mx) for s in logits]
@@ -79,7 +99,7 @@ def bf_attend_row(mode, q, p, K, V, L, W=0, n_sink=0, alpha=1.0, lam=0.0,
     if mode != "fold":
         return o_loc, w_loc, []
     pf = L - W - 1
-    o_far, w_far = seg_out(segs["far"], lambda j: pf, alpha)
+    o_far, w_far = seg_out(segs["far"], lambda j: pf, alpha, far_key)
     lam_eff = lam if segs["far"] else 0.0
     o = [(1 - lam_eff) * a + lam_eff * b for a, b in zip(o_loc, o_far)]
     return o, [(1 - lam_eff) * w for w in w_loc], [lam_eff * w for w in w_far]
@@ -142,6 +162,8 @@ def check_brute_force(orc):
         dict(mode="fold", L=9, W=12, alpha=2.0, lam=0.5),
         dict(mode="fold", L=45, W=12, n_sink=4, alpha=2.0, lam=0.5),
         dict(mode="fold", L=15, W=12, n_sink=4, alpha=1.5, lam=0.5),
+        dict(mode="fold", L=45, W=12, alpha=2.0, lam=0.5, fp8=0.05),
+        dict(mode="fold", L=40, W=9, n_sink=3, alpha=2.0, lam=0.5, fp8=0.004),
         dict(mode="sharp", L=60, beta=0.4, n_ref=8),
         dict(mode="sharp", L=5, beta=0.4, n_ref=8),
     ]
@@ -154,12 +176,14 @@ def check_brute_force(orc):
         prm = orc.Params(mode=cfg["mode"], window=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
                          alpha=cfg.get("alpha", 1.0), far_mix=cfg.get("lam", 0.0),
                          scale_slope=cfg.get("beta", 0.0), scale_ref=cfg.get("n_ref", 4096),
-                         rope_theta=1e4)
+                         rope_theta=1e4, side_fp8_scale=cfg.get("fp8", 0.0))
         got = orc.attend_group(q[None], p, K, V, L, prm)[0]
+        s8 = cfg.get("fp8", 0.0)
         want, _, _ = bf_attend_row(cfg["mode"], list(q), p, K.tolist(), V.tolist(), L,
                                    W=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
                                    alpha=cfg.get("alpha", 1.0), lam=cfg.get("lam", 0.0),
-                                   beta=cfg.get("beta", 0.0), n_ref=cfg.get("n_ref", 4096))
+                                   beta=cfg.get("beta", 0.0), n_ref=cfg.get("n_ref", 4096),
+                                   far_key=(lambda k: bf_side_fp8(k, s8)) if s8 else None)
         assert np.max(np.abs(got - np.array(want))) < 1e-12, cfg
 
 
@@ -375,7 +399,44 @@ def check_nope(orc):
     assert np.allclose(got, want, atol=1e-12)
 
 
-ALL_CHECKS = [check_tree_masks, check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
+def check_e4m3(orc):
+    import torch
+    # every code's value against torch's float8_e4m3fn, and a few closed values
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    for c, v in ((0x00, 0.0), (0x01, 2.0 ** -9), (0x08, 2.0 ** -6), (0x38, 1.0), (0x7E, 448.0),
+                 (0xFE, -448.0), (0x3C, 1.5)):
+        assert orc.e4m3_decode([c])[0] == v, hex(c)
+    # encoding against the pure-Python binade rounding: ties, subnormals,
+    # saturation, signed zeros, and a log-uniform spread over the range
+    rng = np.random.default_rng(21)
+    mags = np.exp2(rng.uniform(-12, 9.5, 4000))
+    xs = (mags * rng.choice([-1.0, 1.0], 4000)).astype(np.float32)
+    special = np.float32([0.0, -0.0, 1.0625, 1.1875, -1.0625, 3 * 2.0 ** -10, 2.0 ** -10,
+                          -(2.0 ** -11), 447.0, 448.0, 463.0, 464.0, 470.0, 1e6, -1e6,
+                          2.0 ** -6 - 2.0 ** -11, 15.5, 17.0])
+    xs = np.concatenate([xs, special])
+    enc = orc.e4m3_encode(xs)
+    dec = orc.e4m3_decode(enc)
+    for x, c, v in zip(xs, enc, dec):
+        w = bf_e4m3(float(x))
+        assert v == w and math.copysign(1.0, v) == math.copysign(1.0, w), (float(x), int(c), v, w)
+    # torch rounds the same way inside the saturation limit
+    m = np.abs(xs) < 464
+    t = torch.from_numpy(xs[m]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(enc[m], t)
+    # the side cache's keys: the float32 quotient's code times the scale
+    k = rng.standard_normal(64)
+    for s in (0.05, 1.0, 0.003):
+        want = [bf_e4m3(float(np.float32(x) / np.float32(s))) * float(np.float32(s)) for x in k]
+        assert np.array_equal(orc.side_fp8_keys(k, s), np.array(want)), s
+
+
+ALL_CHECKS = [check_e4m3, check_tree_masks, check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
               check_brute_force, check_closed_forms, check_weights_sum,
               check_mode_equivalences, check_fold_shared_position, check_gqa,
               check_page_slot]

@@ -45,6 +45,33 @@ def _fold_sinks_ignored(mode, L, W=0, n_sink=0):
 
 
 _select_keys = orc.select_keys
+_e4m3_encode = orc.e4m3_encode
+
+
+def _e4m3_ties_away(x):
+    # an exact midpoint goes to the larger magnitude instead of the even code
+    codes = _e4m3_encode(x)
+    a = np.abs(np.asarray(x, dtype=np.float32).astype(np.float64))
+    mag = codes & 0x7F
+    v = np.abs(orc.e4m3_decode(mag))
+    nxt = np.abs(orc.e4m3_decode(np.minimum(mag + 1, 0x7E)))
+    mid = (a > v) & (a - v == nxt - a)
+    return np.where(mid, codes + 1, codes).astype(np.uint8)
+
+
+def _e4m3_subnormals_flushed(x):
+    codes = _e4m3_encode(x)
+    return np.where((codes & 0x78) == 0, codes & 0x80, codes).astype(np.uint8)
+
+
+def _e4m3_no_saturation(x):
+    codes = _e4m3_encode(x)
+    big = np.abs(np.asarray(x, dtype=np.float32)) >= 464
+    return np.where(big, codes | 0x7F, codes).astype(np.uint8)   # overflow to NaN
+
+
+def _side_fp8_unscaled(k_raw, scale):
+    return orc.e4m3_decode(orc.side_fp8_codes(k_raw, scale))
 
 MUTATIONS = {
     "rope_sign": ("rope", _rope_sign),
@@ -58,6 +85,10 @@ MUTATIONS = {
         np.asarray(pos, dtype=np.int64) if m is None or nt <= 0 else np.asarray(
             [j for j in pos if j < L - nt or (int(m) >> int(j - (L - nt) + 1)) & 1], dtype=np.int64))),
     "fold_sinks_also_far": ("select_keys", _fold_sinks_also_far),
+    "e4m3_ties_away": ("e4m3_encode", _e4m3_ties_away),
+    "e4m3_subnormals_flushed": ("e4m3_encode", _e4m3_subnormals_flushed),
+    "e4m3_no_saturation": ("e4m3_encode", _e4m3_no_saturation),
+    "side_fp8_scale_dropped": ("side_fp8_keys", _side_fp8_unscaled),
     "fold_sinks_ignored": ("select_keys", _fold_sinks_ignored),
     "far_position_off_by_one": ("fold_far_position", lambda L, W: L - W),
     "gamma_no_clamp": ("sharp_gamma", lambda n, b, r: 1.0 + b * math.log(max(n, 1) / r)),
