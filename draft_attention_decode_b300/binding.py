@@ -69,7 +69,9 @@ class da_params(ctypes.Structure):
         ("stages", ctypes.c_int32),
         ("tree_size", ctypes.c_int32),
         ("k_ring_pages", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 1),
+        ("side_fp8", ctypes.c_int32),
+        ("side_scale", ctypes.c_float),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -144,7 +146,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
                 page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0,
-                k_ring_pages=0) -> da_params:
+                k_ring_pages=0, side_fp8=0, side_scale=0.0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -160,6 +162,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.stages = int(stages)
     p.tree_size = int(tree_size)
     p.k_ring_pages = int(k_ring_pages)
+    p.side_fp8, p.side_scale = int(side_fp8), float(side_scale)
     return p
 
 

@@ -27,7 +27,7 @@ struct da_plan_s {
 
 namespace {
 
-constexpr int kAbiVersion = 100;
+constexpr int kAbiVersion = 101;
 
 struct DeviceGuard {
   int prev = -1;
@@ -60,15 +60,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // head_dim elements; box = 64 rows x 128 bytes with the 128-byte swizzle.
 // pages: the cache array's page count (num_pages, or batch * k_ring_pages for
 // FOLD's ring of rotated keys).
-bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p, int64_t pages) {
+// fp8: the array holds one byte per element (FOLD's E4M3 side cache).
+bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p, int64_t pages,
+                      bool fp8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const int es = p.dtype == DA_DTYPE_BF16 ? 2 : 4;
+  const int es = fp8 ? 1 : p.dtype == DA_DTYPE_BF16 ? 2 : 4;
   cuuint64_t gdim[2] = {(cuuint64_t)p.head_dim, (cuuint64_t)pages * p.num_kv_heads * da::kPage};
   cuuint64_t gstride[1] = {(cuuint64_t)p.head_dim * es};
   cuuint32_t box[2] = {(cuuint32_t)(da::kSwizzleRow / es), (cuuint32_t)da::kPage};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, p.dtype == DA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                  : p.dtype == DA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   2, const_cast<void*>(base), gdim, gstride, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -96,6 +99,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->n_tree = p.tree_size;
   a->alpha = p.alpha;
   a->far_mix = p.far_mix;
+  a->far_kscale = p.side_fp8 == 1 ? p.side_scale : 1.f;
   a->beta = p.scale_slope;
   a->n_ref = p.scale_ref;
   a->scale_log2 = pl->scale_log2;
@@ -158,7 +162,14 @@ int draft_attn_check_params(const da_params* p) {
   if (p->tree_size > 0 && (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) &&
       p->tree_size > p->window)
     return DA_ERR_INVALID_ARG;
-  if (p->reserved[0] != 0) return DA_ERR_INVALID_ARG;
+  if (p->reserved[0] != 0 || p->reserved[1] != 0) return DA_ERR_INVALID_ARG;
+  if (p->side_fp8 != 0 && p->side_fp8 != 1) return DA_ERR_INVALID_ARG;
+  if (p->side_fp8 == 1) {
+    if (p->mode != DA_MODE_FOLD) return DA_ERR_INVALID_ARG;
+    if (!(p->side_scale > 0.f) || !std::isfinite(p->side_scale)) return DA_ERR_INVALID_ARG;
+  } else if (p->side_scale != 0.f) {
+    return DA_ERR_INVALID_ARG;
+  }
   if (p->k_ring_pages != 0) {   // FOLD's rotated K kept for the local window only
     if (p->mode != DA_MODE_FOLD || p->window < 1) return DA_ERR_INVALID_ARG;
     if (p->k_ring_pages < (p->window + da::kPage - 1) / da::kPage + 1) return DA_ERR_INVALID_ARG;
@@ -184,6 +195,10 @@ int draft_attn_check_params(const da_params* p) {
   if (rows > 32) return DA_ERR_UNSUPPORTED;
   if (rows > 8 && (p->dtype != DA_DTYPE_BF16 || p->engine == 1)) return DA_ERR_UNSUPPORTED;
   if (p->engine == 2 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
+  // the FP8 side cache is read by the CUDA-core engine with 128-byte key rows
+  if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || p->head_dim != 128 || rows > 4 ||
+                           p->engine == 2))
+    return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -206,7 +221,8 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
   pl->num_sms = sms;
   pl->rows = (params->num_q_heads / params->num_kv_heads) * params->n_q;
   if (!da::choose_kernel(params->dtype, params->head_dim, pl->rows, params->batch, params->mode,
-                         params->engine, params->stages, max_smem, &pl->choice)) {
+                         params->engine, params->stages, max_smem, params->side_fp8 == 1,
+                         &pl->choice)) {
     delete pl;
     return DA_ERR_UNSUPPORTED;
   }
@@ -282,6 +298,8 @@ int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, con
   a.max_pages = pl->p.max_pages_per_seq;
   a.num_pages = pl->p.num_pages;
   a.k_ring = pl->p.k_ring_pages;
+  a.side_f8 = pl->p.side_fp8;
+  a.side_scale = pl->p.side_scale;
   for (int i = 0; i < 64; ++i) a.turn_freq[i] = pl->turn_freq[i];
   cudaError_t e = da::launch_append(pl->p.dtype, pl->p.head_dim, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
@@ -326,7 +344,8 @@ int prepare_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t
       !encode_cache_map(&r->mv, v_cache, pl->p, pl->p.num_pages))
     return DA_ERR_CUDA;
   if (fold) {
-    if (!encode_cache_map(&r->ms, k_side, pl->p, pl->p.num_pages)) return DA_ERR_CUDA;
+    if (!encode_cache_map(&r->ms, k_side, pl->p, pl->p.num_pages, pl->p.side_fp8 == 1))
+      return DA_ERR_CUDA;
   } else {
     r->ms = r->mk;
   }

@@ -7,8 +7,17 @@ namespace da {
 // KV append + RoPE.  One warp per (b, token, kv head); lane f handles the
 // rotate-half pairs (f, f + d/2), f = lane, lane + 32.  Writes the rotated key
 // to the K cache, the raw key to the FOLD side cache ("FOLD", review: the
-// unrotated side cache) and the value to the V cache.
+// unrotated side cache) and the value to the V cache.  With side_f8 the side
+// cache takes one byte per element: the E4M3 code of the float32 quotient
+// k / side_scale (IEEE division), rounded to nearest even and saturated to
+// the largest finite code by cvt's satfinite mode.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;   // lo's code in the low byte
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
   // Wait for the predecessor first, then let the dependent start: a
@@ -52,7 +61,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   const int64_t kpage = a.k_ring > 0 ? (int64_t)b * a.k_ring + pg % a.k_ring : phys;
   T* kc = static_cast<T*>(a.k_cache) + ((kpage * a.H_kv + h) * kPage + (pos - pg * kPage)) * D;
   T* vc = static_cast<T*>(a.v_cache) + dst;
-  T* ks = a.k_side ? static_cast<T*>(a.k_side) + dst : nullptr;
+  T* ks = (a.k_side && !a.side_f8) ? static_cast<T*>(a.k_side) + dst : nullptr;
+  uint8_t* ks8 = (a.k_side && a.side_f8) ? static_cast<uint8_t*>(a.k_side) + dst : nullptr;
 #pragma unroll
   for (int u = 0; u < D / 64; ++u) {
     const int f = lane + 32 * u;
@@ -64,6 +74,11 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     if (ks) {
       ks[f] = kx[u];
       ks[f + D / 2] = ky[u];
+    }
+    if (ks8) {
+      const uint16_t c2 = e4m3x2(__fdiv_rn(x, a.side_scale), __fdiv_rn(y, a.side_scale));
+      ks8[f] = (uint8_t)(c2 & 0xffu);
+      ks8[f + D / 2] = (uint8_t)(c2 >> 8);
     }
     vc[f] = vx[u];
     vc[f + D / 2] = vy[u];

@@ -50,6 +50,7 @@ struct DecodeArgs {
   int32_t mode, W, n_sink;
   int32_t n_tree;       // tree tokens at the end of each context
   float alpha, far_mix, beta;
+  float far_kscale;     // far keys as stored times this are the keys (FP8 side cache scale, else 1)
   int32_t n_ref;
   float scale_log2;     // softmax scale * log2(e)
   int32_t n_cta;

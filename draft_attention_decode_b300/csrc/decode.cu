@@ -7,7 +7,7 @@
 namespace da {
 
 bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
-                   int max_smem, Choice* c) {
+                   int max_smem, bool side_f8, Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
   // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
   // from 5 on, QK^T and PV are dense enough for an n8 tensor-core tile
@@ -16,6 +16,10 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
   if (engine_hint == 1) mma = false;
   if (engine_hint == 2) mma = true;
   c->pingpong = false;
+  c->side_f8 = side_f8;
+  // The FP8 side cache (FOLD) is read by the turn-taking CUDA-core engine only.
+  if (side_f8 && (mma || dtype != DA_DTYPE_BF16 || d != 128 || rows > 4 || mode != DA_MODE_FOLD))
+    return false;
   if (mma) {
     if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
     c->engine = DA_ENGINE_MMA;
@@ -55,6 +59,14 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
     DA_MMA(128, 1, true, 8) DA_MMA(128, 2, true, 16) DA_MMA(128, 2, false, 32)
     DA_MMA(64, 1, true, 8) DA_MMA(64, 2, true, 16) DA_MMA(64, 2, false, 32)
 #undef DA_MMA
+    return cudaErrorInvalidValue;
+  }
+  if (c.side_f8) {
+    if (dtype != DA_DTYPE_BF16 || d != 128 || !c.pingpong) return cudaErrorInvalidValue;
+#define DA_CORE_F8(RK) \
+  if (c.rk == RK) return f(decode_kernel<bf, 128, CoreEngine<bf, 128, RK, true, true>, kVariantCore, RK>);
+    DA_CORE_F8(1) DA_CORE_F8(2) DA_CORE_F8(4)
+#undef DA_CORE_F8
     return cudaErrorInvalidValue;
   }
 #define DA_CORE(T, D, RK)                                                                     \

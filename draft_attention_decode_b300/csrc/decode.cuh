@@ -49,7 +49,8 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
     s.tmask[row] = m;
     float mult = a.scale_log2;
     if (far) {
-      mult *= a.alpha;                       // "FOLD", abstract: concentration factor
+      // "FOLD", abstract: concentration factor; an FP8 side cache's scale
+      mult *= a.alpha * a.far_kscale;
     } else if (a.mode == DA_MODE_SHARP) {    // "SharpDraft", Abstract: query scaling
       int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
       if (a.tree_mask && a.n_tree > 0) {
@@ -180,6 +181,24 @@ struct Chunk<float> {
   }
 };
 
+// Four E4M3 codes (bytes of w, lowest first) as floats: two codes at a time
+// to an f16 pair (every E4M3 value is an f16 value), then each f16 to f32.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float& f0, float& f1, float& f2,
+                                              float& f3) {
+  asm("{\n\t.reg .b16 a, b, c0, c1, c2, c3;\n\t.reg .b32 h0, h1;\n\t"
+      "mov.b32 {a, b}, %4;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h1, b;\n\t"
+      "mov.b32 {c0, c1}, h0;\n\t"
+      "mov.b32 {c2, c3}, h1;\n\t"
+      "cvt.f32.f16 %0, c0;\n\t"
+      "cvt.f32.f16 %1, c1;\n\t"
+      "cvt.f32.f16 %2, c2;\n\t"
+      "cvt.f32.f16 %3, c3;\n\t}"
+      : "=f"(f0), "=f"(f1), "=f"(f2), "=f"(f3)
+      : "r"(w));
+}
+
 // DPL consecutive elements (the PV slice of one lane) as floats.
 template <typename T, int DPL>
 __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
@@ -219,13 +238,19 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 // (only when a score exceeds it by more than 2^8): the result is exact for
 // any reference value, and the accumulators are rescaled only a handful of
 // times.
+// With F8 (FOLD with an FP8 side cache, head_dim 128) a far piece's keys are
+// 128-byte rows of E4M3 codes: lane ds reads its 16 dimensions 16 ds .. 16 ds
+// + 15 as one 16-byte chunk (row-rotated by the swizzle, so the eight lanes of
+// a key cover all 32 banks), and the piece's queries are laid out in that
+// order (begin_far).
 // ---------------------------------------------------------------------------
-template <typename T, int D, int RK, bool PINGPONG>
+template <typename T, int D, int RK, bool PINGPONG, bool F8 = false>
 struct CoreEngine {
   static constexpr int NCW = kConsumerWarps;
   static constexpr int NCT = NCW * 32;
   static constexpr bool kPairs = true;         // takes two pages per step
   static constexpr bool kPingPong = PINGPONG;  // the two warp groups alternate steps
+  static constexpr bool kSideF8 = F8;          // far keys as E4M3 codes
   static constexpr int GW = PINGPONG ? NCW / 2 : NCW;   // warps sharing a step
   static constexpr int LPK = 8;                // lanes per key
   static constexpr int KG = 32 / LPK;          // key groups per pass
@@ -238,6 +263,7 @@ struct CoreEngine {
   static constexpr float kLazy = 8.f;          // log2 headroom before a rescale
   static_assert(RK == 1 || RK == 2 || RK == 4, "rows");
   static_assert(NCH >= 1 && (NCH & (NCH - 1)) == 0, "chunks");
+  static_assert(!F8 || (ES == 2 && D == 128 && PINGPONG), "FP8 side cache: bf16, d 128");
 
   float2 q2[RK][DQ / 2];
   float2 o2[RK][DQ / 2];
@@ -245,6 +271,7 @@ struct CoreEngine {
   // Swizzled byte offsets of the lane's chunks on passes 0 and 1; pass ps adds
   // 1024 (ps / 2) bytes: its row is 8 further on and has the same swizzle.
   uint32_t off[2][NCH];
+  uint32_t off8[2];      // F8: the lane's E4M3 chunk on passes 0 and 1
   int lane, warp, kg, ds;
   static_assert(KG == 4, "rows of passes ps and ps + 2 differ by 8");
   __device__ __forceinline__ uint32_t off_of(int ps, int i) const {
@@ -267,6 +294,13 @@ struct CoreEngine {
 #pragma unroll
       for (int i = 0; i < NCH; ++i)
         off[it][i] = swz_addr(0u, (warp & (GW - 1)) * KPW + kg + KG * it, chunk_of(i) * 16);
+    if constexpr (F8) {
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int row = (warp & (GW - 1)) * KPW + kg + KG * it;
+        off8[it] = swz_addr(0u, row, ds * 16);
+      }
+    }
   }
 
   // Step u (a pair or a single page) belongs to warp group u mod 2.
@@ -296,9 +330,28 @@ struct CoreEngine {
     reset();
   }
 
+  // F8: a far piece takes its queries in the order of the lane's E4M3 chunk
+  // (slot i, pair e: dimensions 16 ds + 8 i + 2 e, + 1).
+  __device__ __forceinline__ void begin_far(const Smem& s, bool far) {
+    if (!far) {
+      begin(s);
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < NCH; ++i)
+#pragma unroll
+      for (int r = 0; r < RK; ++r)
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          const int d0 = ds * 16 + i * EPC + 2 * e;
+          q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0], s.q[r * D + d0 + 1]);
+        }
+    reset();
+  }
+
   // NP consecutive pages of one piece: K/V stage addresses, valid key ranges
-  // [lo, hi) inside each page and tree offsets.
-  template <int NP>
+  // [lo, hi) inside each page and tree offsets.  FK: the keys are E4M3 rows.
+  template <int NP, bool FK = false>
   __device__ __forceinline__ void pages(const Smem& s, const uint32_t (&kb)[NP],
                                         const uint32_t (&vb)[NP], const int (&lo)[NP],
                                         const int (&hi)[NP], const int (&toff)[NP]) {
@@ -321,16 +374,36 @@ struct CoreEngine {
       for (int u = 0; u < NA; ++u)
 #pragma unroll
         for (int r = 0; r < RK; ++r) acc[u][r] = make_float2(0.f, 0.f);
+      if constexpr (FK) {
+        static_assert(NCH * EPC == 16, "one E4M3 chunk per lane and key");
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(kb[pg] + off8[ps & 1] + (uint32_t)(ps >> 1) * (8 * kSwizzleRow)));
+        float f[16];
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        float f[EPC];
-        Chunk<T>::load(kb[pg] + off_of(ps, i), f);
+        for (int j = 0; j < 4; ++j) e4m3x4_to_f32(w[j], f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
 #pragma unroll
-        for (int e = 0; e < EPC / 2; ++e) {
-          const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
+        for (int i = 0; i < NCH; ++i)
 #pragma unroll
-          for (int r = 0; r < RK; ++r)
-            acc[e % NA][r] = ffma2(q2[r][i * (EPC / 2) + e], kk, acc[e % NA][r]);
+          for (int e = 0; e < EPC / 2; ++e) {
+            const float2 kk = make_float2(f[i * EPC + 2 * e], f[i * EPC + 2 * e + 1]);
+#pragma unroll
+            for (int r = 0; r < RK; ++r)
+              acc[e % NA][r] = ffma2(q2[r][i * (EPC / 2) + e], kk, acc[e % NA][r]);
+          }
+      } else {
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          float f[EPC];
+          Chunk<T>::load(kb[pg] + off_of(ps, i), f);
+#pragma unroll
+          for (int e = 0; e < EPC / 2; ++e) {
+            const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
+#pragma unroll
+            for (int r = 0; r < RK; ++r)
+              acc[e % NA][r] = ffma2(q2[r][i * (EPC / 2) + e], kk, acc[e % NA][r]);
+          }
         }
       }
       float v[RK];
@@ -405,11 +478,12 @@ struct CoreEngine {
     }
   }
 
+  template <bool FK = false>
   __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi,
                                        int toff) {
     const uint32_t kb[1] = {kbase}, vb[1] = {vbase};
     const int l[1] = {lo}, h[1] = {hi}, o[1] = {toff};
-    pages<1>(s, kb, vb, l, h, o);
+    pages<1, FK>(s, kb, vb, l, h, o);
   }
 
   // Sum the key groups, merge the consumer warps, write the piece's partial.
@@ -477,6 +551,7 @@ template <typename T, int D, int RK>
 struct CoreEngineWide {
   static constexpr bool kPairs = false;
   static constexpr bool kPingPong = false;
+  static constexpr bool kSideF8 = false;
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int ES = sizeof(T);
@@ -700,6 +775,7 @@ template <int D, int NT, bool SPLIT_PAGES>
 struct MmaEngine {
   static constexpr bool kPairs = false;
   static constexpr bool kPingPong = false;
+  static constexpr bool kSideF8 = false;
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
@@ -1112,7 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   if (warp >= NCW) {
     regs_dec<kProducerRegs>();
-    if (warp == NCW) producer<ES, NCB>(a, s, L, xs, xe, &mk, &mv, &ms);
+    if (warp == NCW) producer<ES, NCB, Engine::kSideF8>(a, s, L, xs, xe, &mk, &mv, &ms);
     return;
   }
   regs_inc<kConsumerRegs>();
@@ -1122,8 +1198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
     const Where w = locate(s, a.B, a.H_kv, xs);
-    prep_queries<T, D, RK, NCT>(a, s, piece_seq(a.mode, w.b, w.h, a.H_kv, w.r));
-    eng.begin(s);
+    const int32_t seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
+    prep_queries<T, D, RK, NCT>(a, s, seq);
+    if constexpr (Engine::kSideF8) eng.begin_far(s, (seq & 1) == 0); else eng.begin(s);
   }
   const uint32_t base = smem_u32(s.stage);
   uint32_t n = 0, pages = 0;
@@ -1135,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PageInfo inf = s.info[st];
     if ((inf.flags & kFirst) && x != xs) {
       prep_queries<T, D, RK, NCT>(a, s, inf.seq);
-      eng.begin(s);
+      if constexpr (Engine::kSideF8) eng.begin_far(s, (inf.seq & 1) == 0); else eng.begin(s);
     }
     const uint32_t kb0 = base + st * L.stage_bytes;
     const int lo0 = (inf.flags & kValid) ? (inf.lohi & 0xffff) : 0;
@@ -1163,6 +1240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int l2[1] = {lo[1]}, h2[1] = {hi[1]}, t2[1] = {to[1]};
             eng.template pages<1>(s, k1, v1, l1, h1, t1);
             eng.template pages<1>(s, k2, v2, l2, h2, t2);
+          } else if constexpr (Engine::kSideF8) {   // FOLD: seq even = far memory
+            if ((inf.seq & 1) == 0) eng.template pages<2, true>(s, kb, vb, lo, hi, to);
+            else eng.template pages<2>(s, kb, vb, lo, hi, to);
           } else {
             eng.template pages<2>(s, kb, vb, lo, hi, to);
           }
@@ -1178,7 +1258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (taken == 1) {
       const bool mine = Engine::kPingPong ? eng.owns(unit) : eng.owns(n);
-      if (hi0 > lo0 && mine) eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
+      if (hi0 > lo0 && mine) {
+        if constexpr (Engine::kSideF8) {
+          if ((inf.seq & 1) == 0) eng.template page<true>(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
+          else eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
+        } else {
+          eng.page(s, kb0, kb0 + NCB * kBoxBytes, lo0, hi0, to0);
+        }
+      }
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[st]);
     }

@@ -30,6 +30,7 @@ struct Choice {
   int variant;     // kVariantCore or kVariantMma (shared-memory layout)
   int rk;          // rows the kernel instance computes
   bool pingpong;   // CUDA cores, <= 4 rows: the two consumer warp groups take turns
+  bool side_f8;    // FOLD far keys from an FP8 E4M3 side cache
   int stages;      // pipeline depth
   uint32_t smem;   // dynamic shared memory bytes
 };
@@ -38,7 +39,7 @@ struct Choice {
 // 0 automatic, 1 CUDA cores, 2 tensor cores) in `mode`; false when none
 // exists or it does not fit in `max_smem` bytes of shared memory.
 bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
-                   int max_smem, Choice* c);
+                   int max_smem, bool side_f8, Choice* c);
 
 cudaError_t prepare_decode(const Choice& c, int dtype, int d);
 cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,
@@ -56,6 +57,8 @@ struct AppendArgs {
   uint32_t* status;
   int32_t B, n_new, H_kv, max_pages, num_pages;
   int32_t k_ring;   // rotated K of page P of sequence b at b * k_ring + P mod k_ring (0: paged)
+  int32_t side_f8;  // k_side holds E4M3 codes of k / side_scale
+  float side_scale;
   float2 turn_freq[64];
 };
 cudaError_t launch_append(int dtype, int d, const AppendArgs& a, cudaStream_t st);

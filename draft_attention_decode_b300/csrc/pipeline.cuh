@@ -198,8 +198,10 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
 
 // The producer warp: block-table translation and TMA issue for the CTA's
 // stretch [xs, xe) of the page line.  ES = element bytes, NCB = 128-byte
-// column boxes per row (head_dim * ES / 128).
-template <int ES, int NCB>
+// column boxes per row (head_dim * ES / 128).  F8: far keys come from an FP8
+// side cache, one 128-byte box per page (head_dim 128), into the stage's first
+// K box.
+template <int ES, int NCB, bool F8>
 __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
                                 int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
                                 const CUtensorMap* ms) {
@@ -260,14 +262,22 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
           uint8_t* kdst = s.stage + st * L.stage_bytes;
           uint8_t* vdst = kdst + NCB * kBoxBytes;
           if (jflags & kValid) {
-            mbar_arrive_expect_tx(&s.full[st], L.stage_bytes);
             const int32_t y = (jphys * a.H_kv + jh) * kPage;
             const int32_t yk = (jkphys * a.H_kv + jh) * kPage;
-            const CUtensorMap* km = jfar ? ms : mk;
+            if (F8 && jfar) {
+              mbar_arrive_expect_tx(&s.full[st], (NCB + 1) * kBoxBytes);
+              tma_load_2d(kdst, ms, 0, yk, &s.full[st], pol);
 #pragma unroll
-            for (int cb = 0; cb < NCB; ++cb) {
-              tma_load_2d(kdst + cb * kBoxBytes, km, cb * (kSwizzleRow / ES), yk, &s.full[st], pol);
-              tma_load_2d(vdst + cb * kBoxBytes, mv, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+              for (int cb = 0; cb < NCB; ++cb)
+                tma_load_2d(vdst + cb * kBoxBytes, mv, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+            } else {
+              mbar_arrive_expect_tx(&s.full[st], L.stage_bytes);
+              const CUtensorMap* km = jfar ? ms : mk;
+#pragma unroll
+              for (int cb = 0; cb < NCB; ++cb) {
+                tma_load_2d(kdst + cb * kBoxBytes, km, cb * (kSwizzleRow / ES), yk, &s.full[st], pol);
+                tma_load_2d(vdst + cb * kBoxBytes, mv, cb * (kSwizzleRow / ES), y, &s.full[st], pol);
+              }
             }
           } else {
             mbar_arrive(&s.full[st]);

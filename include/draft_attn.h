@@ -43,6 +43,8 @@
  *                [num_pages][num_kv_heads][page_size][head_dim]
  *                k_cache holds keys rotated at their own positions, k_side
  *                the same keys un-rotated (FOLD only), v_cache the values.
+ *                With side_fp8 = 1, k_side holds one byte per element: the
+ *                FP8 E4M3 code of k / side_scale.
  *   block_table  int32 [batch][max_pages_per_seq]; logical page j of sequence
  *                b lives in physical page block_table[b][j].
  *   ctx_lens     int32 [batch]: keys 0 .. ctx_lens[b]-1 are visible.
@@ -144,7 +146,17 @@ typedef struct {
                                 every sequence (batch = params.batch), and one
                                 call must not hold two positions R * 64 apart
                                 (they would share a slot).                       */
-  int32_t reserved[1];       /* must be zero                                       */
+  int32_t side_fp8;          /* FOLD only: 0 = k_side in dtype; 1 = k_side as FP8
+                                E4M3 codes (one byte per element) of the float32
+                                quotient k / side_scale, rounded to nearest, ties
+                                to even, saturating at +-448; the far memory reads
+                                code value * side_scale.  Halves the side cache
+                                against bf16 (the FOLD page gives no format for
+                                it).  Needs bf16, head_dim 128 and at most 4 rows
+                                per KV head on the CUDA-core engine
+                                (DA_ERR_UNSUPPORTED otherwise).                   */
+  float   side_scale;        /* > 0 and finite with side_fp8 = 1, else 0           */
+  int32_t reserved[2];       /* must be zero                                       */
 } da_params;
 
 typedef struct {

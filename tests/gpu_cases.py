@@ -25,7 +25,8 @@ class Setup:
     def __init__(self, *, batch, n_q, num_q_heads, num_kv_heads, head_dim, dtype, ctx,
                  mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0, scale_slope=0.0,
                  scale_ref=4096, rope_theta=1e4, num_ctas=0, seed=0, extra_tokens=0,
-                 spare_pages=3, q_pos=None, fill=True, engine=0, tree_size=0):
+                 spare_pages=3, q_pos=None, fill=True, engine=0, tree_size=0,
+                 side_fp8_scale=0.0):
         self.dev = torch.device("cuda", 0)
         self.dtype = dtype
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -50,16 +51,22 @@ class Setup:
             head_dim=head_dim, num_pages=npg, max_pages_per_seq=bt.shape[1], dtype=dtype,
             mode=mode, window=window, n_sink=n_sink, alpha=alpha, far_mix=far_mix,
             scale_slope=scale_slope, scale_ref=scale_ref, rope_theta=rope_theta,
-            num_ctas=num_ctas, engine=engine, tree_size=tree_size)
+            num_ctas=num_ctas, engine=engine, tree_size=tree_size,
+            side_fp8=1 if side_fp8_scale > 0 else 0, side_scale=side_fp8_scale)
         shape = (npg, num_kv_heads, WL.PAGE, head_dim)
         # NaN-filled so that a read of a slot nobody wrote shows up in the output
         self.k_cache = torch.full(shape, float("nan"), dtype=tdt, device=self.dev)
         self.v_cache = torch.full(shape, float("nan"), dtype=tdt, device=self.dev)
-        self.k_side = (torch.full(shape, float("nan"), dtype=tdt, device=self.dev)
-                       if mode == "fold" else None)
+        if mode == "fold" and side_fp8_scale > 0:   # E4M3 codes; 0x7F is NaN
+            self.k_side = torch.full(shape, 0x7F, dtype=torch.uint8, device=self.dev)
+        elif mode == "fold":
+            self.k_side = torch.full(shape, float("nan"), dtype=tdt, device=self.dev)
+        else:
+            self.k_side = None
         self.prm = orc.Params(mode=mode, window=window, n_sink=n_sink if mode in ("window", "fold") else 0,
                               alpha=alpha, far_mix=far_mix, scale_slope=scale_slope,
-                              scale_ref=scale_ref, rope_theta=rope_theta, n_tree=tree_size)
+                              scale_ref=scale_ref, rope_theta=rope_theta, n_tree=tree_size,
+                              side_fp8_scale=side_fp8_scale)
         if fill:
             for b, c in enumerate(self.ctx):
                 self.append(b, 0, c)

@@ -19,7 +19,7 @@ def test_exports_every_header_symbol():
     assert len(names) >= 10
     for n in names:
         assert hasattr(lib, n), n
-    assert B.draft_attn_version() == 100
+    assert B.draft_attn_version() == 101
 
 
 def test_error_strings():
@@ -56,6 +56,24 @@ def _ok_params(**kw):
     (dict(mode="fold", window=16, alpha=2.0, n_sink=4), 0),       # sinks join the local softmax
     (dict(mode="fold", window=16, alpha=2.0, n_sink=-1), -1),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=4, k_ring_pages=5), -1),
+    # FOLD side cache as FP8 E4M3 codes
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=0.05), 0),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=0.05,
+          k_ring_pages=5, n_sink=0), 0),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=0.0), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1,
+          side_scale=float("inf")), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=2, side_scale=1.0), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_scale=1.0), -1),
+    (dict(mode="window", window=200, side_fp8=1, side_scale=1.0), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
+          head_dim=64), -2),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
+          dtype="fp32"), -2),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
+          num_q_heads=64), -2),                      # 8 rows per KV head
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
+          engine="mma"), -2),
     (dict(mode="sharp", scale_slope=-1.0), -1),
     (dict(mode="sharp", scale_ref=0), -1),
     (dict(rope_theta=0.0), 0),                         # NoPE
@@ -88,9 +106,10 @@ def test_check_params(kw, code):
 
 
 def test_reserved_must_be_zero():
-    p = _ok_params()
-    p.reserved[0] = 1
-    assert B.draft_attn_check_params(p) == -1
+    for i in range(2):
+        p = _ok_params()
+        p.reserved[i] = 1
+        assert B.draft_attn_check_params(p) == -1
 
 
 def test_null_params_and_plan_rejected():
@@ -109,13 +128,13 @@ def test_struct_layout_matches_header(tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "draft_attn.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(da_params),"
-        " offsetof(da_params, softmax_scale), offsetof(da_params, reserved),"
+        " offsetof(da_params, side_scale), offsetof(da_params, reserved),"
         " sizeof(da_plan_info), offsetof(da_plan_info, workspace_bytes));return 0;}\n")
     exe = tmp_path / "layout"
     inc = os.path.join(os.path.dirname(B.HEADER))
     subprocess.run(["gcc", f"-I{inc}", str(src), "-o", str(exe)], check=True)
     got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
-    want = [ctypes.sizeof(B.da_params), B.da_params.softmax_scale.offset,
+    want = [ctypes.sizeof(B.da_params), B.da_params.side_scale.offset,
             B.da_params.reserved.offset, ctypes.sizeof(B.da_plan_info),
             B.da_plan_info.workspace_bytes.offset]
     assert [int(x) for x in got] == want
