@@ -585,6 +585,7 @@ def run_ours(args, dist):
         dev, args, flush, dist, peak, ("fold_4x256k", "ragged_tree_16x8"))
     if others is not None:
         others.append(fold_ring_row(dev, args, flush, dist, peak))
+        others.append(fold_fp8_row(dev, args, flush, dist, peak))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -754,6 +755,53 @@ def fold_ring_row(dev, args, flush, dist, peak):
     ring.close()
     dl.close()
     del dl
+    torch.cuda.empty_cache()
+    return row
+
+
+def fold_fp8_row(dev, args, flush, dist, peak):
+    """FOLD 4 x 256K with the side cache as E4M3 codes (da_params.side_fp8):
+    the attention call timed as in all_workloads.  kv_bytes counts what the
+    call must read: bf16 K and V of every local key, one-byte K and bf16 V of
+    every far key."""
+    wl = WL.WORKLOADS["fold_4x256k"]
+    dl = DraftLoop(wl, dev, ("fold",))
+    scale = 1.0 / 64            # N(0, 1) keys: |k| / scale stays well below 448
+    f8 = dl.B.DraftAttention(
+        device=dev.index or 0, batch=wl.batch, n_q=wl.n_q, num_q_heads=wl.num_q_heads,
+        num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_pages=dl.npg,
+        max_pages_per_seq=dl.bt.shape[1], dtype=wl.dtype, mode="fold", window=wl.window,
+        alpha=wl.alpha, far_mix=wl.far_mix, rope_theta=wl.rope_theta, side_fp8=1,
+        side_scale=scale)
+    # set-up, outside the timed region: the codes of the float32 quotient,
+    # rounded to nearest even (what the append kernel writes for these keys)
+    ks8 = torch.empty(dl.k_side.shape, dtype=torch.uint8, device=dev)
+    for i in range(0, dl.k_side.shape[0], 1024):
+        ks8[i:i + 1024] = (dl.k_side[i:i + 1024].float() / scale).to(
+            torch.float8_e4m3fn).view(torch.uint8)
+    torch.cuda.synchronize()
+
+    def call():
+        f8.run(dl.q[0], dl.qpos[0], dl.lens[0], dl.bt, dl.k_cache, dl.v_cache, ks8, out=dl.out)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+    nb = 0
+    for L in dl.lens[0].cpu().tolist():
+        loc = min(wl.window, L)
+        nb += wl.num_kv_heads * wl.head_dim * (4 * loc + 3 * (L - loc))
+    row = {"workload": "fold_4x256k", "mode": "fold, FP8 E4M3 side cache", "us": round(ms * 1e3, 2),
+           "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+           "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+           "side_cache_bytes": ks8.numel(),
+           "side_cache_bytes_bf16": dl.k_side.numel() * dl.k_side.element_size()}
+    assert f8.status() == (dl.B.DA_OK, 0)
+    f8.close()
+    dl.close()
+    del dl, ks8
     torch.cuda.empty_cache()
     return row
 
