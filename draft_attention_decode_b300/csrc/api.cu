@@ -29,6 +29,11 @@ namespace {
 
 constexpr int kAbiVersion = 101;
 
+// FOLD's rotated-K ring: pages of sinks that keep their own slots.
+int32_t ring_sink_pages(const da_params& p) {
+  return p.n_sink > 0 ? (int32_t)(((int64_t)p.n_sink + da::kPage - 1) / da::kPage) : 0;
+}
+
 struct DeviceGuard {
   int prev = -1;
   bool ok = false;
@@ -106,6 +111,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->n_cta = p.num_ctas;
   a->min_pages = p.min_pages_per_cta > 0 ? p.min_pages_per_cta : da::kMinPagesPerCta;
   a->k_ring = p.k_ring_pages;
+  a->k_ring_sp = p.k_ring_pages > 0 ? ring_sink_pages(p) : 0;
   for (int i = 0; i < 64; ++i) a->turn_freq[i] = pl->turn_freq[i];
 }
 
@@ -172,7 +178,9 @@ int draft_attn_check_params(const da_params* p) {
   }
   if (p->k_ring_pages != 0) {   // FOLD's rotated K kept for the local window only
     if (p->mode != DA_MODE_FOLD || p->window < 1) return DA_ERR_INVALID_ARG;
-    if (p->k_ring_pages < (p->window + da::kPage - 1) / da::kPage + 1) return DA_ERR_INVALID_ARG;
+    if (p->n_sink < 0) return DA_ERR_INVALID_ARG;
+    if (p->k_ring_pages < ring_sink_pages(*p) + (p->window + da::kPage - 1) / da::kPage + 1)
+      return DA_ERR_INVALID_ARG;
     if ((int64_t)p->k_ring_pages * p->batch * p->num_kv_heads * da::kPage >= (int64_t)1 << 31)
       return DA_ERR_INVALID_ARG;
   }
@@ -182,8 +190,6 @@ int draft_attn_check_params(const da_params* p) {
   if ((p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) && p->n_sink < 0)
     return DA_ERR_INVALID_ARG;
   if (p->mode == DA_MODE_FOLD) {
-    // the ring keeps rotated K for the local window only, not for sinks
-    if (p->k_ring_pages != 0 && p->n_sink != 0) return DA_ERR_INVALID_ARG;
     if (!(p->alpha > 0.f) || !std::isfinite(p->alpha)) return DA_ERR_INVALID_ARG;
     if (!(p->far_mix >= 0.f && p->far_mix <= 1.f)) return DA_ERR_INVALID_ARG;
   }
@@ -298,6 +304,7 @@ int draft_attn_append_kv(da_plan_t pl, const void* k_new, const void* v_new, con
   a.max_pages = pl->p.max_pages_per_seq;
   a.num_pages = pl->p.num_pages;
   a.k_ring = pl->p.k_ring_pages;
+  a.k_ring_sp = pl->p.k_ring_pages > 0 ? ring_sink_pages(pl->p) : 0;
   a.side_f8 = pl->p.side_fp8;
   a.side_scale = pl->p.side_scale;
   for (int i = 0; i < 64; ++i) a.turn_freq[i] = pl->turn_freq[i];

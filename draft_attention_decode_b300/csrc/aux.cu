@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     return;
   }
   const int64_t dst = (((int64_t)phys * a.H_kv + h) * kPage + (pos - pg * kPage)) * D;
-  const int64_t kpage = a.k_ring > 0 ? (int64_t)b * a.k_ring + pg % a.k_ring : phys;
+  const int64_t kpage =
+      a.k_ring > 0 ? (int64_t)b * a.k_ring + ring_slot(pg, a.k_ring, a.k_ring_sp) : phys;
   T* kc = static_cast<T*>(a.k_cache) + ((kpage * a.H_kv + h) * kPage + (pos - pg * kPage)) * D;
   T* vc = static_cast<T*>(a.v_cache) + dst;
   T* ks = (a.k_side && !a.side_f8) ? static_cast<T*>(a.k_side) + dst : nullptr;

@@ -60,7 +60,8 @@ struct DecodeArgs {
   // this kernel start, so every input but the caches it writes may be read
   // before griddepcontrol.wait; only the producer's first cache load waits.
   int32_t inputs_ready;
-  int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + P mod k_ring
+  int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + ring_slot(P)
+  int32_t k_ring_sp;    // pages of sinks at the head of each sequence's ring
   float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 
@@ -125,6 +126,13 @@ __host__ __device__ __forceinline__ bool range_is_far(int mode, int r) {
 
 __host__ __device__ __forceinline__ int32_t range_pages(int32_t k0, int32_t k1) {
   return k1 > k0 ? (k1 + kPage - 1) / kPage - k0 / kPage : 0;
+}
+
+// FOLD's ring of rotated keys: slot of logical page P in a sequence's R
+// pages.  The first sp pages (the sinks' pages) keep their own slots; later
+// pages cycle through the other R - sp.
+__host__ __device__ __forceinline__ int32_t ring_slot(int32_t P, int32_t R, int32_t sp) {
+  return P < sp ? P : sp + (P - sp) % (R - sp);
 }
 
 // Shared virtual position of the FOLD far memory (the newest far token).

@@ -56,7 +56,8 @@ struct AppendArgs {
   void* k_side;
   uint32_t* status;
   int32_t B, n_new, H_kv, max_pages, num_pages;
-  int32_t k_ring;   // rotated K of page P of sequence b at b * k_ring + P mod k_ring (0: paged)
+  int32_t k_ring;   // rotated K of page P of sequence b at b * k_ring + ring_slot (0: paged)
+  int32_t k_ring_sp;  // sink pages at the head of the ring
   int32_t side_f8;  // k_side holds E4M3 codes of k / side_scale
   float side_scale;
   float2 turn_freq[64];

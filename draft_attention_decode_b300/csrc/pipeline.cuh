@@ -234,7 +234,8 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
       flags = (first ? kFirst : 0) | (last ? kLast : 0) | (phys >= 0 ? kValid : 0);
       far = (fold && w.r == 0) ? 1 : 0;
-      kphys = (a.k_ring > 0 && !far) ? w.b * a.k_ring + P % a.k_ring : phys;
+      kphys = (a.k_ring > 0 && !far) ? w.b * a.k_ring + ring_slot(P, a.k_ring, a.k_ring_sp)
+                                     : phys;
       if (a.tree_mask && a.n_tree > 0 && !far) {
         const int32_t t0 = s.len[w.b] - a.n_tree;   // position of tree token 0
         if (pk0 + kPage > t0) toff = pk0 - t0;

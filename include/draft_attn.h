@@ -135,17 +135,20 @@ typedef struct {
   int32_t tree_size;         /* draft-tree tokens at the end of each context,
                                 0..64 (<= window in window and FOLD modes); the
                                 per-query masks go to draft_attn_run_tree        */
-  int32_t k_ring_pages;      /* FOLD only: 0, or R >= ceil(window / 64) + 1.  The
-                                rotated K cache then keeps only the local window:
+  int32_t k_ring_pages;      /* FOLD only: 0, or R >= S + ceil(window / 64) + 1,
+                                S = ceil(n_sink / 64) the sinks' pages.  The
+                                rotated K cache then keeps only the local keys:
                                 logical page P of sequence b lives at page
-                                b * R + (P mod R) of k_cache (batch * R pages),
-                                while the side cache and the V cache stay paged
-                                by the block table.  The far memory reads the
-                                side cache only, so the unrotated keys are the
-                                one full-length copy of K.  Appends then cover
-                                every sequence (batch = params.batch), and one
-                                call must not hold two positions R * 64 apart
-                                (they would share a slot).                       */
+                                b * R + P for P < S, else at b * R + S +
+                                ((P - S) mod (R - S)), of k_cache (batch * R
+                                pages), while the side cache and the V cache stay
+                                paged by the block table.  The far memory reads
+                                the side cache only, so the unrotated keys are
+                                the one full-length copy of K.  Appends then
+                                cover every sequence (batch = params.batch), and
+                                one call must not hold two positions of pages
+                                >= S that are (R - S) * 64 apart (they would
+                                share a slot).                                   */
   int32_t side_fp8;          /* FOLD only: 0 = k_side in dtype; 1 = k_side as FP8
                                 E4M3 codes (one byte per element) of the float32
                                 quotient k / side_scale, rounded to nearest, ties

@@ -56,6 +56,9 @@ def _ok_params(**kw):
     (dict(mode="fold", window=16, alpha=2.0, n_sink=4), 0),       # sinks join the local softmax
     (dict(mode="fold", window=16, alpha=2.0, n_sink=-1), -1),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=4, k_ring_pages=5), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=4, k_ring_pages=6), 0),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=70, k_ring_pages=6), -1),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, n_sink=70, k_ring_pages=7), 0),
     # FOLD side cache as FP8 E4M3 codes
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=0.05), 0),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=0.05,

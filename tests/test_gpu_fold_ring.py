@@ -21,7 +21,8 @@ def _need_gpu(cuda_lib):
     yield
 
 
-def _fold_run(W, L0, steps, H_q, H_kv, ring, seed, d=128, alpha=2.0, lam=0.5, fused=False):
+def _fold_run(W, L0, steps, H_q, H_kv, ring, seed, d=128, alpha=2.0, lam=0.5, fused=False,
+              n_sink=0):
     """FOLD draft steps; returns the outputs, the oracle's and the K cache."""
     dev = torch.device("cuda", 0)
     B_ = len(L0)
@@ -35,18 +36,20 @@ def _fold_run(W, L0, steps, H_q, H_kv, ring, seed, d=128, alpha=2.0, lam=0.5, fu
             for b in range(B_)]
     bt = torch.tensor(np.stack(rows), dtype=torch.int32, device=dev)
     num_pages = B_ * max_pages
-    R = (W + 63) // 64 + 1 if ring else 0
+    SP = (n_sink + 63) // 64                 # the sinks' pages keep their own slots
+    R = SP + (W + 63) // 64 + 1 if ring else 0
     da = B.DraftAttention(device=0, batch=B_, n_q=1, num_q_heads=H_q, num_kv_heads=H_kv,
                           head_dim=d, num_pages=num_pages, max_pages_per_seq=max_pages,
                           dtype="bf16", mode="fold", window=W, alpha=alpha, far_mix=lam,
-                          rope_theta=1e4, k_ring_pages=R)
+                          rope_theta=1e4, k_ring_pages=R, n_sink=n_sink)
     k_pages = B_ * R if ring else num_pages
     kc = torch.full((k_pages, H_kv, 64, d), float("nan"), dtype=torch.bfloat16, device=dev)
     vc = torch.full((num_pages, H_kv, 64, d), float("nan"), dtype=torch.bfloat16, device=dev)
     ks = torch.full_like(vc, float("nan"))
     # every sequence in each append (ring rows are sequence indices); no two
-    # positions of one append share a ring slot; padding positions are -1
-    chunk = 64 * R if ring else 1 << 20
+    # positions of one append share a ring slot (page-aligned chunks of R - SP
+    # pages); padding positions are -1
+    chunk = 64 * (R - SP) if ring else 1 << 20
     for s0 in range(0, max(L0), chunk):
         n = min(chunk, max(L0) - s0)
         kk = torch.zeros((B_, n, H_kv, d), dtype=torch.bfloat16, device=dev)
@@ -59,7 +62,7 @@ def _fold_run(W, L0, steps, H_q, H_kv, ring, seed, d=128, alpha=2.0, lam=0.5, fu
             pos[b, :m] = torch.arange(s0, s0 + m, dtype=torch.int32, device=dev)
         da.append_kv(kk, vv, pos, bt, kc, vc, ks)
     outs, wants = [], []
-    prm = orc.Params("fold", window=W, alpha=alpha, far_mix=lam, rope_theta=1e4)
+    prm = orc.Params("fold", window=W, n_sink=n_sink, alpha=alpha, far_mix=lam, rope_theta=1e4)
     G = H_q // H_kv
     for st in range(steps):
         k_new = torch.stack([k_raw[b][c + st:c + st + 1] for b, c in enumerate(L0)]).contiguous()
@@ -90,17 +93,19 @@ def _fold_run(W, L0, steps, H_q, H_kv, ring, seed, d=128, alpha=2.0, lam=0.5, fu
     return outs, wants, kc, bt
 
 
-@pytest.mark.parametrize("W,shape,fused", [(200, (32, 8), False), (2048, (32, 8), True),
-                                           (64, (64, 8), False), (130, (16, 2), True)],
-                         ids=["w200-r4", "w2048-r4-step", "w64-r8", "w130-r8-step"])
-def test_fold_ring_draft_loop(W, shape, fused):
+@pytest.mark.parametrize("W,shape,fused,ns", [(200, (32, 8), False, 0), (2048, (32, 8), True, 0),
+                                              (64, (64, 8), False, 0), (130, (16, 2), True, 0),
+                                              (200, (32, 8), False, 4), (130, (64, 8), True, 70)],
+                         ids=["w200-r4", "w2048-r4-step", "w64-r8", "w130-r8-step",
+                              "w200-r4-sinks4", "w130-r8-step-sinks70"])
+def test_fold_ring_draft_loop(W, shape, fused, ns):
     """Draft steps crossing page boundaries; the initial fill wraps the ring
-    many times."""
+    many times; the sinks' pages keep their own slots."""
     H_q, H_kv = shape
     L0 = [64 * 70 - 3, 64 * 21 + 10]
     steps = 9
-    ring_out, wants, _, _ = _fold_run(W, L0, steps, H_q, H_kv, True, 37, fused=fused)
-    paged_out, _, _, _ = _fold_run(W, L0, steps, H_q, H_kv, False, 37, fused=fused)
+    ring_out, wants, _, _ = _fold_run(W, L0, steps, H_q, H_kv, True, 37, fused=fused, n_sink=ns)
+    paged_out, _, _, _ = _fold_run(W, L0, steps, H_q, H_kv, False, 37, fused=fused, n_sink=ns)
     for st in range(steps):
         assert torch.equal(ring_out[st], paged_out[st]), f"step {st}"
         if st % 3 == 0:
