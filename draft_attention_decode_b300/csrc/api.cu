@@ -201,9 +201,10 @@ int draft_attn_check_params(const da_params* p) {
   if (rows > 32) return DA_ERR_UNSUPPORTED;
   if (rows > 8 && (p->dtype != DA_DTYPE_BF16 || p->engine == 1)) return DA_ERR_UNSUPPORTED;
   if (p->engine == 2 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
-  // the FP8 side cache is read by the CUDA-core engine with 128-byte key rows
-  if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || p->head_dim != 128 || rows > 4 ||
-                           p->engine == 2))
+  // the FP8 side cache: 128-byte key rows (bf16, head_dim 128), read by the
+  // turn-taking CUDA-core engine (<= 4 rows) or the tensor-core engine
+  if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || p->head_dim != 128 ||
+                           (p->engine == 1 && rows > 4)))
     return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }

@@ -17,8 +17,9 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
   if (engine_hint == 2) mma = true;
   c->pingpong = false;
   c->side_f8 = side_f8;
-  // The FP8 side cache (FOLD) is read by the turn-taking CUDA-core engine only.
-  if (side_f8 && (mma || dtype != DA_DTYPE_BF16 || d != 128 || rows > 4 || mode != DA_MODE_FOLD))
+  // The FP8 side cache (FOLD): the turn-taking CUDA-core engine (<= 4 rows) or
+  // the tensor-core engine, bf16, head_dim 128.
+  if (side_f8 && (dtype != DA_DTYPE_BF16 || d != 128 || mode != DA_MODE_FOLD || (!mma && rows > 4)))
     return false;
   if (mma) {
     if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
@@ -52,6 +53,15 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
 template <class F>
 static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
   using bf = __nv_bfloat16;
+  // The FP8 side-cache instances first: they take precedence over the engine's others.
+  if (c.side_f8 && c.engine == DA_ENGINE_MMA) {
+    if (dtype != DA_DTYPE_BF16 || d != 128) return cudaErrorInvalidValue;
+#define DA_MMA_F8(NT, SPLIT, RK) \
+  if (c.rk == RK) return f(decode_kernel<bf, 128, MmaEngine<128, NT, SPLIT, true>, 1, RK>);
+    DA_MMA_F8(1, true, 8) DA_MMA_F8(2, true, 16) DA_MMA_F8(2, false, 32)
+#undef DA_MMA_F8
+    return cudaErrorInvalidValue;
+  }
   if (c.engine == DA_ENGINE_MMA) {
     if (dtype != DA_DTYPE_BF16) return cudaErrorInvalidValue;
 #define DA_MMA(D, NT, SPLIT, RK) \

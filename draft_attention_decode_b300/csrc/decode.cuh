@@ -32,7 +32,7 @@ namespace da {
 // [rk][d] as FP32, and each row's draft-tree mask into s.tmask.  Rows >= R
 // are zero.  Consumer threads only.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int RK, int NCT>
+template <typename T, int D, int RK, int NCT, bool KSQ = true>
 __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
   const int tid = threadIdx.x;
   const int bh = seq >> 1, b = bh / a.H_kv, h = bh - b * a.H_kv;
@@ -50,7 +50,8 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
     float mult = a.scale_log2;
     if (far) {
       // "FOLD", abstract: concentration factor; an FP8 side cache's scale
-      mult *= a.alpha * a.far_kscale;
+      // (unless the engine applies it to the scores: KSQ false)
+      mult *= KSQ ? a.alpha * a.far_kscale : a.alpha;
     } else if (a.mode == DA_MODE_SHARP) {    // "SharpDraft", Abstract: query scaling
       int32_t n = visible_keys(a.mode, L, a.W, a.n_sink);
       if (a.tree_mask && a.n_tree > 0) {
@@ -251,6 +252,7 @@ struct CoreEngine {
   static constexpr bool kPairs = true;         // takes two pages per step
   static constexpr bool kPingPong = PINGPONG;  // the two warp groups alternate steps
   static constexpr bool kSideF8 = F8;          // far keys as E4M3 codes
+  static constexpr bool kFarScaleInQ = true;
   static constexpr int GW = PINGPONG ? NCW / 2 : NCW;   // warps sharing a step
   static constexpr int LPK = 8;                // lanes per key
   static constexpr int KG = 32 / LPK;          // key groups per pass
@@ -552,6 +554,7 @@ struct CoreEngineWide {
   static constexpr bool kPairs = false;
   static constexpr bool kPingPong = false;
   static constexpr bool kSideF8 = false;
+  static constexpr bool kFarScaleInQ = true;
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int ES = sizeof(T);
@@ -759,6 +762,26 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E4M3 codes (low byte first) as an f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(r) : "r"(two_codes));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -771,11 +794,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 //    a small draft tree).
 //  * otherwise: both groups work on every page, on row halves of
 //    RK = 16 NT rows (32 rows: an 8-token draft tree over a GQA group of 4).
-template <int D, int NT, bool SPLIT_PAGES>
+// With F8 (FOLD with an FP8 side cache, head_dim 128) a far piece's QK^T is an
+// f16 MMA: E4M3 codes widen exactly to f16 pairs, and the k order inside each
+// k-step is permuted so that a thread's A elements are whole bytes of its own
+// 32-byte span of the key row: logical k = 2t + j (+ 8 h) of k-step ks is
+// dimension 32 t + 4 ks + 2 h + j.  The queries take the same order (in f16)
+// and the side cache's scale multiplies the scores.
+template <int D, int NT, bool SPLIT_PAGES, bool F8 = false>
 struct MmaEngine {
   static constexpr bool kPairs = false;
   static constexpr bool kPingPong = false;
-  static constexpr bool kSideF8 = false;
+  static constexpr bool kSideF8 = F8;
+  static constexpr bool kFarScaleInQ = !F8;   // F8: the scale goes on the scores
+  static_assert(!F8 || D == 128, "FP8 side cache: head_dim 128");
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
@@ -785,6 +816,7 @@ struct MmaEngine {
   uint32_t qf[KS][NT][2];
   float O[KS][NT][4];
   float m[NT][2], l[NT][2];
+  float kscale;          // F8: the side cache's scale
   int lane, warp, kb, grp, g, t;
 
   __device__ __forceinline__ void init() {
@@ -826,6 +858,25 @@ struct MmaEngine {
     reset();
   }
 
+  // F8: a far piece's queries in f16, in the permuted k order.
+  __device__ __forceinline__ void begin_far(const Smem& s, bool far) {
+    if (!far) {
+      begin(s);
+      return;
+    }
+    const int row0 = SPLIT_PAGES ? 0 : grp * RW;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float* qr = s.q + (row0 + 8 * nt + g) * D + 32 * t + 4 * ks;
+        qf[ks][nt][0] = pack_f16(qr[0], qr[1]);
+        qf[ks][nt][1] = pack_f16(qr[2], qr[3]);
+      }
+    reset();
+  }
+
+  template <bool FK = false>
   __device__ __forceinline__ void page(const Smem& s, uint32_t kbase, uint32_t vbase, int lo, int hi,
                                        int toff) {
     const int key0 = 16 * kb;
@@ -835,13 +886,37 @@ struct MmaEngine {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) S[nt][c] = 0.f;
-    const int krow = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    if constexpr (FK) {
+      // rows key0 + g and key0 + g + 8; bytes 32 t .. 32 t + 31 (chunks 2t, 2t+1)
+      uint32_t w[2][2][4];
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(swz_addr(kbase, krow, (16 * ks + (lane >> 4) * 8) * 2), a);
+      for (int rh = 0; rh < 2; ++rh)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+        for (int c = 0; c < 2; ++c)
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w[rh][c][0]), "=r"(w[rh][c][1]), "=r"(w[rh][c][2]), "=r"(w[rh][c][3])
+                       : "r"(swz_addr(kbase, key0 + g + 8 * rh, (2 * t + c) * 16)));
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t w0 = w[0][ks >> 2][ks & 3], w1 = w[1][ks >> 2][ks & 3];
+        const uint32_t a[4] = {e4m3x2_f16x2(w0 & 0xffffu), e4m3x2_f16x2(w1 & 0xffffu),
+                               e4m3x2_f16x2(w0 >> 16), e4m3x2_f16x2(w1 >> 16)};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) S[nt][c] *= kscale;
+    } else {
+      const int krow = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(swz_addr(kbase, krow, (16 * ks + (lane >> 4) * 8) * 2), a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      }
     }
     if (toff != kNoTree) {   // draft-tree keys a row does not see
       const int row0 = SPLIT_PAGES ? 0 : grp * RW;
@@ -1194,12 +1269,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_inc<kConsumerRegs>();
   Engine eng;
   eng.init();
+  if constexpr (!Engine::kFarScaleInQ) eng.kscale = a.far_kscale;
   zero_empty<T, D, NCT>(a, s);
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
     const Where w = locate(s, a.B, a.H_kv, xs);
     const int32_t seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
-    prep_queries<T, D, RK, NCT>(a, s, seq);
+    prep_queries<T, D, RK, NCT, Engine::kFarScaleInQ>(a, s, seq);
     if constexpr (Engine::kSideF8) eng.begin_far(s, (seq & 1) == 0); else eng.begin(s);
   }
   const uint32_t base = smem_u32(s.stage);
@@ -1211,7 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status)) break;
     const PageInfo inf = s.info[st];
     if ((inf.flags & kFirst) && x != xs) {
-      prep_queries<T, D, RK, NCT>(a, s, inf.seq);
+      prep_queries<T, D, RK, NCT, Engine::kFarScaleInQ>(a, s, inf.seq);
       if constexpr (Engine::kSideF8) eng.begin_far(s, (inf.seq & 1) == 0); else eng.begin(s);
     }
     const uint32_t kb0 = base + st * L.stage_bytes;

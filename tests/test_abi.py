@@ -74,9 +74,11 @@ def _ok_params(**kw):
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
           dtype="fp32"), -2),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
-          num_q_heads=64), -2),                      # 8 rows per KV head
+          num_q_heads=64), 0),                       # 8 rows per KV head: tensor cores
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
-          engine="mma"), -2),
+          num_q_heads=64, engine="cuda_core"), -2),
+    (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
+          engine="mma"), 0),
     (dict(mode="sharp", scale_slope=-1.0), -1),
     (dict(mode="sharp", scale_ref=0), -1),
     (dict(rope_theta=0.0), 0),                         # NoPE

@@ -1,8 +1,9 @@
 """FOLD with the side cache as FP8 E4M3 codes (da_params.side_fp8): the append
 kernel's bytes equal the oracle's codes bit for bit, and the attention over
 the quantised far memory matches the float64 oracle, which quantises the same
-way, at every row count, split, with sinks, draft trees and the rotated-K
-ring; keys outside the saturation limit clamp the same way on both sides."""
+way, at every row count and engine, split, with sinks, draft trees and the
+rotated-K ring; keys outside the saturation limit clamp the same way on both
+sides."""
 import numpy as np
 import pytest
 import torch
@@ -44,10 +45,11 @@ def test_append_writes_e4m3_codes(scale):
     s.close()
 
 
-SHAPES = [(8, 8, 1), (16, 8, 1), (32, 8, 1)]   # 1, 2 and 4 rows per KV head
+# rows per KV head 1, 2, 4 (CUDA cores), 8, 16, 32 (tensor cores)
+SHAPES = [(8, 8, 1), (16, 8, 1), (32, 8, 1), (64, 8, 1), (32, 8, 4), (32, 8, 8)]
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=lambda x: "h%d_%d" % x[:2])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda x: "h%d_%d_q%d" % x)
 @pytest.mark.parametrize("kw", [dict(), dict(n_sink=70), dict(num_ctas=7), dict(num_ctas=1)],
                          ids=["plain", "sinks", "ctas7", "ctas1"])
 def test_fold_fp8_parity(shape, kw):
@@ -55,18 +57,31 @@ def test_fold_fp8_parity(shape, kw):
     s = Setup(batch=3, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
               ctx=[3000, 129, 1000], mode="fold", window=200, alpha=2.0, far_mix=0.5, seed=33,
               side_fp8_scale=1 / 64, **kw)
-    assert s.da.info()["engine_name"] == "cuda_core"
+    rows = (h // hk) * nq
+    assert s.da.info()["engine_name"] == ("cuda_core" if rows <= 4 else "mma")
     compare(s.run(), s.oracle(), "bf16", f"fold fp8 {shape} {kw}")
     assert s.status() == (B.DA_OK, 0)
     s.close()
 
 
-def test_fold_fp8_saturating_scale():
+@pytest.mark.parametrize("h,engine", [(32, "auto"), (64, "auto"), (32, "mma")],
+                         ids=["r4-core", "r8-mma", "r4-mma-forced"])
+def test_fold_fp8_saturating_scale(h, engine):
     """A scale that saturates part of the keys: both sides clamp to 448."""
-    s = Setup(batch=1, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+    s = Setup(batch=1, n_q=1, num_q_heads=h, num_kv_heads=8, head_dim=128, dtype="bf16",
               ctx=[2500], mode="fold", window=256, alpha=2.0, far_mix=0.7, seed=34,
-              side_fp8_scale=1 / 256)
-    compare(s.run(), s.oracle(), "bf16", "fold fp8 saturating")
+              side_fp8_scale=1 / 256, engine=engine)
+    compare(s.run(), s.oracle(), "bf16", f"fold fp8 saturating {h} {engine}")
+    s.close()
+
+
+def test_fold_fp8_tiny_scale_tensor_cores():
+    """A tiny scale (codes far from 1): the tensor-core engine applies it to the
+    scores, not to its f16 queries."""
+    s = Setup(batch=1, n_q=1, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=[3000], mode="fold", window=256, alpha=2.0, far_mix=0.7, seed=38,
+              side_fp8_scale=1e-3)
+    compare(s.run(), s.oracle(), "bf16", "fold fp8 scale 1e-3")
     s.close()
 
 
@@ -135,10 +150,10 @@ def test_fold_fp8_with_k_ring():
     ref.close()
 
 
-def test_fp8_side_needs_cuda_core_rows():
+def test_fp8_side_refused_on_the_wide_cuda_core_engine():
     p = B.make_params(batch=1, n_q=1, num_q_heads=64, num_kv_heads=8, head_dim=128,
                       num_pages=10, max_pages_per_seq=10, mode="fold", window=64, alpha=2.0,
-                      far_mix=0.5, side_fp8=1, side_scale=1.0)
+                      far_mix=0.5, side_fp8=1, side_scale=1.0, engine="cuda_core")
     with pytest.raises(B.DraftAttnError) as e:
         B.draft_attn_plan(p, 0)
     assert e.value.code == B.DA_ERR_UNSUPPORTED
