@@ -176,7 +176,7 @@ int draft_attn_check_params(const da_params* p) {
   } else if (p->side_scale != 0.f) {
     return DA_ERR_INVALID_ARG;
   }
-  if (p->k_ring_pages != 0) {   // FOLD's rotated K kept for the local window only
+  if (p->k_ring_pages != 0) {   // FOLD's rotated K kept for the local keys only
     if (p->mode != DA_MODE_FOLD || p->window < 1) return DA_ERR_INVALID_ARG;
     if (p->n_sink < 0) return DA_ERR_INVALID_ARG;
     if (p->k_ring_pages < ring_sink_pages(*p) + (p->window + da::kPage - 1) / da::kPage + 1)
