@@ -586,6 +586,7 @@ def run_ours(args, dist):
     if others is not None:
         others.append(fold_ring_row(dev, args, flush, dist, peak))
         others.append(fold_fp8_row(dev, args, flush, dist, peak))
+        others.append(fold_fp8_row(dev, args, flush, dist, peak, engine="mma"))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -759,11 +760,11 @@ def fold_ring_row(dev, args, flush, dist, peak):
     return row
 
 
-def fold_fp8_row(dev, args, flush, dist, peak):
+def fold_fp8_row(dev, args, flush, dist, peak, engine="auto"):
     """FOLD 4 x 256K with the side cache as E4M3 codes (da_params.side_fp8):
-    the attention call timed as in all_workloads.  kv_bytes counts what the
-    call must read: bf16 K and V of every local key, one-byte K and bf16 V of
-    every far key."""
+    the attention call timed as in all_workloads, on the automatic engine or
+    forced onto the tensor cores.  kv_bytes counts what the call must read:
+    bf16 K and V of every local key, one-byte K and bf16 V of every far key."""
     wl = WL.WORKLOADS["fold_4x256k"]
     dl = DraftLoop(wl, dev, ("fold",))
     scale = 1.0 / 64            # N(0, 1) keys: |k| / scale stays well below 448
@@ -772,7 +773,7 @@ def fold_fp8_row(dev, args, flush, dist, peak):
         num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_pages=dl.npg,
         max_pages_per_seq=dl.bt.shape[1], dtype=wl.dtype, mode="fold", window=wl.window,
         alpha=wl.alpha, far_mix=wl.far_mix, rope_theta=wl.rope_theta, side_fp8=1,
-        side_scale=scale)
+        side_scale=scale, engine=engine)
     # set-up, outside the timed region: the codes of the float32 quotient,
     # rounded to nearest even (what the append kernel writes for these keys)
     ks8 = torch.empty(dl.k_side.shape, dtype=torch.uint8, device=dev)
@@ -793,7 +794,8 @@ def fold_fp8_row(dev, args, flush, dist, peak):
     for L in dl.lens[0].cpu().tolist():
         loc = min(wl.window, L)
         nb += wl.num_kv_heads * wl.head_dim * (4 * loc + 3 * (L - loc))
-    row = {"workload": "fold_4x256k", "mode": "fold, FP8 E4M3 side cache", "us": round(ms * 1e3, 2),
+    label = "fold, FP8 E4M3 side cache" + (", tensor-core engine forced" if engine == "mma" else "")
+    row = {"workload": "fold_4x256k", "mode": label, "us": round(ms * 1e3, 2),
            "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
            "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
            "side_cache_bytes": ks8.numel(),
