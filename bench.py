@@ -586,7 +586,7 @@ def run_ours(args, dist):
     if others is not None:
         others.append(fold_ring_row(dev, args, flush, dist, peak))
         others.append(fold_fp8_row(dev, args, flush, dist, peak))
-        others.append(fold_fp8_row(dev, args, flush, dist, peak, engine="mma"))
+        others.append(fold_fp8_row(dev, args, flush, dist, peak, engine="cuda_core"))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -762,8 +762,8 @@ def fold_ring_row(dev, args, flush, dist, peak):
 
 def fold_fp8_row(dev, args, flush, dist, peak, engine="auto"):
     """FOLD 4 x 256K with the side cache as E4M3 codes (da_params.side_fp8):
-    the attention call timed as in all_workloads, on the automatic engine or
-    forced onto the tensor cores.  kv_bytes counts what the call must read:
+    the attention call timed as in all_workloads, on the automatic engine (the
+    tensor cores) or forced onto the CUDA cores.  kv_bytes counts what the call must read:
     bf16 K and V of every local key, one-byte K and bf16 V of every far key."""
     wl = WL.WORKLOADS["fold_4x256k"]
     dl = DraftLoop(wl, dev, ("fold",))
@@ -794,7 +794,7 @@ def fold_fp8_row(dev, args, flush, dist, peak, engine="auto"):
     for L in dl.lens[0].cpu().tolist():
         loc = min(wl.window, L)
         nb += wl.num_kv_heads * wl.head_dim * (4 * loc + 3 * (L - loc))
-    label = "fold, FP8 E4M3 side cache" + (", tensor-core engine forced" if engine == "mma" else "")
+    label = "fold, FP8 E4M3 side cache" + (", CUDA-core engine forced" if engine == "cuda_core" else "")
     row = {"workload": "fold_4x256k", "mode": label, "us": round(ms * 1e3, 2),
            "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
            "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),

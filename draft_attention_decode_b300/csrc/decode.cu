@@ -11,8 +11,11 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
   // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
   // from 5 on, QK^T and PV are dense enough for an n8 tensor-core tile
-  // (bf16 only).  engine_hint 1/2 forces the CUDA cores / tensor cores.
-  bool mma = dtype == DA_DTYPE_BF16 && rows > 4;
+  // (bf16 only).  An FP8 side cache goes to the tensor cores at any row count:
+  // there its codes widen to f16 in one cvt per pair and feed the MMA, while
+  // on the FP32 pipes the widening makes the far scan issue-bound.
+  // engine_hint 1/2 forces the CUDA cores / tensor cores.
+  bool mma = dtype == DA_DTYPE_BF16 && (rows > 4 || side_f8);
   if (engine_hint == 1) mma = false;
   if (engine_hint == 2) mma = true;
   c->pingpong = false;
