@@ -121,26 +121,32 @@ def test_fold_fp8_tree():
     s.close()
 
 
-def test_fold_fp8_with_k_ring():
-    """The rotated K in a ring and the side cache in FP8: the side cache is the
-    one full-length copy of K, at one byte per element."""
+@pytest.mark.parametrize("ns,engine", [(0, "auto"), (70, "auto"), (70, "cuda_core")],
+                         ids=["plain", "sinks70", "sinks70-core"])
+def test_fold_fp8_with_k_ring(ns, engine):
+    """The rotated K in a ring (sink pages in their own slots) and the side cache
+    in FP8: the side cache is the one full-length copy of K, at one byte per
+    element; outputs equal the paged run's bit for bit."""
     dev = torch.device("cuda", 0)
     W, L, H_kv, d = 300, 4000, 8, 128
     ref = Setup(batch=1, n_q=1, num_q_heads=32, num_kv_heads=H_kv, head_dim=d, dtype="bf16",
-                ctx=[L], mode="fold", window=W, alpha=2.0, far_mix=0.5, seed=37,
-                side_fp8_scale=1 / 64)
+                ctx=[L], mode="fold", window=W, n_sink=ns, alpha=2.0, far_mix=0.5, seed=37,
+                side_fp8_scale=1 / 64, engine=engine)
     want = ref.run()
-    R = (W + 63) // 64 + 1
+    compare(want, ref.oracle(), "bf16", f"fold fp8 sinks={ns} {engine}")
+    SP = (ns + 63) // 64
+    R = SP + (W + 63) // 64 + 1
     da = B.DraftAttention(device=0, batch=1, n_q=1, num_q_heads=32, num_kv_heads=H_kv,
                           head_dim=d, num_pages=ref.num_pages,
                           max_pages_per_seq=ref.block_table.shape[1], dtype="bf16", mode="fold",
-                          window=W, alpha=2.0, far_mix=0.5, k_ring_pages=R, side_fp8=1,
-                          side_scale=1 / 64)
+                          window=W, n_sink=ns, alpha=2.0, far_mix=0.5, k_ring_pages=R,
+                          side_fp8=1, side_scale=1 / 64, engine=engine)
     kc = torch.full((R, H_kv, 64, d), float("nan"), dtype=torch.bfloat16, device=dev)
     vc = torch.full_like(ref.v_cache, float("nan"))
     ks = torch.full_like(ref.k_side, 0x7F)
-    for s0 in range(0, L, 64 * R):
-        n = min(64 * R, L - s0)
+    chunk = 64 * (R - SP)                 # page-aligned: no two positions share a slot
+    for s0 in range(0, L, chunk):
+        n = min(chunk, L - s0)
         pos = torch.arange(s0, s0 + n, dtype=torch.int32, device=dev).unsqueeze(0)
         da.append_kv(ref.k_raw[0][s0:s0 + n].unsqueeze(0).contiguous(),
                      ref.v[0][s0:s0 + n].unsqueeze(0).contiguous(), pos, ref.block_table,
