@@ -73,13 +73,17 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const da_params& p, int6
   const int es = fp8 ? 1 : p.dtype == DA_DTYPE_BF16 ? 2 : 4;
   cuuint64_t gdim[2] = {(cuuint64_t)p.head_dim, (cuuint64_t)pages * p.num_kv_heads * da::kPage};
   cuuint64_t gstride[1] = {(cuuint64_t)p.head_dim * es};
-  cuuint32_t box[2] = {(cuuint32_t)(da::kSwizzleRow / es), (cuuint32_t)da::kPage};
+  // fp8 rows of 64 bytes (head_dim 64) are copied whole and unswizzled
+  const bool narrow = fp8 && p.head_dim * es < da::kSwizzleRow;
+  cuuint32_t box[2] = {(cuuint32_t)(narrow ? p.head_dim : da::kSwizzleRow / es),
+                       (cuuint32_t)da::kPage};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                   : p.dtype == DA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   2, const_cast<void*>(base), gdim, gstride, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  narrow ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -201,10 +205,9 @@ int draft_attn_check_params(const da_params* p) {
   if (rows > 32) return DA_ERR_UNSUPPORTED;
   if (rows > 8 && (p->dtype != DA_DTYPE_BF16 || p->engine == 1)) return DA_ERR_UNSUPPORTED;
   if (p->engine == 2 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
-  // the FP8 side cache: 128-byte key rows (bf16, head_dim 128), read by the
-  // turn-taking CUDA-core engine (<= 4 rows) or the tensor-core engine
-  if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || p->head_dim != 128 ||
-                           (p->engine == 1 && rows > 4)))
+  // the FP8 side cache (bf16 caches): the tensor-core engine, or the
+  // turn-taking CUDA-core engine up to 4 rows
+  if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || (p->engine == 1 && rows > 4)))
     return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }

@@ -22,7 +22,7 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
   c->side_f8 = side_f8;
   // The FP8 side cache (FOLD): the turn-taking CUDA-core engine (<= 4 rows) or
   // the tensor-core engine, bf16, head_dim 128.
-  if (side_f8 && (dtype != DA_DTYPE_BF16 || d != 128 || mode != DA_MODE_FOLD || (!mma && rows > 4)))
+  if (side_f8 && (dtype != DA_DTYPE_BF16 || mode != DA_MODE_FOLD || (!mma && rows > 4)))
     return false;
   if (mma) {
     if (dtype != DA_DTYPE_BF16 || rows > 32) return false;
@@ -58,10 +58,11 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
   using bf = __nv_bfloat16;
   // The FP8 side-cache instances first: they take precedence over the engine's others.
   if (c.side_f8 && c.engine == DA_ENGINE_MMA) {
-    if (dtype != DA_DTYPE_BF16 || d != 128) return cudaErrorInvalidValue;
-#define DA_MMA_F8(NT, SPLIT, RK) \
-  if (c.rk == RK) return f(decode_kernel<bf, 128, MmaEngine<128, NT, SPLIT, true>, 1, RK>);
-    DA_MMA_F8(1, true, 8) DA_MMA_F8(2, true, 16) DA_MMA_F8(2, false, 32)
+    if (dtype != DA_DTYPE_BF16) return cudaErrorInvalidValue;
+#define DA_MMA_F8(D, NT, SPLIT, RK) \
+  if (d == D && c.rk == RK) return f(decode_kernel<bf, D, MmaEngine<D, NT, SPLIT, true>, 1, RK>);
+    DA_MMA_F8(128, 1, true, 8) DA_MMA_F8(128, 2, true, 16) DA_MMA_F8(128, 2, false, 32)
+    DA_MMA_F8(64, 1, true, 8) DA_MMA_F8(64, 2, true, 16) DA_MMA_F8(64, 2, false, 32)
 #undef DA_MMA_F8
     return cudaErrorInvalidValue;
   }
@@ -75,10 +76,12 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
     return cudaErrorInvalidValue;
   }
   if (c.side_f8) {
-    if (dtype != DA_DTYPE_BF16 || d != 128 || !c.pingpong) return cudaErrorInvalidValue;
-#define DA_CORE_F8(RK) \
-  if (c.rk == RK) return f(decode_kernel<bf, 128, CoreEngine<bf, 128, RK, true, true>, kVariantCore, RK>);
-    DA_CORE_F8(1) DA_CORE_F8(2) DA_CORE_F8(4)
+    if (dtype != DA_DTYPE_BF16 || !c.pingpong) return cudaErrorInvalidValue;
+#define DA_CORE_F8(D, RK)     \
+  if (d == D && c.rk == RK) \
+    return f(decode_kernel<bf, D, CoreEngine<bf, D, RK, true, true>, kVariantCore, RK>);
+    DA_CORE_F8(128, 1) DA_CORE_F8(128, 2) DA_CORE_F8(128, 4)
+    DA_CORE_F8(64, 1) DA_CORE_F8(64, 2) DA_CORE_F8(64, 4)
 #undef DA_CORE_F8
     return cudaErrorInvalidValue;
   }

@@ -239,11 +239,12 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 // (only when a score exceeds it by more than 2^8): the result is exact for
 // any reference value, and the accumulators are rescaled only a handful of
 // times.
-// With F8 (FOLD with an FP8 side cache, head_dim 128) a far piece's keys are
-// 128-byte rows of E4M3 codes: lane ds reads its 16 dimensions 16 ds .. 16 ds
-// + 15 as one 16-byte chunk (row-rotated by the swizzle, so the eight lanes of
-// a key cover all 32 banks), and the piece's queries are laid out in that
-// order (begin_far).
+// With F8 (FOLD with an FP8 side cache) a far piece's keys are rows of D
+// E4M3 codes: lane ds reads its DQ = D/8 dimensions DQ ds .. DQ ds + DQ - 1 in
+// one load (d 128: a 16-byte chunk of a 128-byte row, row-rotated by the TMA
+// swizzle, so the eight lanes of a key cover all 32 banks; d 64: 8 bytes of an
+// unswizzled 64-byte row, four consecutive keys filling 256 contiguous bytes),
+// and the piece's queries are laid out in that order (begin_far).
 // ---------------------------------------------------------------------------
 template <typename T, int D, int RK, bool PINGPONG, bool F8 = false>
 struct CoreEngine {
@@ -265,7 +266,7 @@ struct CoreEngine {
   static constexpr float kLazy = 8.f;          // log2 headroom before a rescale
   static_assert(RK == 1 || RK == 2 || RK == 4, "rows");
   static_assert(NCH >= 1 && (NCH & (NCH - 1)) == 0, "chunks");
-  static_assert(!F8 || (ES == 2 && D == 128 && PINGPONG), "FP8 side cache: bf16, d 128");
+  static_assert(!F8 || (ES == 2 && PINGPONG), "FP8 side cache: bf16, turn-taking groups");
 
   float2 q2[RK][DQ / 2];
   float2 o2[RK][DQ / 2];
@@ -273,7 +274,7 @@ struct CoreEngine {
   // Swizzled byte offsets of the lane's chunks on passes 0 and 1; pass ps adds
   // 1024 (ps / 2) bytes: its row is 8 further on and has the same swizzle.
   uint32_t off[2][NCH];
-  uint32_t off8[2];      // F8: the lane's E4M3 chunk on passes 0 and 1
+  uint32_t off8[2];      // F8: the lane's E4M3 codes on passes 0 and 1 (pass ps: + 8 D (ps / 2))
   int lane, warp, kg, ds;
   static_assert(KG == 4, "rows of passes ps and ps + 2 differ by 8");
   __device__ __forceinline__ uint32_t off_of(int ps, int i) const {
@@ -300,7 +301,7 @@ struct CoreEngine {
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int row = (warp & (GW - 1)) * KPW + kg + KG * it;
-        off8[it] = swz_addr(0u, row, ds * 16);
+        off8[it] = D == 128 ? swz_addr(0u, row, ds * 16) : (uint32_t)(row * D + ds * DQ);
       }
     }
   }
@@ -332,8 +333,8 @@ struct CoreEngine {
     reset();
   }
 
-  // F8: a far piece takes its queries in the order of the lane's E4M3 chunk
-  // (slot i, pair e: dimensions 16 ds + 8 i + 2 e, + 1).
+  // F8: a far piece takes its queries in the order of the lane's E4M3 codes
+  // (slot i, pair e: dimensions DQ ds + EPC i + 2 e, + 1).
   __device__ __forceinline__ void begin_far(const Smem& s, bool far) {
     if (!far) {
       begin(s);
@@ -345,7 +346,7 @@ struct CoreEngine {
       for (int r = 0; r < RK; ++r)
 #pragma unroll
         for (int e = 0; e < EPC / 2; ++e) {
-          const int d0 = ds * 16 + i * EPC + 2 * e;
+          const int d0 = ds * DQ + i * EPC + 2 * e;
           q2[r][i * (EPC / 2) + e] = make_float2(s.q[r * D + d0], s.q[r * D + d0 + 1]);
         }
     reset();
@@ -377,14 +378,18 @@ struct CoreEngine {
 #pragma unroll
         for (int r = 0; r < RK; ++r) acc[u][r] = make_float2(0.f, 0.f);
       if constexpr (FK) {
-        static_assert(NCH * EPC == 16, "one E4M3 chunk per lane and key");
-        uint32_t w[4];
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(kb[pg] + off8[ps & 1] + (uint32_t)(ps >> 1) * (8 * kSwizzleRow)));
-        float f[16];
+        static_assert(NCH * EPC == DQ && (DQ == 16 || DQ == 8), "one load per lane and key");
+        constexpr int NW = DQ / 4;   // 32-bit words of codes
+        uint32_t w[NW];
+        const uint32_t ka = kb[pg] + off8[ps & 1] + (uint32_t)(ps >> 1) * (8 * D);
+        if constexpr (NW == 4)
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(ka));
+        else
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(ka));
+        float f[DQ];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) e4m3x4_to_f32(w[j], f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+        for (int j = 0; j < NW; ++j) e4m3x4_to_f32(w[j], f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
 #pragma unroll
         for (int i = 0; i < NCH; ++i)
 #pragma unroll
@@ -794,19 +799,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 //    a small draft tree).
 //  * otherwise: both groups work on every page, on row halves of
 //    RK = 16 NT rows (32 rows: an 8-token draft tree over a GQA group of 4).
-// With F8 (FOLD with an FP8 side cache, head_dim 128) a far piece's QK^T is an
-// f16 MMA: E4M3 codes widen exactly to f16 pairs, and the k order inside each
-// k-step is permuted so that a thread's A elements are whole bytes of its own
-// 32-byte span of the key row: logical k = 2t + j (+ 8 h) of k-step ks is
-// dimension 32 t + 4 ks + 2 h + j.  The queries take the same order (in f16)
-// and the side cache's scale multiplies the scores.
+// With F8 (FOLD with an FP8 side cache) a far piece's QK^T is an f16 MMA:
+// E4M3 codes widen exactly to f16 pairs, and the k order inside each k-step is
+// permuted so that a thread's A elements are whole bytes of its own span of
+// SP = D/4 bytes of the key row: logical k = 2t + j (+ 8 h) of k-step ks is
+// dimension SP t + 4 ks + 2 h + j.  The queries take the same order (in f16)
+// and the side cache's scale multiplies the scores.  Key rows are 128-byte
+// swizzled (d 128) or 64-byte unswizzled (d 64).
 template <int D, int NT, bool SPLIT_PAGES, bool F8 = false>
 struct MmaEngine {
   static constexpr bool kPairs = false;
   static constexpr bool kPingPong = false;
   static constexpr bool kSideF8 = F8;
   static constexpr bool kFarScaleInQ = !F8;   // F8: the scale goes on the scores
-  static_assert(!F8 || D == 128, "FP8 side cache: head_dim 128");
+  static_assert(D == 128 || D == 64, "head_dim");
   static constexpr int NCW = 8;
   static constexpr int NCT = NCW * 32;
   static constexpr int RK = SPLIT_PAGES ? 8 * NT : 16 * NT;
@@ -869,7 +875,7 @@ struct MmaEngine {
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float* qr = s.q + (row0 + 8 * nt + g) * D + 32 * t + 4 * ks;
+        const float* qr = s.q + (row0 + 8 * nt + g) * D + (D / 4) * t + 4 * ks;
         qf[ks][nt][0] = pack_f16(qr[0], qr[1]);
         qf[ks][nt][1] = pack_f16(qr[2], qr[3]);
       }
@@ -887,15 +893,20 @@ struct MmaEngine {
 #pragma unroll
       for (int c = 0; c < 4; ++c) S[nt][c] = 0.f;
     if constexpr (FK) {
-      // rows key0 + g and key0 + g + 8; bytes 32 t .. 32 t + 31 (chunks 2t, 2t+1)
-      uint32_t w[2][2][4];
+      // rows key0 + g and key0 + g + 8; bytes SP t .. SP t + SP - 1 (NC chunks)
+      constexpr int NC = D / 64;
+      uint32_t w[2][NC][4];
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NC; ++c) {
+          const int row = key0 + g + 8 * rh;
+          const uint32_t ad = D == 128 ? swz_addr(kbase, row, (2 * t + c) * 16)
+                                       : kbase + (uint32_t)(row * D + 16 * t);
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(w[rh][c][0]), "=r"(w[rh][c][1]), "=r"(w[rh][c][2]), "=r"(w[rh][c][3])
-                       : "r"(swz_addr(kbase, key0 + g + 8 * rh, (2 * t + c) * 16)));
+                       : "r"(ad));
+        }
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint32_t w0 = w[0][ks >> 2][ks & 3], w1 = w[1][ks >> 2][ks & 3];

@@ -199,8 +199,8 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
 // The producer warp: block-table translation and TMA issue for the CTA's
 // stretch [xs, xe) of the page line.  ES = element bytes, NCB = 128-byte
 // column boxes per row (head_dim * ES / 128).  F8: far keys come from an FP8
-// side cache, one 128-byte box per page (head_dim 128), into the stage's first
-// K box.
+// side cache, one box of 64 rows x head_dim bytes per page, into the stage's
+// first K box.
 template <int ES, int NCB, bool F8>
 __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
                                 int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
@@ -266,7 +266,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
             const int32_t y = (jphys * a.H_kv + jh) * kPage;
             const int32_t yk = (jkphys * a.H_kv + jh) * kPage;
             if (F8 && jfar) {
-              mbar_arrive_expect_tx(&s.full[st], (NCB + 1) * kBoxBytes);
+              mbar_arrive_expect_tx(&s.full[st], NCB * kBoxBytes + kPage * (NCB * kSwizzleRow / ES));
               tma_load_2d(kdst, ms, 0, yk, &s.full[st], pol);
 #pragma unroll
               for (int cb = 0; cb < NCB; ++cb)

@@ -155,9 +155,9 @@ typedef struct {
                                 to even, saturating at +-448; the far memory reads
                                 code value * side_scale.  Halves the side cache
                                 against bf16 (the FOLD page gives no format for
-                                it).  Needs bf16 and head_dim 128.  Runs on the
-                                tensor-core engine unless engine = 1 forces the
-                                CUDA cores (then at most 4 rows per KV head;
+                                it).  Needs bf16.  Runs on the tensor-core
+                                engine unless engine = 1 forces the CUDA cores
+                                (then at most 4 rows per KV head;
                                 DA_ERR_UNSUPPORTED otherwise).                   */
   float   side_scale;        /* > 0 and finite with side_fp8 = 1, else 0           */
   int32_t reserved[2];       /* must be zero                                       */

@@ -70,7 +70,7 @@ def _ok_params(**kw):
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_scale=1.0), -1),
     (dict(mode="window", window=200, side_fp8=1, side_scale=1.0), -1),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
-          head_dim=64), -2),
+          head_dim=64), 0),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,
           dtype="fp32"), -2),
     (dict(mode="fold", window=200, alpha=2.0, far_mix=0.5, side_fp8=1, side_scale=1.0,

@@ -67,6 +67,26 @@ def test_fold_fp8_parity(shape, kw, engine):
     s.close()
 
 
+@pytest.mark.parametrize("shape,engine", [((8, 8, 1), "cuda_core"), ((32, 8, 1), "cuda_core"),
+                                          ((32, 8, 1), "auto"), ((64, 8, 1), "auto"),
+                                          ((32, 8, 8), "auto")],
+                         ids=["r1-core", "r4-core", "r4-mma", "r8-mma", "r32-mma"])
+def test_fold_fp8_head_dim_64(shape, engine):
+    """64-byte E4M3 key rows (unswizzled): the append's bytes and the attention
+    against the oracle on both engines."""
+    h, hk, nq = shape
+    s = Setup(batch=2, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=64, dtype="bf16",
+              ctx=[2600, 300], mode="fold", window=200, n_sink=4, alpha=2.0, far_mix=0.5,
+              seed=39, side_fp8_scale=1 / 32, engine=engine)
+    torch.cuda.synchronize()
+    for b, L in enumerate(s.ctx):
+        np.testing.assert_array_equal(
+            _side_bytes(s, b, L), orc.side_fp8_codes(s.k_raw[b][:L].float().cpu().numpy(), 1 / 32))
+    compare(s.run(), s.oracle(), "bf16", f"fold fp8 d64 {shape} {engine}")
+    assert s.status() == (B.DA_OK, 0)
+    s.close()
+
+
 @pytest.mark.parametrize("h,engine", [(32, "cuda_core"), (64, "auto"), (32, "auto")],
                          ids=["r4-core", "r8-mma", "r4-mma"])
 def test_fold_fp8_saturating_scale(h, engine):
