@@ -818,16 +818,42 @@ def profile_loop(args):
         wl = WL.resized(wl, args.ctx)
     dl = DraftLoop(wl, dev, (args.profile_loop,))
     torch.cuda.synchronize()
-    torch.cuda.profiler.start()   # with ncu --profile-from-start off: the loop only
-    for _ in range(args.reps):
-        dl.loop(args.profile_loop)
-    torch.cuda.synchronize()
-    torch.cuda.profiler.stop()
-    code, bits = dl.plans[args.profile_loop].status()
+    if args.side_fp8:
+        # FOLD with the side cache as E4M3 codes: the attention call on the first
+        # draft step's inputs, `reps` times (set-up converts the side cache)
+        if args.profile_loop != "fold":
+            raise SystemExit("--side-fp8 needs --profile-loop fold")
+        scale = 1.0 / 64
+        da = B.DraftAttention(
+            device=0, batch=wl.batch, n_q=wl.n_q, num_q_heads=wl.num_q_heads,
+            num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_pages=dl.npg,
+            max_pages_per_seq=dl.bt.shape[1], dtype=wl.dtype, mode="fold", window=wl.window,
+            alpha=wl.alpha, far_mix=wl.far_mix, rope_theta=wl.rope_theta, side_fp8=1,
+            side_scale=scale)
+        ks8 = torch.empty(dl.k_side.shape, dtype=torch.uint8, device=dev)
+        for i in range(0, dl.k_side.shape[0], 1024):
+            ks8[i:i + 1024] = (dl.k_side[i:i + 1024].float() / scale).to(
+                torch.float8_e4m3fn).view(torch.uint8)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        for _ in range(args.reps):
+            da.run(dl.q[0], dl.qpos[0], dl.lens[0], dl.bt, dl.k_cache, dl.v_cache, ks8, out=dl.out)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        code, bits = da.status()
+        da.close()
+    else:
+        torch.cuda.profiler.start()   # with ncu --profile-from-start off: the loop only
+        for _ in range(args.reps):
+            dl.loop(args.profile_loop)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        code, bits = dl.plans[args.profile_loop].status()
     dl.close()
     if code != B.DA_OK:
         raise SystemExit(f"device status {bits:#x}")
-    print(f"profile loop ok: {wl.name} ctx={wl.ctx[0]} mode={args.profile_loop} reps={args.reps}")
+    print(f"profile loop ok: {wl.name} ctx={wl.ctx[0]} mode={args.profile_loop} reps={args.reps}"
+          + (" side_fp8" if args.side_fp8 else ""))
 
 
 def main():
@@ -846,6 +872,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--ctx", type=int, default=0, help="override the workload's context")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--side-fp8", action="store_true",
+                    help="with --profile-loop fold: the attention call over an E4M3 side cache")
     args = ap.parse_args()
     if args.profile_loop:
         profile_loop(args)
