@@ -148,7 +148,8 @@ typedef struct {
                                 cover every sequence (batch = params.batch), and
                                 one call must not hold two positions of pages
                                 >= S that are (R - S) * 64 apart (they would
-                                share a slot).                                   */
+                                share a slot).  draft_attn_ring_size(window,
+                                n_sink) gives the smallest R.                    */
   int32_t side_fp8;          /* FOLD only: 0 = k_side in dtype; 1 = k_side as FP8
                                 E4M3 codes (one byte per element) of the float32
                                 quotient k / side_scale, rounded to nearest, ties

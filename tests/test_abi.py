@@ -143,3 +143,13 @@ def test_struct_layout_matches_header(tmp_path):
             B.da_params.reserved.offset, ctypes.sizeof(B.da_plan_info),
             B.da_plan_info.workspace_bytes.offset]
     assert [int(x) for x in got] == want
+
+
+@pytest.mark.parametrize("W,ns", [(2048, 0), (200, 4), (200, 70), (130, 0), (64, 64)])
+def test_ring_size_is_the_smallest_fold_k_ring(W, ns):
+    """draft_attn_ring_size gives the smallest k_ring_pages FOLD accepts."""
+    n_ring, _ = B.draft_attn_ring_size(W, ns)
+    p = _ok_params(mode="fold", window=W, n_sink=ns, alpha=2.0, far_mix=0.5, k_ring_pages=n_ring)
+    assert B.draft_attn_check_params(p) == 0
+    p.k_ring_pages = n_ring - 1
+    assert B.draft_attn_check_params(p) == -1
