@@ -100,6 +100,21 @@ def test_fold_4x256k(mode):
     s.close()
 
 
+@pytest.mark.parametrize("engine", ["auto", "cuda_core"])
+def test_fold_4x256k_fp8_side_cache(engine):
+    """The FOLD workload with its side cache as E4M3 codes (scale 1/64), in the
+    configurations the benchmark times: the append writes the codes, sampled
+    outputs match the oracle, which quantises the far keys the same way."""
+    wl = WL.WORKLOADS["fold_4x256k"]
+    s = _setup(wl, "fold", side_fp8_scale=1 / 64, engine=engine)
+    assert s.da.info()["engine_name"] == ("mma" if engine == "auto" else "cuda_core")
+    out = s.run()
+    groups = sample_groups(wl.batch, wl.n_q, wl.num_kv_heads, 4, 37)
+    compare(out, s.oracle(groups), wl.dtype, f"fold_4x256k fp8 {engine}")
+    assert s.status() == (B.DA_OK, 0)
+    s.close()
+
+
 @pytest.mark.parametrize("mode", ["full", "window", "sharp"])
 def test_ragged_tree_16x8(mode):
     wl = WL.WORKLOADS["ragged_tree_16x8"]
