@@ -153,3 +153,10 @@ def test_ring_size_is_the_smallest_fold_k_ring(W, ns):
     assert B.draft_attn_check_params(p) == 0
     p.k_ring_pages = n_ring - 1
     assert B.draft_attn_check_params(p) == -1
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No CPU or PyTorch fallback: without the built library, loading raises."""
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(ImportError, match="no CPU or PyTorch fallback"):
+        B.load_library(str(tmp_path / "libdraft_attn.so"))
