@@ -44,7 +44,8 @@
  *                k_cache holds keys rotated at their own positions, k_side
  *                the same keys un-rotated (FOLD only), v_cache the values.
  *                With side_fp8 = 1, k_side holds one byte per element: the
- *                FP8 E4M3 code of k / side_scale.
+ *                FP8 E4M3 code of k / side_scale.  With k_ring_pages = R,
+ *                k_cache is [batch * R][num_kv_heads][page_size][head_dim].
  *   block_table  int32 [batch][max_pages_per_seq]; logical page j of sequence
  *                b lives in physical page block_table[b][j].
  *   ctx_lens     int32 [batch]: keys 0 .. ctx_lens[b]-1 are visible.
