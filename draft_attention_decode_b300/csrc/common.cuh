@@ -360,6 +360,15 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int byte) {
   return base + box * kBoxBytes + row * kSwizzleRow + ((chunk ^ (row & 7)) << 4) + (byte & 15);
 }
 
+// swz_addr of byte 32 ks + b0 (b0 < 32) of a row, from the address a0 of byte
+// b0: inside a row, 16-byte chunk 2 ks' + (b0 / 16) sits at that chunk XOR the
+// row's swizzle, i.e. a0's chunk XOR 2 ks', with ks' = ks mod 4 (bits 5-6 of
+// the address, all zero in the 1024-byte-aligned stage base and row offset);
+// every 4 steps move to the next 128-byte column box.
+__device__ __forceinline__ uint32_t swz_step(uint32_t a0, int ks) {
+  return (a0 ^ ((uint32_t)(ks & 3) << 5)) + (uint32_t)(ks >> 2) * kBoxBytes;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

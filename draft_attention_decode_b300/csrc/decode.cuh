@@ -921,10 +921,11 @@ struct MmaEngine {
         for (int c = 0; c < 4; ++c) S[nt][c] *= kscale;
     } else {
       const int krow = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t ka0 = swz_addr(kbase, krow, (lane >> 4) * 16);   // k-step 0
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t a[4];
-        ldsm_x4(swz_addr(kbase, krow, (16 * ks + (lane >> 4) * 8) * 2), a);
+        ldsm_x4(swz_step(ka0, ks), a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_bf16(S[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
       }
@@ -993,10 +994,11 @@ struct MmaEngine {
       mask23 = (ok(k2 + 8) ? 0x0000ffffu : 0u) | (ok(k2 + 9) ? 0xffff0000u : 0u);
     }
     const int vrow = key0 + (lane & 7) + (lane >> 4) * 8;
+    const uint32_t va0 = swz_addr(vbase, vrow, ((lane >> 3) & 1) * 16);   // m-tile 0
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t a[4];
-      ldsm_x4_t(swz_addr(vbase, vrow, (16 * mt + ((lane >> 3) & 1) * 8) * 2), a);
+      ldsm_x4_t(swz_step(va0, mt), a);
       a[0] &= mask01; a[1] &= mask01; a[2] &= mask23; a[3] &= mask23;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_bf16(O[mt][nt], a, bp[nt][0], bp[nt][1]);
