@@ -359,9 +359,17 @@ struct CoreEngine {
                                         const uint32_t (&vb)[NP], const int (&lo)[NP],
                                         const int (&hi)[NP], const int (&toff)[NP]) {
     constexpr int NIT = PP * NP;
+    // With 4 rows two passes share one reduce-scatter (8 values over the 8
+    // lanes of a key group): lane ds then holds row ds & 3 of pass
+    // 2 j + (ds >> 2), no lane duplicates another, and a lane keeps NIT / 2
+    // scores.  Fewer rows keep one reduce-scatter per pass.
+    constexpr bool PAIR = RK == 4;
+    static_assert(!PAIR || (PP % 2 == 0), "paired passes stay inside a page");
+    constexpr int NS = PAIR ? NIT / 2 : NIT;   // scores per lane
     const int kw = (warp & (GW - 1)) * KPW + kg;   // the lane's key on pass 0
-    float sc[NIT];
+    float sc[NS];
     bool ok[NIT];
+    float vp[PAIR ? 2 * RK : 1];   // PAIR: the even pass's partial sums
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int pg = it / PP, ps = it % PP;
@@ -420,8 +428,19 @@ struct CoreEngine {
         if constexpr (NA == 2) t = make_float2(t.x + acc[1][r].x, t.y + acc[1][r].y);
         v[r] = t.x + t.y;
       }
-      const float sr = reduce_scatter<RK, LPK>(v, ds);
-      sc[it] = ok[it] ? sr : -INFINITY;
+      if constexpr (PAIR) {
+#pragma unroll
+        for (int r = 0; r < RK; ++r) vp[(it & 1) * RK + r] = v[r];
+        if (it & 1) sc[it >> 1] = reduce_scatter<2 * RK, LPK>(vp, ds);
+      } else {
+        const float sr = reduce_scatter<RK, LPK>(v, ds);
+        sc[it] = ok[it] ? sr : -INFINITY;
+      }
+    }
+    if constexpr (PAIR) {
+#pragma unroll
+      for (int j = 0; j < NS; ++j)
+        if (!((ds & 4) ? ok[2 * j + 1] : ok[2 * j])) sc[j] = -INFINITY;
     }
     // Draft-tree keys the row does not see (only pages that hold tree keys).
     bool has_tree = false;
@@ -430,15 +449,19 @@ struct CoreEngine {
     if (has_tree) {
       const uint64_t tm = s.tmask[ds & (RK - 1)];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it)
-        if (!tree_visible(kw + KG * (it % PP), toff[it / PP], tm)) sc[it] = -INFINITY;
+      for (int j = 0; j < NS; ++j) {
+        const int it = PAIR ? 2 * j + (ds >> 2) : j;   // the pass of the lane's key
+        if (!tree_visible(kw + KG * (it % PP), toff[(PAIR ? 2 * j : j) / PP], tm))
+          sc[j] = -INFINITY;
+      }
     }
-    // Row maximum over the warp's keys (lanes with the same ds).
+    // Row maximum over the warp's keys (lanes holding the same row).
     float mx = sc[0];
 #pragma unroll
-    for (int it = 1; it < NIT; ++it) mx = fmaxf(mx, sc[it]);
+    for (int j = 1; j < NS; ++j) mx = fmaxf(mx, sc[j]);
 #pragma unroll
-    for (int m = LPK; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    for (int m = PAIR ? RK : LPK; m < 32; m <<= 1)
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
     const bool raise = mx > m_run + kLazy;
     if (__any_sync(0xffffffffu, raise)) {
       const float m_new = raise ? mx : m_run;
@@ -455,11 +478,11 @@ struct CoreEngine {
         }
       }
     }
-    float p[NIT];
+    float p[NS];
 #pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-      p[it] = sc[it] > -INFINITY ? fast_exp2(sc[it] - m_run) : 0.f;
-      l_run += p[it];
+    for (int j = 0; j < NS; ++j) {
+      p[j] = sc[j] > -INFINITY ? fast_exp2(sc[j] - m_run) : 0.f;
+      l_run += p[j];
     }
     // PV in the QK^T layout.  A key outside [lo, hi) may hold anything, NaN
     // included: it reads the zeroed chunk instead (its probability is 0).
@@ -469,7 +492,8 @@ struct CoreEngine {
       float pr[RK];
 #pragma unroll
       for (int r = 0; r < RK; ++r)
-        pr[r] = __shfl_sync(0xffffffffu, p[it], (lane & ~(LPK - 1)) | r);
+        pr[r] = PAIR ? __shfl_sync(0xffffffffu, p[it >> 1], (lane & ~(LPK - 1)) | r | ((it & 1) << 2))
+                     : __shfl_sync(0xffffffffu, p[it], (lane & ~(LPK - 1)) | r);
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         float f[EPC];
@@ -496,8 +520,9 @@ struct CoreEngine {
   // Sum the key groups, merge the consumer warps, write the piece's partial.
   __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
     float lt = l_run;
+    // with 4 rows lanes ds and ds ^ 4 hold one row's sums over different keys
 #pragma unroll
-    for (int m = LPK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
+    for (int m = RK == 4 ? RK : LPK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
     if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
 #pragma unroll
     for (int r = 0; r < RK; ++r)
