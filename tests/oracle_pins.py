@@ -354,6 +354,8 @@ def check_tree_masks(orc):
     for mode, kw, bkw in (("full", {}, {}), ("window", dict(window=12, n_sink=2), dict(W=12, n_sink=2)),
                           ("fold", dict(window=10, alpha=2.0, far_mix=0.3),
                            dict(W=10, alpha=2.0, lam=0.3)),
+                          ("fold", dict(window=10, n_sink=3, alpha=2.0, far_mix=0.3),
+                           dict(W=10, n_sink=3, alpha=2.0, lam=0.3)),
                           ("sharp", dict(scale_slope=0.4, scale_ref=8), dict(beta=0.4, n_ref=8))):
         for mask in (0b101001, 0b1, 0b111111, 0):
             prm = orc.Params(mode=mode, n_tree=nt, rope_theta=1e4, **kw)
