@@ -438,7 +438,67 @@ def check_e4m3(orc):
         assert np.array_equal(orc.side_fp8_keys(k, s), np.array(want)), s
 
 
+def check_append_rotated_keys(orc):
+    """The rotated cache's keys: every (token, head) against the complex form
+    at its own position, for a [B, n_new, H_kv, d] append with positions
+    [B, n_new] near the ends of the workloads' ranges."""
+    rng = np.random.default_rng(31)
+    positions = [[0, 4095, 4096], [131075, 1048581, 63]]
+    for theta in (1e4, 1e6):
+        k = rng.standard_normal((2, 3, 4, 16))
+        got = orc.append_rotated_keys(k, np.array(positions), theta)
+        assert got.shape == k.shape
+        for b in range(2):
+            for t in range(3):
+                for h in range(4):
+                    want = bf_rope(list(k[b, t, h]), positions[b][t], theta)
+                    assert np.max(np.abs(got[b, t, h] - np.array(want))) < 1e-9, (theta, b, t, h)
+    # one token, one head: the same single rotation
+    k1 = rng.standard_normal((1, 1, 1, 8))
+    got = orc.append_rotated_keys(k1, np.array([[7]]), 1e4)[0, 0, 0]
+    assert np.max(np.abs(got - np.array(bf_rope(list(k1[0, 0, 0]), 7, 1e4)))) < 1e-12
+
+
+def check_chunked_paths(orc):
+    """The oracle walks long selections in chunks of keys.  With chunks far
+    smaller than the selection (7, 16 and 64 keys, so that every case crosses
+    several chunk boundaries, ragged tail included) the result must still be
+    the brute-force one, in every mode."""
+    rng = np.random.default_rng(37)
+    d = 8
+    configs = [
+        dict(mode="full", L=37), dict(mode="window", L=50, W=16, n_sink=3),
+        dict(mode="window", L=58, W=40, n_sink=9),
+        dict(mode="fold", L=45, W=12, alpha=2.0, lam=0.5),
+        dict(mode="fold", L=45, W=12, n_sink=4, alpha=2.0, lam=0.5),
+        dict(mode="fold", L=52, W=9, n_sink=3, alpha=2.0, lam=0.5, fp8=0.004),
+        dict(mode="sharp", L=60, beta=0.4, n_ref=8),
+        dict(mode="full", L=200, chunks=(64,)), dict(mode="fold", L=200, W=70, alpha=1.5,
+                                                     lam=0.4, chunks=(64,)),
+    ]
+    for cfg in configs:
+        L = cfg["L"]
+        K = rng.standard_normal((L, d))
+        V = rng.standard_normal((L, d))
+        q = rng.standard_normal((2, d))
+        p = L + 1
+        s8 = cfg.get("fp8", 0.0)
+        prm = orc.Params(mode=cfg["mode"], window=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
+                         alpha=cfg.get("alpha", 1.0), far_mix=cfg.get("lam", 0.0),
+                         scale_slope=cfg.get("beta", 0.0), scale_ref=cfg.get("n_ref", 4096),
+                         rope_theta=1e4, side_fp8_scale=s8)
+        want = [bf_attend_row(cfg["mode"], list(q[r]), p, K.tolist(), V.tolist(), L,
+                              W=cfg.get("W", 0), n_sink=cfg.get("n_sink", 0),
+                              alpha=cfg.get("alpha", 1.0), lam=cfg.get("lam", 0.0),
+                              beta=cfg.get("beta", 0.0), n_ref=cfg.get("n_ref", 4096),
+                              far_key=(lambda k: bf_side_fp8(k, s8)) if s8 else None)[0]
+                for r in range(2)]
+        for chunk in cfg.get("chunks", (7, 16)):
+            got = orc.attend_group(q, p, K, V, L, prm, chunk=chunk)
+            assert np.max(np.abs(got - np.array(want))) < 1e-12, (cfg, chunk)
+
+
 ALL_CHECKS = [check_e4m3, check_tree_masks, check_nope, check_rope_complex, check_rope_d2, check_inv_freq, check_selection,
               check_brute_force, check_closed_forms, check_weights_sum,
               check_mode_equivalences, check_fold_shared_position, check_gqa,
-              check_page_slot]
+              check_page_slot, check_append_rotated_keys, check_chunked_paths]

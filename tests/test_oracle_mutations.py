@@ -76,6 +76,53 @@ def _e4m3_no_saturation(x):
 def _side_fp8_unscaled(k_raw, scale):
     return orc.e4m3_decode(orc.side_fp8_codes(k_raw, scale))
 
+
+def _logits_chunk_positions_restart(q_rot, k_raw, key_pos, theta, chunk):
+    # every chunk after the first takes the first chunk's key positions
+    n = k_raw.shape[0]
+    out = np.empty((n, q_rot.shape[0]), dtype=np.float64)
+    key_pos = np.broadcast_to(np.asarray(key_pos, dtype=np.int64), (n,))
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        kr = orc.rope(np.asarray(k_raw[a:b], dtype=np.float64), key_pos[0:b - a], theta)
+        out[a:b] = kr @ q_rot.T
+    return out
+
+
+def _logits_chunk_shifted(q_rot, k_raw, key_pos, theta, chunk):
+    # the keys of chunk c are written one row late (an off-by-one slice)
+    n = k_raw.shape[0]
+    out = np.zeros((n, q_rot.shape[0]), dtype=np.float64)
+    key_pos = np.broadcast_to(np.asarray(key_pos, dtype=np.int64), (n,))
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        kr = orc.rope(np.asarray(k_raw[a:b], dtype=np.float64), key_pos[a:b], theta)
+        lo = a + 1 if a else a
+        out[lo:b] = (kr @ q_rot.T)[: b - lo]
+    return out
+
+
+def _weighted_sum_chunk_values_restart(w, v, chunk):
+    # every chunk's weights meet the first chunk's values
+    o = np.zeros((w.shape[1], v.shape[1]), dtype=np.float64)
+    for a in range(0, w.shape[0], chunk):
+        b = min(w.shape[0], a + chunk)
+        o += w[a:b].T @ np.asarray(v[0:b - a], dtype=np.float64)
+    return o
+
+
+def _append_at_next_position(k_new, pos, theta):
+    return orc.rope(np.asarray(k_new, dtype=np.float64),
+                    np.asarray(pos, dtype=np.int64)[..., None] + 1, theta)
+
+
+def _append_pos_wrong_axis(k_new, pos, theta):
+    # positions broadcast over the head axis instead of the token axis
+    k = np.asarray(k_new, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.int64)
+    p = np.resize(pos.reshape(-1), k.shape[:-1])
+    return orc.rope(k, p, theta)
+
 MUTATIONS = {
     "rope_sign": ("rope", _rope_sign),
     "rope_pairing": ("rope", _rope_adjacent_pairs),
@@ -104,6 +151,11 @@ MUTATIONS = {
                              lambda pos, bt, P=64: (np.asarray(bt)[np.asarray(pos) % P],
                                                     np.asarray(pos) // P,
                                                     np.asarray(bt)[np.asarray(pos) % P] * P + np.asarray(pos) // P)),
+    "logits_chunk_positions_restart": ("_logits", _logits_chunk_positions_restart),
+    "logits_chunk_off_by_one": ("_logits", _logits_chunk_shifted),
+    "weighted_sum_chunk_values_restart": ("_weighted_sum", _weighted_sum_chunk_values_restart),
+    "append_at_next_position": ("append_rotated_keys", _append_at_next_position),
+    "append_pos_wrong_axis": ("append_rotated_keys", _append_pos_wrong_axis),
 }
 
 
