@@ -52,6 +52,8 @@ from draft_attention_decode_b300 import workloads as WL  # noqa: E402
 METRIC = "draft-step attention µs and KV GB/s (% of HBM peak) vs context, full vs window"
 HEADLINE = "mtp_draft_128k"
 FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure the fractions are also quoted against
+MIN_REPLAYS = 50           # tables report the median of at least this many replays
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -330,6 +332,18 @@ def time_graph(g, steps, warmup, flush, dist, stream=None):
     return dist.max(sum(ms) / len(ms)), ms
 
 
+def median_replay(g, steps, warmup, flush, dist):
+    """Median ms of at least MIN_REPLAYS timed replays (max over ranks)."""
+    _, ms = time_graph(g, max(steps, MIN_REPLAYS), warmup, flush, dist)
+    return dist.max(statistics.median(ms))
+
+
+def rates(nbytes, ms, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kv_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
 def time_calls(fn, steps, warmup, flush, dist):
     """Like time_graph for an un-captured callable (the per-launch roofline
     timing of the attention call)."""
@@ -347,99 +361,187 @@ def time_calls(fn, steps, warmup, flush, dist):
         ev[i][1].record(st)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
-    return dist.max(sum(ms) / len(ms))
+    return dist.max(sum(ms) / len(ms)), dist.max(statistics.median(ms))
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, k_host, v_host, q_host, L, p, groups, mode):
-    """Runs the float64 oracle for `groups` (KV-head indices) of one draft
-    step; returns the KV bytes those groups read."""
+# (workload, modes) the CPU baseline covers: every workload and mode the
+# benchmark times on the GPU.
+CPU_PLAN = (("mtp_draft_128k", ("full", "window")), ("mtp_draft_1m", ("full", "window")),
+            ("fold_4x256k", ("fold", "full", "window")),
+            ("ragged_tree_16x8", ("full", "window", "sharp")),
+            ("tiny_window_fp32", ("full", "window")))
+
+
+def host_workers():
+    """Host cores this process may run on (its CPU affinity)."""
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_params(wl, mode):
     import oracle.draft_attn_oracle as orc
-    prm = orc.Params(mode=mode, window=wl.window_for(mode), n_sink=wl.sinks_for(mode),
-                     alpha=wl.alpha, far_mix=wl.far_mix, scale_slope=wl.scale_slope,
-                     scale_ref=wl.scale_ref, rope_theta=wl.rope_theta)
-    G = wl.num_q_heads // wl.num_kv_heads
-    es = 2 if wl.dtype == "bf16" else 4
-    nbytes = 0
-    for g in groups:
-        orc.attend_group(q_host[g * G:(g + 1) * G], p, k_host[g], v_host[g], L, prm)
-        nbytes += selected_keys(mode, L, prm.window, prm.n_sink) * 2 * wl.head_dim * es
-    return nbytes
+    return orc.Params(mode=mode, window=wl.window_for(mode), n_sink=wl.sinks_for(mode),
+                      alpha=wl.alpha, far_mix=wl.far_mix, scale_slope=wl.scale_slope,
+                      scale_ref=wl.scale_ref, rope_theta=wl.rope_theta)
 
 
-def host_kv(wl, L, groups, seed):
-    """Host float32 keys/values of `groups` KV heads for an L-token context
-    (seeded CPU draws: same shape and distribution as the GPU workload)."""
+def step_units(wl):
+    """The work units of the workload's first draft step: one (sequence b,
+    query token t, KV head g) each, with its context length L and query
+    position p (draft loops: the first appended token, L = ctx + 1, p = ctx;
+    otherwise p = ctx + t)."""
+    units = []
+    for b, c in enumerate(wl.ctx):
+        if wl.draft_steps:
+            L, ps = c + 1, [c]
+        else:
+            L, ps = c, [c + t for t in range(wl.n_q)]
+        for t, p in enumerate(ps):
+            for g in range(wl.num_kv_heads):
+                units.append((b, t, g, L, p))
+    return units
+
+
+def host_kv(wl, L, seed):
+    """Host float32 keys and values [L, d] of one KV head (seeded draws of the
+    workload's distribution, rounded to its dtype).  Every unit of a
+    workload reads this one pair (a sequence shorter than L its prefix): the
+    oracle's cost depends on the shapes only."""
     dt = wl.torch_dtype
-    k = {g: WL.randn((L, wl.head_dim), dt, "cpu", seed * 16 + 2 + 97 * g).float().numpy()
-         for g in groups}
-    v = {g: WL.randn((L, wl.head_dim), dt, "cpu", seed * 16 + 3 + 97 * g).float().numpy()
-         for g in groups}
-    q = WL.randn((wl.num_q_heads, wl.head_dim), dt, "cpu", seed * 16 + 1).float().numpy()
-    return k, v, q
+    k = WL.randn((L, wl.head_dim), dt, "cpu", seed * 16 + 2).float().numpy()
+    v = WL.randn((L, wl.head_dim), dt, "cpu", seed * 16 + 3).float().numpy()
+    return k, v
 
 
-def blas_threads():
+def oracle_unit_bytes(wl, mode, L):
+    es = 2 if wl.dtype == "bf16" else 4
+    return selected_keys(mode, L, wl.window_for(mode), wl.sinks_for(mode)) * 2 * wl.head_dim * es
+
+
+def run_units(wl, mode, units, kv, workers, budget_s, rng):
+    """Runs the float64 oracle over `units` on `workers` host threads (BLAS
+    held to one thread each, so the threads are the cores used), submitting
+    units until `budget_s` has passed; the ones in flight then finish.
+    Returns (KV bytes of the units done, seconds, units done)."""
+    from concurrent.futures import FIRST_COMPLETED, ThreadPoolExecutor, wait
+    import oracle.draft_attn_oracle as orc
+    prm = oracle_params(wl, mode)
+    G = wl.num_q_heads // wl.num_kv_heads
+    k, v = kv
+    qs = [rng.standard_normal((G, wl.head_dim)) for _ in range(len(units))]
+
+    def one(i):
+        b, t, g, L, p = units[i]
+        orc.attend_group(qs[i], p, k[:max(L, 1)], v[:max(L, 1)], L, prm)
+        return oracle_unit_bytes(wl, mode, L)
+
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
+        from threadpoolctl import threadpool_limits
+        limit = threadpool_limits(limits=1, user_api="blas")
     except Exception:
-        return 1
+        limit = None
+    nbytes, n_done, nxt = 0, 0, 0
+    try:
+        with ThreadPoolExecutor(workers) as ex:
+            t0 = time.perf_counter()
+            running = set()
+            while True:
+                while (len(running) < workers and nxt < len(units)
+                       and time.perf_counter() - t0 < budget_s):
+                    running.add(ex.submit(one, nxt))
+                    nxt += 1
+                if not running:
+                    break
+                done, running = wait(running, return_when=FIRST_COMPLETED)
+                for f in done:
+                    nbytes += f.result()
+                    n_done += 1
+            dt = time.perf_counter() - t0
+    finally:
+        if limit is not None:
+            limit.unregister()
+    return nbytes, dt, n_done
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """The oracle as it stands, timed on the host on a bounded sample of the
-    headline workload: KV-head groups of its first draft step in full mode,
-    until `budget_s` seconds have passed."""
-    L = wl.ctx[0] + 1
-    p = wl.ctx[0]
-    groups = list(range(wl.num_kv_heads))
-    k, v, q = host_kv(wl, L, groups, wl.seed)
-    done, nbytes = [], 0
-    t0 = time.perf_counter()
-    for g in groups:
-        nbytes += oracle_sample(wl, k, v, q, L, p, [g], "full")
-        done.append(g)
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s",
-            "cores": blas_threads(), "kind": "oracle",
-            "sample": f"full mode, first draft step (L={L}), {len(done)} of "
-                      f"{wl.num_kv_heads} KV-head groups ({wl.num_q_heads // wl.num_kv_heads} "
-                      f"query rows each), float64 numpy, {dt:.1f} s",
-            "host_cpus": len(os.sched_getaffinity(0))}
+def cpu_baseline(budget_s=2.0):
+    """The oracle as it stands, timed on the host cores, on a bounded sample of
+    every workload and mode the benchmark times: the units (sequence, query
+    token, KV head) of each workload's first draft step, in a seeded order,
+    on one thread per host core, until `budget_s` per workload and mode (the
+    units in flight then finish).  The headline entry is the 128K workload's
+    full mode (the line's own metric and workload)."""
+    workers = host_workers()
+    rng = np.random.default_rng(0)
+    rows = []
+    for name, modes in CPU_PLAN:
+        wl = WL.WORKLOADS[name]
+        units = step_units(wl)
+        kv = host_kv(wl, max(u[3] for u in units), wl.seed)
+        order = rng.permutation(len(units))
+        units = [units[i] for i in order]
+        for mode in modes:
+            nbytes, dt, n_done = run_units(wl, mode, units, kv, workers, budget_s, rng)
+            step_bytes = sum(oracle_unit_bytes(wl, mode, u[3]) for u in units)
+            rate = nbytes / dt
+            rows.append({"workload": name, "mode": mode, "gbs": round(rate / 1e9, 4),
+                         "s_per_draft_step": round(step_bytes / rate, 3),
+                         "units_timed": n_done, "units_per_step": len(units),
+                         "seconds": round(dt, 2)})
+        del kv
+    head = next(r for r in rows if r["workload"] == HEADLINE and r["mode"] == "full")
+    return {"value": head["gbs"], "unit": "GB/s", "cores": workers, "kind": "oracle",
+            "sample": (f"float64 numpy oracle, one thread per host core ({workers}, BLAS at one "
+                       f"thread each); per workload and mode, units (sequence, query token, KV "
+                       f"head) of its first draft step in a seeded order until {budget_s:g} s "
+                       f"had passed (units in flight then finished); headline = "
+                       f"{HEADLINE} full mode: {head['units_timed']} of "
+                       f"{head['units_per_step']} units"),
+            "per_workload": rows, "cpu_model": cpu_model()}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def run_reference(args, dist):
-    """--impl reference: the oracle on the host cores, same metric/config."""
+    """--impl reference: the oracle on the host cores, same metric/config.
+    Each step is one whole full-mode draft step of the 128K workload (its
+    eight KV-head groups, one per host thread)."""
     if dist.rank != 0:
         return
     wl = WL.WORKLOADS[HEADLINE]
-    L = wl.ctx[0] + 1
-    groups = [0, 1]
-    k, v, q = host_kv(wl, L, groups, wl.seed)
+    units = step_units(wl)
+    kv = host_kv(wl, units[0][3], wl.seed)
+    workers = host_workers()
+    rng = np.random.default_rng(0)
     for _ in range(args.warmup):
-        oracle_sample(wl, k, v, q, L, wl.ctx[0], groups[:1], "full")
-    nbytes = 0
-    t0 = time.perf_counter()
+        run_units(wl, "full", units, kv, workers, 1e9, rng)
+    nbytes, dt = 0, 0.0
     for _ in range(args.steps):
-        nbytes += oracle_sample(wl, k, v, q, L, wl.ctx[0], groups, "full")
-    dt = time.perf_counter() - t0
+        b, t, _ = run_units(wl, "full", units, kv, workers, 1e9, rng)
+        nbytes += b
+        dt += t
     val = nbytes / dt / 1e9
-    sample = (f"each step: 2 of 8 KV-head groups of one full-mode draft step at L={L} "
-              f"(float64 numpy oracle)")
+    sample = (f"each step: one whole full-mode draft step at L={units[0][3]} (all "
+              f"{len(units)} KV-head groups), float64 numpy oracle, one thread per host "
+              f"core ({workers}, BLAS at one thread each)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, "full"),
-        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": blas_threads(),
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": workers,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -533,41 +635,47 @@ def run_ours(args, dist):
     res = {}
     torch.cuda.profiler.start()   # profilers started with capture off see only this region
     for m in ("full", "window"):
-        ms, _ = time_graph(graphs[m], args.steps, args.warmup, flush, dist)
+        ms, all_ms = time_graph(graphs[m], args.steps, args.warmup, flush, dist)
+        med = dist.max(statistics.median(all_ms))
         nbytes = dl.kv_bytes(m)
         res[m] = {"ms_per_loop": ms, "us_per_draft_step": ms * 1e3 / dl.steps,
+                  "us_per_draft_step_median": med * 1e3 / dl.steps,
                   "kv_bytes_per_loop": nbytes, "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
-                  "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+                  "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+                  "frac_of_nominal": nbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
     torch.cuda.profiler.stop()
     clk = clocks.stop()
     # the same loops with a separate append launch per draft step
     two = {}
     for m in ("full", "window"):
         g2 = dl.capture(m, fused=False)
-        ms, _ = time_graph(g2, args.steps, args.warmup, flush, dist)
+        ms = median_replay(g2, args.steps, args.warmup, flush, dist)
         two[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 3),
-                  "kv_gbs": round(dl.kv_bytes(m) / (ms * 1e-3) / 1e9, 1)}
+                  **rates(dl.kv_bytes(m), ms, peak)}
         del g2
 
     # roofline of the dominant kernel: the full-mode attention call of the
     # last draft step, timed on its own launch stream
     Lr = dl.lens[-1]
-    ms_call = time_calls(lambda: dl.plans["full"].run(dl.q[-1], dl.qpos[-1], Lr, dl.bt,
-                                                      dl.k_cache, dl.v_cache, None, out=dl.out),
-                         max(args.steps, 10), args.warmup, flush, dist)
+    ms_call, ms_call_med = time_calls(
+        lambda: dl.plans["full"].run(dl.q[-1], dl.qpos[-1], Lr, dl.bt, dl.k_cache, dl.v_cache,
+                                     None, out=dl.out),
+        max(args.steps, MIN_REPLAYS), args.warmup, flush, dist)
     call_bytes = wl.batch * int(Lr[0]) * 2 * wl.num_kv_heads * wl.head_dim * 2
     achieved = call_bytes / (ms_call * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                 "kernel": f"decode_kernel (one draft_attn_run, full mode, L={int(Lr[0])})",
                 "bytes_per_launch": call_bytes, "us_per_launch": round(ms_call * 1e3, 2),
+                "us_per_launch_median": round(ms_call_med * 1e3, 2),
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs copy bandwidth)"}
 
     # the 4-row shape on the tensor cores (an n8 tile half padding), for comparison
     mma = dl._plan("full", engine="mma")
-    ms_mma = time_calls(lambda: mma.run(dl.q[-1], dl.qpos[-1], Lr, dl.bt, dl.k_cache, dl.v_cache,
-                                        None, out=dl.out), max(args.steps, 10), args.warmup,
-                        flush, dist)
+    ms_mma, _ = time_calls(lambda: mma.run(dl.q[-1], dl.qpos[-1], Lr, dl.bt, dl.k_cache,
+                                           dl.v_cache, None, out=dl.out),
+                           max(args.steps, MIN_REPLAYS), args.warmup, flush, dist)
     mma.close()
     engines = {"cuda_core_us": round(ms_call * 1e3, 2), "tensor_core_padded_us":
                round(ms_mma * 1e3, 2), "note": "attention call alone, full mode; the default "
@@ -589,7 +697,7 @@ def run_ours(args, dist):
         others.append(fold_fp8_row(dev, args, flush, dist, peak, engine="cuda_core"))
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl)
+        cpu = cpu_baseline()
     line = {
         "metric": METRIC, "value": round(res["full"]["kv_gbs"], 2), "unit": "GB/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -671,10 +779,9 @@ def context_sweep(dev, args, flush, dist, peak):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 call()
-            ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+            ms = median_replay(g, args.steps, args.warmup, flush, dist)
             nb = selected_keys(m, L, wl.window_for(m), wl.sinks_for(m)) * 2 * 8 * 128 * 2
-            row[m] = {"us": round(ms * 1e3, 2), "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-                      "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+            row[m] = {"us": round(ms * 1e3, 2), **rates(nb, ms, peak)}
         rows.append(row)
     dl.close()
     del dl
@@ -684,11 +791,9 @@ def context_sweep(dev, args, flush, dist, peak):
     loop = {"context": base.ctx[0], "draft_steps": dl.steps}
     for m in ("full", "window"):
         g = dl.capture(m)
-        ms, _ = time_graph(g, max(args.steps // 4, 10), args.warmup, flush, dist)
+        ms = median_replay(g, args.steps, args.warmup, flush, dist)
         nb = dl.kv_bytes(m)
-        loop[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 2),
-                   "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-                   "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+        loop[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 2), **rates(nb, ms, peak)}
     dl.close()
     del dl
     torch.cuda.empty_cache()
@@ -707,11 +812,10 @@ def all_workloads(dev, args, flush, dist, peak, names):
         dl = DraftLoop(wl, dev, wl.modes)
         for m in wl.modes:
             g = dl.capture(m)
-            ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+            ms = median_replay(g, args.steps, args.warmup, flush, dist)
             nb = dl.kv_bytes(m)
             table.append({"workload": name, "mode": m, "us": round(ms * 1e3, 2),
-                          "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-                          "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4)})
+                          "kv_bytes": nb, **rates(nb, ms, peak)})
         dl.close()
         del dl
         torch.cuda.empty_cache()
@@ -745,11 +849,10 @@ def fold_ring_row(dev, args, flush, dist, peak):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         call()
-    ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+    ms = median_replay(g, args.steps, args.warmup, flush, dist)
     nb = dl.kv_bytes("fold")
     row = {"workload": "fold_4x256k", "mode": "fold, rotated K in a ring", "us": round(ms * 1e3, 2),
-           "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-           "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+           "kv_bytes": nb, **rates(nb, ms, peak),
            "k_cache_bytes": kr.numel() * kr.element_size(),
            "k_cache_bytes_paged": dl.k_cache.numel() * dl.k_cache.element_size()}
     assert ring.status() == (dl.B.DA_OK, 0)
@@ -789,15 +892,14 @@ def fold_fp8_row(dev, args, flush, dist, peak, engine="auto"):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         call()
-    ms, _ = time_graph(g, max(args.steps, 20), args.warmup, flush, dist)
+    ms = median_replay(g, args.steps, args.warmup, flush, dist)
     nb = 0
     for L in dl.lens[0].cpu().tolist():
         loc = min(wl.window, L)
         nb += wl.num_kv_heads * wl.head_dim * (4 * loc + 3 * (L - loc))
     label = "fold, FP8 E4M3 side cache" + (", CUDA-core engine forced" if engine == "cuda_core" else "")
     row = {"workload": "fold_4x256k", "mode": label, "us": round(ms * 1e3, 2),
-           "kv_bytes": nb, "kv_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-           "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+           "kv_bytes": nb, **rates(nb, ms, peak),
            "side_cache_bytes": ks8.numel(),
            "side_cache_bytes_bf16": dl.k_side.numel() * dl.k_side.element_size()}
     assert f8.status() == (dl.B.DA_OK, 0)
@@ -816,6 +918,8 @@ def profile_loop(args):
     wl = WL.WORKLOADS[args.workload]
     if args.ctx:
         wl = WL.resized(wl, args.ctx)
+    if args.ctx_cap:
+        wl = WL.resized(wl, [min(c, args.ctx_cap) for c in wl.ctx])
     dl = DraftLoop(wl, dev, (args.profile_loop,))
     torch.cuda.synchronize()
     if args.side_fp8:
@@ -871,6 +975,8 @@ def main():
                     help="run the draft loop of --workload in MODE --reps times, untimed")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--ctx", type=int, default=0, help="override the workload's context")
+    ap.add_argument("--ctx-cap", type=int, default=0,
+                    help="cap every context of the workload at this length (ragged batches)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--side-fp8", action="store_true",
                     help="with --profile-loop fold: the attention call over an E4M3 side cache")

@@ -33,8 +33,8 @@ DA_STATIC_WORKSPACE_BYTES = 8 << 20
 MODES = {"full": 0, "window": 1, "fold": 2, "sharp": 3}
 DTYPES = {"bf16": 0, "fp32": 1}
 TORCH_DTYPES = {0: torch.bfloat16, 1: torch.float32}
-ENGINES = {0: "cuda_core", 1: "mma"}
-ENGINE_HINTS = {"auto": 0, "cuda_core": 1, "mma": 2}
+ENGINES = {0: "cuda_core", 1: "mma", 2: "tc05"}
+ENGINE_HINTS = {"auto": 0, "cuda_core": 1, "mma": 2, "tc05": 3}
 
 
 class DraftAttnError(RuntimeError):
@@ -71,7 +71,8 @@ class da_params(ctypes.Structure):
         ("k_ring_pages", ctypes.c_int32),
         ("side_fp8", ctypes.c_int32),
         ("side_scale", ctypes.c_float),
-        ("reserved", ctypes.c_int32 * 2),
+        ("cluster_ctas", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 
@@ -84,7 +85,7 @@ class da_plan_info(ctypes.Structure):
         ("engine", ctypes.c_int32),
         ("stages", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("cluster_ctas", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -146,7 +147,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
                 page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0,
-                k_ring_pages=0, side_fp8=0, side_scale=0.0) -> da_params:
+                k_ring_pages=0, side_fp8=0, side_scale=0.0, cluster_ctas=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -163,6 +164,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.tree_size = int(tree_size)
     p.k_ring_pages = int(k_ring_pages)
     p.side_fp8, p.side_scale = int(side_fp8), float(side_scale)
+    p.cluster_ctas = int(cluster_ctas)
     return p
 
 
@@ -218,7 +220,7 @@ def draft_attn_plan(params: da_params, device: int = 0):
 def draft_attn_plan_info(plan) -> dict:
     info = da_plan_info()
     _check(load_library().draft_attn_plan_info(plan, ctypes.byref(info)), "draft_attn_plan_info")
-    d = {f: getattr(info, f) for f, _ in info._fields_ if f != "reserved"}
+    d = {f: getattr(info, f) for f, _ in info._fields_}
     d["engine_name"] = ENGINES.get(d["engine"], "?")
     return d
 

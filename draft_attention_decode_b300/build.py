@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdraft_attn.so")
 
-SOURCES = ["api.cu", "decode.cu", "aux.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_cluster.cu", "decode_tc.cu", "aux.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -116,6 +116,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->min_pages = p.min_pages_per_cta > 0 ? p.min_pages_per_cta : da::kMinPagesPerCta;
   a->k_ring = p.k_ring_pages;
   a->k_ring_sp = p.k_ring_pages > 0 ? ring_sink_pages(p) : 0;
+  a->cluster = pl->choice.cluster;
   for (int i = 0; i < 64; ++i) a->turn_freq[i] = pl->turn_freq[i];
 }
 
@@ -165,14 +166,18 @@ int draft_attn_check_params(const da_params* p) {
   if (!(p->rope_theta >= 0.0) || !std::isfinite(p->rope_theta)) return DA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return DA_ERR_INVALID_ARG;
   if (p->num_ctas < 0 || p->num_ctas > 65535) return DA_ERR_INVALID_ARG;
-  if (p->engine < 0 || p->engine > 2) return DA_ERR_INVALID_ARG;
+  if (p->engine < 0 || p->engine > 3) return DA_ERR_INVALID_ARG;
   if (p->min_pages_per_cta < 0 || p->min_pages_per_cta > (1 << 20)) return DA_ERR_INVALID_ARG;
   if (p->stages != 0 && (p->stages < 2 || p->stages > 8)) return DA_ERR_INVALID_ARG;
   if (p->tree_size < 0 || p->tree_size > 64) return DA_ERR_INVALID_ARG;
   if (p->tree_size > 0 && (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) &&
       p->tree_size > p->window)
     return DA_ERR_INVALID_ARG;
-  if (p->reserved[0] != 0 || p->reserved[1] != 0) return DA_ERR_INVALID_ARG;
+  if (p->reserved[0] != 0) return DA_ERR_INVALID_ARG;
+  if (p->cluster_ctas < -1 || p->cluster_ctas > 16) return DA_ERR_INVALID_ARG;
+  if (p->cluster_ctas > 0 &&
+      (p->mode != DA_MODE_WINDOW || p->num_ctas != 0 || p->min_pages_per_cta != 0))
+    return DA_ERR_INVALID_ARG;
   if (p->side_fp8 != 0 && p->side_fp8 != 1) return DA_ERR_INVALID_ARG;
   if (p->side_fp8 == 1) {
     if (p->mode != DA_MODE_FOLD) return DA_ERR_INVALID_ARG;
@@ -205,6 +210,9 @@ int draft_attn_check_params(const da_params* p) {
   if (rows > 32) return DA_ERR_UNSUPPORTED;
   if (rows > 8 && (p->dtype != DA_DTYPE_BF16 || p->engine == 1)) return DA_ERR_UNSUPPORTED;
   if (p->engine == 2 && p->dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
+  if (p->engine == 3 && (p->dtype != DA_DTYPE_BF16 || p->head_dim != 128 || p->side_fp8 == 1 ||
+                         (p->stages != 0 && p->stages > 3)))
+    return DA_ERR_UNSUPPORTED;
   // the FP8 side cache (bf16 caches): the tensor-core engine, or the
   // turn-taking CUDA-core engine up to 4 rows
   if (p->side_fp8 == 1 && (p->dtype != DA_DTYPE_BF16 || (p->engine == 1 && rows > 4)))
@@ -237,6 +245,50 @@ int draft_attn_plan(const da_params* params, int device, da_plan_t* plan, size_t
     return DA_ERR_UNSUPPORTED;
   }
   if (pl->p.num_ctas == 0) pl->p.num_ctas = sms;  // one persistent CTA per SM
+  // Window mode: one cluster of CTAs per (sequence, KV head) when asked for,
+  // or, automatically, when every such cluster can be resident at once (the
+  // selection of a window is short: its latency, not the grid's reach, is
+  // what the partition has to minimise).
+  pl->choice.cluster = 0;
+  if (params->mode == DA_MODE_WINDOW && params->cluster_ctas != -1 &&
+      da::cluster_supported(pl->choice, params->dtype, params->head_dim)) {
+    const int64_t heads = (int64_t)params->batch * params->num_kv_heads;
+    const int64_t pmax = ring_sink_pages(*params) + (params->window + da::kPage - 1) / da::kPage + 1;
+    const int dt = params->dtype, hd = params->head_dim;
+    da::Choice cc = pl->choice;
+    int C = 0;
+    if (params->cluster_ctas > 0) {
+      if (!da::fit_cluster(&cc, dt, hd, params->batch, params->cluster_ctas, params->stages,
+                           max_smem)) {
+        delete pl;
+        return DA_ERR_UNSUPPORTED;
+      }
+      C = params->cluster_ctas;
+    } else if (params->num_ctas == 0 && params->min_pages_per_cta == 0 && heads <= sms) {
+      int64_t c = sms / heads;
+      c = c < 16 ? c : 16;
+      c = c < pmax ? c : pmax;
+      for (; c >= 1 && C == 0; --c) {
+        da::Choice t = pl->choice;
+        if (!da::fit_cluster(&t, dt, hd, params->batch, (int)c, params->stages, max_smem)) continue;
+        if (da::prepare_cluster(t, dt, hd, (int)c) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        if (da::max_active_clusters(t, dt, hd, (int)c) >= heads) {
+          cc = t;
+          C = (int)c;
+        }
+      }
+    }
+    if (C > 0) {
+      if (da::prepare_cluster(cc, dt, hd, C) != cudaSuccess) {
+        delete pl;
+        return DA_ERR_CUDA;
+      }
+      pl->choice = cc;
+    }
+  }
   const int d = params->head_dim;
   // workspace: per-(b, kv head) page counters, then the partial (m, l, o) slots
   pl->cnt_bytes = ((size_t)params->batch * params->num_kv_heads * 4 + 255) / 256 * 256;
@@ -276,6 +328,9 @@ int draft_attn_plan_info(da_plan_t pl, da_plan_info* info) {
   info->engine = pl->choice.engine;
   info->stages = pl->choice.stages;
   info->smem_bytes = (int32_t)pl->choice.smem;
+  info->cluster_ctas = pl->choice.cluster;
+  if (pl->choice.cluster > 0)
+    info->num_ctas = pl->p.batch * pl->p.num_kv_heads * pl->choice.cluster;
   info->workspace_bytes = pl->ws_bytes;
   return DA_OK;
 }
@@ -374,10 +429,12 @@ int prepare_run(da_plan_t pl, const void* q, const int32_t* q_pos, const int32_t
 }
 
 int launch_run(da_plan_t pl, const RunPrep& r, void* stream) {
-  return da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, r.a, r.mk, r.mv, r.ms,
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? DA_OK
-             : DA_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      pl->choice.cluster > 0
+          ? da::launch_cluster(pl->choice, pl->p.dtype, pl->p.head_dim, r.a, r.mk, r.mv, r.ms, st)
+          : da::launch_decode(pl->choice, pl->p.dtype, pl->p.head_dim, r.a, r.mk, r.mv, r.ms, st);
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 }  // namespace

@@ -25,6 +25,7 @@ constexpr int kMaxBatch = 1024;
 // 128 * 40 + 256 * 232 = 384 * 168.
 constexpr int kVariantCore = 0;
 constexpr int kVariantMma = 1;
+constexpr int kVariantTc = 2;     // the tcgen05 kernel (its own layout, decode_tc.cuh)
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 128;
@@ -62,6 +63,7 @@ struct DecodeArgs {
   int32_t inputs_ready;
   int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + ring_slot(P)
   int32_t k_ring_sp;    // pages of sinks at the head of each sequence's ring
+  int32_t cluster;      // CTAs per cluster of the cluster partition (0: flat partition)
   float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 
@@ -271,17 +273,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up after ~2^31 SM cycles (about a second), sets the
-// timeout status bit and returns false.  Never expected to trigger.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// timeout status bit and the CTA's abort flag (a shared-memory word every
+// waiting thread of the CTA polls) and returns false; a thread that sees the
+// flag set by another gives up at once.  Never expected to trigger.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          volatile int32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
     if (clock64() - t0 > (1ll << 31)) {
       atomicOr(status, DA_STATUS_WAIT_TIMEOUT);
+      *abort = 1;
       return false;
     }
   }
+}
+
+// Bounded wait that ignores the abort flag (used to let copies already in
+// flight land before a CTA that gave up exits); false after ~2^28 cycles.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > (1ll << 28)) return false;
+  return true;
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -349,6 +365,86 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Thread-block clusters: rank of this CTA in its cluster, the cluster's size,
+// the shared-memory address of the same location in CTA `rank`'s shared
+// memory (distributed shared memory), loads from such addresses, and the
+// cluster-wide barrier (release/acquire: shared-memory writes before it are
+// visible to every CTA of the cluster after it).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+// Generic address of the same shared-memory location in CTA `rank` of the
+// cluster (generic loads and stores reach it).
+template <typename T>
+__device__ __forceinline__ T* dsmem_ptr(T* local, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<T*>(r);
+}
+// Arrive on the mbarrier at `local`'s place in CTA `rank`, releasing this
+// thread's earlier writes (its distributed-shared-memory stores included) to
+// the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               ::"r"(dsmem_addr(smem_u32(local), rank)) : "memory");
+}
+// Bounded wait (as mbar_wait) that acquires at cluster scope: writes other
+// CTAs released before their arrivals are visible after it.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                  volatile int32_t* abort) {
+  long long t0 = 0;
+  bool started = false;
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    if (ok) return true;
+    if (!started) {
+      t0 = clock64();
+      started = true;
+    }
+    if (*abort) return false;
+    if (clock64() - t0 > (1ll << 31)) {
+      atomicOr(status, DA_STATUS_WAIT_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
 }
 
 // Address of element (row, byte offset) inside a stage buffer laid out as

@@ -1,7 +1,7 @@
 // Instantiations and dispatch of the split-KV decode kernel.
 #include <type_traits>
 
-#include "decode.cuh"
+#include "decode_tc.cuh"
 #include "internal.h"
 
 namespace da {
@@ -9,6 +9,27 @@ namespace da {
 bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
                    int max_smem, bool side_f8, Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
+  if (engine_hint == 3) {
+    // the tcgen05 kernel: bf16, head_dim 128, up to 32 rows, no FP8 side cache
+    if (dtype != DA_DTYPE_BF16 || d != 128 || rows > kTcRows || side_f8) return false;
+    if (stages > kTcMaxStages) return false;
+    c->engine = DA_ENGINE_TC05;
+    c->variant = kVariantTc;
+    c->rk = kTcRows;
+    c->pingpong = false;
+    c->side_f8 = false;
+    const int hi = stages > 0 ? stages : kTcMaxStages, lo = stages > 0 ? stages : 2;
+    for (int s = hi; s >= lo; --s) {
+      const TcLayout L = make_tc_layout(s, batch);
+      if (tc_layout_check(L, s, batch) != 0) continue;
+      if ((int)L.total <= max_smem) {
+        c->stages = s;
+        c->smem = L.total;
+        return true;
+      }
+    }
+    return false;
+  }
   // Rows of one KV head that share every key: up to 4 stay on the FP32 pipes;
   // from 5 on, QK^T and PV are dense enough for an n8 tensor-core tile
   // (bf16 only).  An FP8 side cache goes to the tensor cores at any row count:
@@ -43,6 +64,24 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
   const int s_lo = stages > 0 ? stages : 2;
   for (int s = s_hi; s >= s_lo; --s) {
     const Layout L = make_layout(c->variant, es, d, c->rk, s, batch);
+    if (layout_check(L, c->variant, es, d, c->rk, s, batch) != 0) continue;
+    if ((int)L.total <= max_smem) {
+      c->stages = s;
+      c->smem = L.total;
+      return true;
+    }
+  }
+  return false;
+}
+
+bool fit_cluster(Choice* c, int dtype, int d, int batch, int cluster, int stages, int max_smem) {
+  c->cluster = cluster;
+  if (c->engine == DA_ENGINE_TC05) return true;   // its partials stay in its own stages
+  const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
+  const int s_hi = stages > 0 ? stages : kMaxAutoStages, s_lo = stages > 0 ? stages : 2;
+  for (int s = s_hi; s >= s_lo; --s) {
+    const Layout L = make_layout(c->variant, es, d, c->rk, s, batch, cluster);
+    if (layout_check(L, c->variant, es, d, c->rk, s, batch, cluster) != 0) continue;
     if ((int)L.total <= max_smem) {
       c->stages = s;
       c->smem = L.total;
@@ -104,6 +143,7 @@ static cudaError_t with_kernel(const Choice& c, int dtype, int d, F&& f) {
 }
 
 cudaError_t prepare_decode(const Choice& c, int dtype, int d) {
+  if (c.engine == DA_ENGINE_TC05) return tc_prepare(c, 0);
   return with_kernel(c, dtype, d, [&](auto kern) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
   });
@@ -112,6 +152,7 @@ cudaError_t prepare_decode(const Choice& c, int dtype, int d) {
 cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,
                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
                           cudaStream_t st) {
+  if (c.engine == DA_ENGINE_TC05) return tc_launch(c, a, mk, mv, ms, st);
   return with_kernel(c, dtype, d, [&](auto kern) {
     return launch_pdl(kern, dim3(a.n_cta), dim3(kThreads), c.smem, st, a, mk, mv, ms, c.stages);
   });

@@ -32,8 +32,12 @@ namespace da {
 // [rk][d] as FP32, and each row's draft-tree mask into s.tmask.  Rows >= R
 // are zero.  Consumer threads only.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int RK, int NCT, bool KSQ = true>
-__device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
+// QB: the rows go to qtile instead, as bf16 in the 128-byte-swizzled K-major
+// layout the tcgen05 engine's MMA reads (two [RK][64] boxes, dimensions 0-63
+// then 64-127).
+template <typename T, int D, int RK, int NCT, bool KSQ = true, bool QB = false>
+__device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq,
+                                    uint8_t* qtile = nullptr) {
   const int tid = threadIdx.x;
   const int bh = seq >> 1, b = bh / a.H_kv, h = bh - b * a.H_kv;
   const int32_t L = s.len[b];
@@ -102,8 +106,17 @@ __device__ inline void prep_queries(const DecodeArgs& a, Smem& s, int seq) {
         xr = (qx[u] * c.x - qy[u] * c.y) * mult;
         yr = (qy[u] * c.x + qx[u] * c.y) * mult;
       }
-      s.q[row * D + f] = xr;
-      s.q[row * D + f + D / 2] = yr;
+      if constexpr (QB) {
+        // dims f and f + D/2 (D = 128: box 0 and box 1, same column)
+        static_assert(D == 128, "tcgen05 query tile");
+        const int byte = f * 2;
+        const uint32_t off = (uint32_t)row * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
+        *reinterpret_cast<__nv_bfloat16*>(qtile + off) = __float2bfloat16_rn(xr);
+        *reinterpret_cast<__nv_bfloat16*>(qtile + RK * 128 + off) = __float2bfloat16_rn(yr);
+      } else {
+        s.q[row * D + f] = xr;
+        s.q[row * D + f + D / 2] = yr;
+      }
     }
   }
   named_barrier(1, NCT);
@@ -518,7 +531,8 @@ struct CoreEngine {
   }
 
   // Sum the key groups, merge the consumer warps, write the piece's partial.
-  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+  // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
+  __device__ __forceinline__ void finish(const Smem& s, float* part) {
     float lt = l_run;
     // with 4 rows lanes ds and ds ^ 4 hold one row's sums over different keys
 #pragma unroll
@@ -547,7 +561,6 @@ struct CoreEngine {
                 o2[r][i * (EPC / 2) + e];
     }
     named_barrier(1, NCT);
-    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
     for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       float M = -INFINITY;
@@ -730,7 +743,8 @@ struct CoreEngineWide {
   }
 
   // Merge the eight warps' states and write the piece's partial to `slot`.
-  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+  // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
+  __device__ __forceinline__ void finish(const Smem& s, float* part) {
     float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
     lt += __shfl_xor_sync(0xffffffffu, lt, 16);
     if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
@@ -740,7 +754,6 @@ struct CoreEngineWide {
       for (int e = 0; e < DPL / 2; ++e)
         *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + lane * DPL + 2 * e) = o2[r][e];
     named_barrier(1, NCT);
-    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
     for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       float M = -INFINITY;
@@ -1031,7 +1044,8 @@ struct MmaEngine {
   }
 
   // Merge the warps holding each row and write the piece's partial to `slot`.
-  __device__ __forceinline__ void finish(const DecodeArgs& a, const Smem& s, int64_t slot) {
+  // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
+  __device__ __forceinline__ void finish(const Smem& s, float* part) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1055,7 +1069,6 @@ struct MmaEngine {
       }
     named_barrier(1, NCT);
     constexpr int NW = SPLIT_PAGES ? 8 : 4;   // warps holding one row
-    float* part = a.part + slot * (int64_t)slot_floats(RK, D);
     for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
       const int r = idx / D, dim = idx - r * D;
       const int w0 = SPLIT_PAGES ? 0 : (r / RW) * 4;
@@ -1261,6 +1274,72 @@ __device__ inline void ticket(const DecodeArgs& a, Smem& s, int seq, uint32_t pa
   if (last) merge_sequence<T, D, RK, NCT>(a, s, b, h);
 }
 
+// Cluster partition: merge of the partials the cluster's CTAs hold in their
+// shared memory (at the same offset `local` in each), read through
+// distributed shared memory.  Work items are (row, 4 dimensions), spread
+// over the cluster's consumer threads; each loads every CTA's (m, l, o)
+// before it merges, so the remote loads are in flight together.
+template <typename T, int D, int RK, int NCT>
+__device__ inline void cluster_merge(const DecodeArgs& a, int b, int h, uint32_t local) {
+  constexpr int C4 = D / 4;
+  constexpr int kMaxCluster = 16;
+  const uint32_t cn = cluster_size(), cr = cluster_rank();
+  uint32_t src[kMaxCluster];
+#pragma unroll
+  for (int k = 0; k < kMaxCluster; ++k) src[k] = dsmem_addr(local, (uint32_t)k < cn ? k : 0);
+  for (int item = threadIdx.x * (int)cn + (int)cr; item < a.R * C4; item += NCT * (int)cn) {
+    const int r = item / C4, c4 = item - r * C4;
+    float mm[kMaxCluster], ll[kMaxCluster];
+    float4 oo[kMaxCluster];
+#pragma unroll
+    for (int k = 0; k < kMaxCluster; ++k) {
+      mm[k] = -INFINITY;
+      ll[k] = 0.f;
+      oo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if ((uint32_t)k < cn) {
+        mm[k] = dsmem_ld_f32(src[k] + 4u * r);
+        ll[k] = dsmem_ld_f32(src[k] + 4u * (RK + r));
+        oo[k] = dsmem_ld_f32x4(src[k] + 4u * (slot_o_off(RK) + r * D + 4 * c4));
+      }
+    }
+    MergeState st;
+    st.init();
+#pragma unroll
+    for (int k = 0; k < kMaxCluster; ++k) st.add(mm[k], ll[k], oo[k]);
+    float res[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) res[k] = st.l > 0.f ? st.o[k] / st.l : 0.f;
+    const int t = r / a.G, j = r - t * a.G;
+    T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + 4 * c4;
+    store4<T>(out, res);
+  }
+}
+
+// Cluster partition, rank 0: merge of the partials every CTA of the cluster
+// stored into this CTA's receive slots.  Work items are (row, 4 dimensions).
+template <typename T, int D, int RK, int NCT>
+__device__ inline void recv_merge(const DecodeArgs& a, const Smem& s, int b, int h) {
+  constexpr int C4 = D / 4;
+  constexpr int64_t SF = slot_floats(RK, D);
+  const int cn = (int)cluster_size();
+  for (int item = threadIdx.x; item < a.R * C4; item += NCT) {
+    const int r = item / C4, c4 = item - r * C4;
+    MergeState st;
+    st.init();
+    for (int k = 0; k < cn; ++k) {
+      const float* slot = s.recv + k * SF;
+      st.add(slot[r], slot[RK + r],
+             *reinterpret_cast<const float4*>(slot + slot_o_off(RK) + r * D + 4 * c4));
+    }
+    float res[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) res[q] = st.l > 0.f ? st.o[q] / st.l : 0.f;
+    const int t = r / a.G, j = r - t * a.G;
+    T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + 4 * c4;
+    store4<T>(out, res);
+  }
+}
+
 // Rows of (b, h) whose selection is empty get a zero output (nobody merges
 // them); CTA (b * H_kv + h) mod n_cta writes it.
 template <typename T, int D, int NCT>
@@ -1280,7 +1359,20 @@ __device__ inline void zero_empty(const DecodeArgs& a, const Smem& s) {
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <typename T, int D, class Engine, int VARIANT, int RK>
+//
+// Two partitions of the work:
+//  * flat (CLUSTER false): one persistent CTA per SM takes an equal stretch
+//    of the page line of every (sequence, KV head, range); pieces leave
+//    partials in the workspace and the last CTA of each (sequence, KV head)
+//    merges them (ticket, merge_sequence).
+//  * cluster (CLUSTER true; one-segment modes whose selection is short, such
+//    as window mode): one thread-block cluster of a.cluster CTAs per
+//    (sequence, KV head).  CTA r of the cluster takes an equal r-th share of
+//    that head's pages (one piece), leaves its partial in its own shared
+//    memory, and after a cluster barrier the CTAs merge the partials through
+//    distributed shared memory and write the output: no workspace round trip,
+//    no ticket, and no CTA merges alone at the end.
+template <typename T, int D, class Engine, int VARIANT, int RK, bool CLUSTER = false>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ms,
@@ -1291,28 +1383,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NCW = Engine::NCW;
   constexpr int NCT = NCW * 32;
   static_assert(NCW == kConsumerWarps, "consumer warps");
-  const Layout L = make_layout(VARIANT, ES, D, RK, stages, a.B);
+  static_assert(!CLUSTER || !Engine::kPingPong, "cluster partition: shared-step engines");
+  static_assert(!CLUSTER || slot_floats(RK, D) * 4 <= 2 * (D * ES / kSwizzleRow) * kBoxBytes,
+                "the partial fits in one pipeline stage");
+  const Layout L = make_layout(VARIANT, ES, D, RK, stages, a.B, CLUSTER ? a.cluster : 0);
   Smem s = carve(smem_raw, L);
-  prologue<D, ES, NCW>(a, s, L);
-  const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
-  const int64_t n_act = active_ctas(TP, a.n_cta, a.min_pages);
-  const int64_t xs = blockIdx.x < n_act ? cta_begin(blockIdx.x, TP, n_act) : 0;
-  const int64_t xe = blockIdx.x < n_act ? cta_begin(blockIdx.x + 1, TP, n_act) : 0;
+  int64_t xs, xe;
+  int cb = 0, ch = 0;   // cluster partition: the cluster's (sequence, KV head)
+  uint32_t cr = 0;      // and this CTA's rank in it
+  int32_t Lb = 0;
+  if constexpr (CLUSTER) {
+    // No page prefix: the CTA knows its (sequence, KV head) from its cluster
+    // and its pages from that one context length, read by every thread.
+    cluster_start<D, NCW>(a, s, L);
+    cr = cluster_rank();
+    const uint32_t cn = cluster_size();
+    const int bh = (int)(blockIdx.x / cn);
+    cb = bh / a.H_kv;
+    ch = bh - cb * a.H_kv;
+    Lb = clamp_ctx(__ldg(a.ctx_lens + cb), a.max_pages, a.status);
+    s.len[cb] = Lb;   // query preparation reads it (every thread writes the same value)
+    const Ranges rg = mode_ranges(a.mode, Lb, a.W, a.n_sink);
+    const int64_t nb = range_pages(rg.k0[0], rg.k1[0]) + range_pages(rg.k0[1], rg.k1[1]) +
+                       range_pages(rg.k0[2], rg.k1[2]);
+    xs = nb * cr / cn;
+    xe = nb * (cr + 1) / cn;
+  } else {
+    prologue<D, ES, NCW>(a, s, L);
+    const int64_t TP = (int64_t)s.pfx[a.B] * a.H_kv;
+    const int64_t n_act = active_ctas(TP, a.n_cta, a.min_pages);
+    xs = blockIdx.x < n_act ? cta_begin(blockIdx.x, TP, n_act) : 0;
+    xe = blockIdx.x < n_act ? cta_begin(blockIdx.x + 1, TP, n_act) : 0;
+  }
   const int warp = threadIdx.x >> 5;
   if (warp >= NCW) {
     regs_dec<kProducerRegs>();
-    if (warp == NCW) producer<ES, NCB, Engine::kSideF8>(a, s, L, xs, xe, &mk, &mv, &ms);
+    if (warp == NCW) {
+      if constexpr (CLUSTER)
+        producer_head<ES, NCB, Engine::kSideF8>(a, s, L, cb, ch, Lb, xs, xe, &mk, &mv, &ms);
+      else
+        producer<ES, NCB, Engine::kSideF8>(a, s, L, xs, xe, &mk, &mv, &ms);
+    }
     return;
   }
   regs_inc<kConsumerRegs>();
   Engine eng;
   eng.init();
   if constexpr (!Engine::kFarScaleInQ) eng.kscale = a.far_kscale;
-  zero_empty<T, D, NCT>(a, s);
+  if constexpr (!CLUSTER) zero_empty<T, D, NCT>(a, s);
+  // cluster partition: this CTA's partial goes straight to its slot in rank
+  // 0's shared memory
+  float* const dst_part =
+      CLUSTER ? dsmem_ptr(s.recv + (size_t)cr * slot_floats(RK, D), 0u) : nullptr;
+  bool wrote = false;
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
-    const Where w = locate(s, a.B, a.H_kv, xs);
-    const int32_t seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
+    int32_t seq;
+    if constexpr (CLUSTER) {
+      seq = piece_seq(a.mode, cb, ch, a.H_kv, 0);   // one segment (no FOLD here)
+    } else {
+      const Where w = locate(s, a.B, a.H_kv, xs);
+      seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
+    }
     prep_queries<T, D, RK, NCT, Engine::kFarScaleInQ>(a, s, seq);
     if constexpr (Engine::kSideF8) eng.begin_far(s, (seq & 1) == 0); else eng.begin(s);
   }
@@ -1322,7 +1454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool long_stretch = !Engine::kPingPong || xe - xs >= 4;
   for (int64_t x = xs; x < xe;) {
     const uint32_t st = n % L.stages;
-    if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status)) break;
+    if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status, s.abort)) break;
     const PageInfo inf = s.info[st];
     if ((inf.flags & kFirst) && x != xs) {
       prep_queries<T, D, RK, NCT, Engine::kFarScaleInQ>(a, s, inf.seq);
@@ -1339,7 +1471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // short stretch goes page by page, so that both warp groups work
       if (!last && long_stretch) {
         const uint32_t st1 = (n + 1) % L.stages;
-        if (!mbar_wait(&s.full[st1], ((n + 1) / L.stages) & 1u, a.status)) break;
+        if (!mbar_wait(&s.full[st1], ((n + 1) / L.stages) & 1u, a.status, s.abort)) break;
         const PageInfo inf1 = s.info[st1];
         const uint32_t kb1 = base + st1 * L.stage_bytes;
         const uint32_t kb[2] = {kb0, kb1};
@@ -1388,10 +1520,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     n += taken;
     ++unit;
     if (last) {
-      eng.finish(a, s, (int64_t)blockIdx.x + inf.seq);
-      ticket<T, D, RK, NCT>(a, s, inf.seq, pages);
+      if constexpr (CLUSTER) {
+        eng.finish(s, dst_part);   // the CTA's one piece
+        wrote = true;
+      } else {
+        eng.finish(s, a.part + ((int64_t)blockIdx.x + inf.seq) * slot_floats(RK, D));
+        ticket<T, D, RK, NCT>(a, s, inf.seq, pages);
+      }
       pages = 0;
     }
+  }
+  // The producer warp waits for this before it exits (it lets its copies
+  // land first when a wait gave up).
+  named_barrier_arrive(kEndBarrier, NCT + 32);
+  if constexpr (CLUSTER) {
+    // A CTA with no pages (a selection shorter than the cluster) or one whose
+    // wait gave up contributes an empty partial.
+    if (!wrote || *s.abort) {
+      for (int r = threadIdx.x; r < RK; r += NCT) {
+        dst_part[r] = -INFINITY;
+        dst_part[RK + r] = 0.f;
+      }
+    }
+    // Every consumer thread releases its stores into rank 0's slot and
+    // arrives on rank 0's merge barrier; rank 0 merges once all have arrived
+    // (the other CTAs are done: nothing reads their shared memory).
+    mbar_arrive_remote(s.merge_bar, 0u);
+    if (cr == 0 && mbar_wait_cluster(s.merge_bar, 0u, a.status, s.abort))
+      recv_merge<T, D, RK, NCT>(a, s, cb, ch);
   }
 }
 

@@ -33,6 +33,7 @@ struct Choice {
   bool side_f8;    // FOLD far keys from an FP8 E4M3 side cache
   int stages;      // pipeline depth
   uint32_t smem;   // dynamic shared memory bytes
+  int cluster;     // 0: flat partition; else CTAs per cluster of the cluster partition
 };
 
 // Picks the kernel instance for `rows` query rows per KV head (engine_hint:
@@ -42,6 +43,31 @@ bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_h
                    int max_smem, bool side_f8, Choice* c);
 
 cudaError_t prepare_decode(const Choice& c, int dtype, int d);
+
+// Cluster partition (one cluster of CTAs per (sequence, KV head); decode
+// kernels of decode_cluster.cu).  cluster_supported: whether an instance
+// exists for the choice (shared-step engines, no FP8 side cache).
+// prepare_cluster: sets the instance's attributes for clusters of up to
+// `cluster` CTAs.  max_active_clusters: how many clusters of `cluster` CTAs
+// the device holds at once (0 on error).
+bool cluster_supported(const Choice& c, int dtype, int d);
+// Sets c's cluster size and, with rank 0's receive slots for `cluster`
+// partials in its layout, its pipeline depth (stages, or the deepest that
+// fits when 0) and shared memory; false when nothing fits in max_smem.
+bool fit_cluster(Choice* c, int dtype, int d, int batch, int cluster, int stages, int max_smem);
+cudaError_t prepare_cluster(const Choice& c, int dtype, int d, int cluster);
+int max_active_clusters(const Choice& c, int dtype, int d, int cluster);
+cudaError_t launch_cluster(const Choice& c, int dtype, int d, const DecodeArgs& a,
+                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
+                           cudaStream_t st);
+
+// The tcgen05 kernel (decode_tc.cu): attributes for the flat partition
+// (cluster 0) or clusters of up to `cluster` CTAs, resident clusters, launch
+// (the grid follows c.cluster).
+cudaError_t tc_prepare(const Choice& c, int cluster);
+int tc_max_active_clusters(const Choice& c, int cluster);
+cudaError_t tc_launch(const Choice& c, const DecodeArgs& a, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& ms, cudaStream_t st);
 cudaError_t launch_decode(const Choice& c, int dtype, int d, const DecodeArgs& a,
                           const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& ms,
                           cudaStream_t st);

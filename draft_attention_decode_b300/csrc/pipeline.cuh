@@ -18,6 +18,10 @@ namespace da {
 
 enum : int { kFirst = 1, kLast = 2, kValid = 4 };
 
+// Named barrier ids: 1 the consumer warps among themselves, 2 the end of the
+// kernel (consumers arrive, the producer warp waits; see producer()).
+constexpr int kEndBarrier = 2;
+
 // Tree offset of a page with no draft-tree key under a mask.
 constexpr int32_t kNoTree = -(1 << 30);
 
@@ -33,7 +37,7 @@ struct PageInfo {
 struct Layout {
   uint32_t stage_bytes, stages;
   uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
-      n01_off, flag_off, tm_off, rm_off, total;
+      n01_off, flag_off, tm_off, rm_off, recv_off, recv_slots, mbar_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -41,8 +45,10 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 // Merge buffers hold `rm` rows per consumer warp: rk on the CUDA cores, 16
 // on the tensor cores; the CUDA-core variant also keeps a per-warp
 // probability buffer (used by the 5..8-row engine).
+// recv_slots: cluster partition, the CTAs per cluster whose partials rank 0
+// receives (0 for the flat partition).
 __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk, int stages,
-                                              int batch) {
+                                              int batch, int recv_slots = 0) {
   Layout L;
   L.stage_bytes = 2u * (uint32_t)(d * es / kSwizzleRow) * kBoxBytes;
   L.stages = stages;
@@ -63,9 +69,58 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.flag_off = off;  off += 128;
   L.tm_off = off;    off += align_up((uint32_t)rk * 8, 128);
   L.rm_off = off;    off += align_up((uint32_t)rk * 4, 128);
+  L.recv_off = off;  L.recv_slots = (uint32_t)recv_slots;
+  off += align_up((uint32_t)recv_slots * slot_floats(rk, d) * 4, 128);
+  L.mbar_off = off;  off += recv_slots > 0 ? 128 : 0;   // the merge barrier
 
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
+}
+
+// Checks the alignment and extent of every region of a layout, as the
+// kernels use them: the stage ring at the 1024-byte-aligned base, each stage
+// a whole number of 1024-byte swizzle atoms (128-byte-swizzled TMA
+// destinations); every other region 128-byte aligned (which covers the
+// 8-byte mbarriers and uint64 masks and the 16-byte ld.shared.v4 / float4
+// accesses), in order, large enough, without overlap, and the zero chunk of
+// the flag block 16-byte aligned.  Returns 0, or the number of the first
+// check that fails.  Host code runs it for every layout a plan may choose.
+__host__ __device__ inline int layout_check(const Layout& L, int variant, int es, int d, int rk,
+                                            int stages, int batch, int recv_slots = 0) {
+  if ((int)L.recv_slots != recv_slots) return 3;
+  if (L.stage_bytes == 0 || L.stage_bytes % 1024 != 0) return 1;
+  if ((uint32_t)stages != L.stages) return 2;
+  const uint32_t ncw = (uint32_t)kConsumerWarps;
+  const uint32_t rm = variant == kVariantMma ? 16u : (uint32_t)rk;
+  struct Region { uint32_t off, need; };
+  const Region r[] = {
+      {0, L.stage_bytes * (uint32_t)stages},
+      {L.q_off, (uint32_t)rk * d * 4},
+      {L.mo_off, ncw * rm * d * 4},
+      {L.ml_off, ncw * rm * 8},
+      {L.p_off, variant == kVariantCore ? ncw * 9 * (uint32_t)rk * 4 : 0u},
+      {L.info_off, (uint32_t)stages * (uint32_t)sizeof(PageInfo)},
+      {L.bar_off, (uint32_t)stages * 16},
+      {L.invf_off, (uint32_t)(d / 2) * 8},
+      {L.len_off, (uint32_t)batch * 4},
+      {L.pfx_off, (uint32_t)(batch + 1) * 4},
+      {L.n0_off, (uint32_t)batch * 4},
+      {L.n01_off, (uint32_t)batch * 4},
+      {L.flag_off, 80},
+      {L.tm_off, (uint32_t)rk * 8},
+      {L.rm_off, (uint32_t)rk * 4},
+      {L.recv_off, L.recv_slots * (uint32_t)slot_floats(rk, d) * 4},
+      {L.mbar_off, L.recv_slots ? 8u : 0u},
+  };
+  constexpr int n = sizeof(r) / sizeof(r[0]);
+  for (int i = 1; i < n; ++i) {
+    if (r[i].off % 128 != 0) return 10 + i;
+    if (r[i].off < r[i - 1].off + r[i - 1].need) return 30 + i;
+  }
+  if ((L.flag_off + 64) % 16 != 0) return 50;
+  if (L.total < r[n - 1].off + r[n - 1].need + 1024) return 51;
+  if (es * d % kSwizzleRow != 0) return 52;
+  return 0;
 }
 
 struct Smem {
@@ -83,9 +138,12 @@ struct Smem {
   int32_t* n0;          // [B] pages per head of range 0
   int32_t* n01;         // [B] pages per head of ranges 0 and 1
   int32_t* flag;        // broadcast of the merge ticket (word 0)
+  volatile int32_t* abort;   // word 1 of the flag block: set when a wait gave up
   uint32_t zero16;      // shared address of 16 zero bytes (words 16..19 of the flag block)
   uint64_t* tmask;      // [rk] visible tree keys of each row of the current piece
   float* rmult;         // [rk] logit multiplier of each row of the current piece
+  float* recv;          // cluster partition, rank 0: one partial slot per CTA of the cluster
+  uint64_t* merge_bar;  // cluster partition, rank 0: every CTA's consumers arrive once filled
 };
 
 __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
@@ -106,9 +164,12 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.n0 = reinterpret_cast<int32_t*>(p + L.n0_off);
   s.n01 = reinterpret_cast<int32_t*>(p + L.n01_off);
   s.flag = reinterpret_cast<int32_t*>(p + L.flag_off);
+  s.abort = s.flag + 1;
   s.zero16 = smem_u32(p + L.flag_off + 64);
   s.tmask = reinterpret_cast<uint64_t*>(p + L.tm_off);
   s.rmult = reinterpret_cast<float*>(p + L.rm_off);
+  s.recv = reinterpret_cast<float*>(p + L.recv_off);
+  s.merge_bar = reinterpret_cast<uint64_t*>(p + L.mbar_off);
   return s;
 }
 
@@ -120,6 +181,7 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   grid_dep_launch_dependents();
   for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.turn_freq[i];
   if (tid < 4) s.flag[16 + tid] = 0;
+  if (tid == 0) *s.abort = 0;
   if (tid == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
       mbar_init(&s.full[i], 1);
@@ -196,15 +258,46 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
   return w;
 }
 
+// Per-page fields the producer derives for flat position x.
+struct PageFields {
+  int32_t seq, lohi, flags, phys, far, h, toff, kphys;
+};
+
+// Fields of page P (of range r of sequence b's KV head h), the page being
+// the first or last of its piece as given.
+__device__ __forceinline__ PageFields page_fields(const DecodeArgs& a, const Smem& s, int b, int h,
+                                                  int32_t Lb, const Ranges& rg, int r, int kr,
+                                                  bool first, bool last) {
+  const bool fold = a.mode == DA_MODE_FOLD;
+  const int32_t k0 = rg.lo(r), k1 = rg.hi(r);
+  const int32_t P = k0 / kPage + kr;
+  const int32_t pk0 = P * kPage;
+  const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;
+  PageFields f;
+  f.h = h;
+  f.seq = piece_seq(a.mode, b, h, a.H_kv, r);
+  f.lohi = lo | (hi << 16);
+  f.phys = phys_page(a.block_table, b, P, a.max_pages, a.num_pages, a.status);
+  f.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (f.phys >= 0 ? kValid : 0);
+  f.far = (fold && r == 0) ? 1 : 0;
+  f.kphys = (a.k_ring > 0 && !f.far) ? b * a.k_ring + ring_slot(P, a.k_ring, a.k_ring_sp) : f.phys;
+  f.toff = kNoTree;
+  if (a.tree_mask && a.n_tree > 0 && !f.far) {
+    const int32_t t0 = Lb - a.n_tree;   // position of tree token 0
+    if (pk0 + kPage > t0) f.toff = pk0 - t0;
+  }
+  return f;
+}
+
 // The producer warp: block-table translation and TMA issue for the CTA's
 // stretch [xs, xe) of the page line.  ES = element bytes, NCB = 128-byte
 // column boxes per row (head_dim * ES / 128).  F8: far keys come from an FP8
 // side cache, one box of 64 rows x head_dim bytes per page, into the stage's
-// first K box.
-template <int ES, int NCB, bool F8>
-__device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
-                                int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
-                                const CUtensorMap* ms) {
+// first K box.  fields(x) gives the page fields of position x.
+template <int ES, int NCB, bool F8, class Fields>
+__device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
+                                     int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
+                                     const CUtensorMap* ms, Fields&& fields) {
   const int lane = threadIdx.x & 31;
   const uint64_t pol = policy_evict_first();
   if (lane == 0) {
@@ -212,34 +305,16 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
     prefetch_tmap(mv);
     if (a.mode == DA_MODE_FOLD) prefetch_tmap(ms);
   }
-  const bool fold = a.mode == DA_MODE_FOLD;
-  uint32_t n = 0;
+  uint32_t n = 0;        // pages armed so far (loads issued, or a plain arrive)
+  bool stopped = false;
   for (int64_t base = xs; base < xe; base += 32) {
     const int64_t x = base + lane;
     int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree;
     int32_t kphys = -1;   // page of the K array (the ring slot of a FOLD local page)
     if (x < xe) {
-      const Where w = locate(s, a.B, a.H_kv, x);
-      const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
-      const int32_t k0 = rg.lo(w.r), k1 = rg.hi(w.r);
-      const int32_t P = k0 / kPage + w.kr;
-      const int32_t pk0 = P * kPage;
-      const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;
-      const int32_t nb = s.pfx[w.b + 1] - s.pfx[w.b], n0 = s.n0[w.b];
-      h = w.h;
-      seq = piece_seq(a.mode, w.b, w.h, a.H_kv, w.r);
-      lohi = lo | (hi << 16);
-      phys = phys_page(a.block_table, w.b, P, a.max_pages, a.num_pages, a.status);
-      const bool first = x == xs || w.k == 0 || (fold && w.k == n0);
-      const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
-      flags = (first ? kFirst : 0) | (last ? kLast : 0) | (phys >= 0 ? kValid : 0);
-      far = (fold && w.r == 0) ? 1 : 0;
-      kphys = (a.k_ring > 0 && !far) ? w.b * a.k_ring + ring_slot(P, a.k_ring, a.k_ring_sp)
-                                     : phys;
-      if (a.tree_mask && a.n_tree > 0 && !far) {
-        const int32_t t0 = s.len[w.b] - a.n_tree;   // position of tree token 0
-        if (pk0 + kPage > t0) toff = pk0 - t0;
-      }
+      const PageFields f = fields(x);
+      seq = f.seq; lohi = f.lohi; flags = f.flags; phys = f.phys; far = f.far; h = f.h;
+      toff = f.toff; kphys = f.kphys;
     }
     const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
     for (int j = 0; j < cnt; ++j) {
@@ -251,6 +326,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
       const int32_t jh = __shfl_sync(0xffffffffu, h, j);
       const int32_t jtoff = __shfl_sync(0xffffffffu, toff, j);
       const int32_t jkphys = __shfl_sync(0xffffffffu, kphys, j);
+      int gave_up = 0;
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
@@ -258,7 +334,7 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
           grid_dep_wait();
           fence_proxy_async_global();
         }
-        if (mbar_wait(&s.empty[st], par ^ 1u, a.status)) {
+        if (mbar_wait(&s.empty[st], par ^ 1u, a.status, s.abort)) {
           s.info[st] = PageInfo{jseq, jlohi, jflags, jtoff};
           uint8_t* kdst = s.stage + st * L.stage_bytes;
           uint8_t* vdst = kdst + NCB * kBoxBytes;
@@ -283,12 +359,89 @@ __device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, i
           } else {
             mbar_arrive(&s.full[st]);
           }
+        } else {
+          gave_up = 1;   // a wait gave up: issue nothing more
         }
+      }
+      if (__shfl_sync(0xffffffffu, gave_up, 0)) {
+        stopped = true;
+        break;
       }
       ++n;
       __syncwarp();
     }
+    if (stopped) break;
   }
+  // Every consumer warp arrives here once its page loop is over.  If any wait
+  // of the CTA gave up, the copies this warp armed may still be in flight:
+  // let them land (bounded) before the CTA, and its shared memory, goes away.
+  // Only the last `stages` pages can be outstanding, one per stage.
+  named_barrier(kEndBarrier, kConsumerThreads + 32);
+  if (lane == 0 && *s.abort) {
+    const uint32_t first = n > L.stages ? n - L.stages : 0u;
+    for (uint32_t i = first; i < n; ++i) mbar_drain(&s.full[i % L.stages], (i / L.stages) & 1u);
+  }
+  __syncwarp();   // the warp leaves converged
+}
+
+// Flat partition: positions of the page line over every (sequence, KV head, range).
+template <int ES, int NCB, bool F8>
+__device__ inline void producer(const DecodeArgs& a, Smem& s, const Layout& L, int64_t xs,
+                                int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
+                                const CUtensorMap* ms) {
+  const bool fold = a.mode == DA_MODE_FOLD;
+  producer_loop<ES, NCB, F8>(a, s, L, xs, xe, mk, mv, ms, [&](int64_t x) {
+    const Where w = locate(s, a.B, a.H_kv, x);
+    const Ranges rg = mode_ranges(a.mode, s.len[w.b], a.W, a.n_sink);
+    const int32_t nb = s.pfx[w.b + 1] - s.pfx[w.b], n0 = s.n0[w.b];
+    const bool first = x == xs || w.k == 0 || (fold && w.k == n0);
+    const bool last = x == xe - 1 || w.k == nb - 1 || (fold && w.k == n0 - 1);
+    return page_fields(a, s, w.b, w.h, s.len[w.b], rg, w.r, w.kr, first, last);
+  });
+}
+
+// Cluster partition: pages [k_lo, k_hi) of sequence b's KV head h (context
+// length Lb), numbered over the head's ranges, without the flat prefix.
+template <int ES, int NCB, bool F8>
+__device__ inline void producer_head(const DecodeArgs& a, Smem& s, const Layout& L, int b, int h,
+                                     int32_t Lb, int64_t k_lo, int64_t k_hi, const CUtensorMap* mk,
+                                     const CUtensorMap* mv, const CUtensorMap* ms) {
+  const bool fold = a.mode == DA_MODE_FOLD;
+  const Ranges rg = mode_ranges(a.mode, Lb, a.W, a.n_sink);
+  const int32_t n0 = range_pages(rg.k0[0], rg.k1[0]);
+  const int32_t n01 = n0 + range_pages(rg.k0[1], rg.k1[1]);
+  const int32_t nb = n01 + range_pages(rg.k0[2], rg.k1[2]);
+  producer_loop<ES, NCB, F8>(a, s, L, k_lo, k_hi, mk, mv, ms, [&](int64_t x) {
+    const int32_t k = (int32_t)x;
+    const int r = k < n0 ? 0 : (k < n01 ? 1 : 2);
+    const int kr = k - (r == 0 ? 0 : (r == 1 ? n0 : n01));
+    const bool first = x == k_lo || k == 0 || (fold && k == n0);
+    const bool last = x == k_hi - 1 || k == nb - 1 || (fold && k == n0 - 1);
+    return page_fields(a, s, b, h, Lb, rg, r, kr, first, last);
+  });
+}
+
+// Cluster partition start: barriers (the stage ring, and the merge barrier
+// that rank 0's consumers wait on: every consumer thread of every CTA of the
+// cluster arrives once), the angle table, flags; then a cluster barrier, so
+// that no CTA arrives on rank 0's merge barrier before rank 0 initialised it.
+template <int D, int NCW>
+__device__ inline void cluster_start(const DecodeArgs& a, Smem& s, const Layout& L) {
+  const int tid = threadIdx.x;
+  grid_dep_launch_dependents();
+  for (int i = tid; i < D / 2; i += blockDim.x) s.invf[i] = a.turn_freq[i];
+  if (tid < 4) s.flag[16 + tid] = 0;
+  if (tid == 0) {
+    *s.abort = 0;
+    for (uint32_t i = 0; i < L.stages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], NCW);
+    }
+    mbar_init(s.merge_bar, L.recv_slots * kConsumerThreads);
+    fence_barrier_init();
+  }
+  if (!a.inputs_ready) grid_dep_wait();
+  cluster_sync_all();
 }
 
 }  // namespace da

@@ -19,9 +19,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct StaticWs {
-  std::once_flag once[kMaxDevices];
+  std::mutex mu;
   void* ptr[kMaxDevices] = {};
-  cudaError_t err[kMaxDevices] = {};
 };
 
 StaticWs& static_ws() {
@@ -29,23 +28,34 @@ StaticWs& static_ws() {
   return s;
 }
 
-// Device address of the array on `device` (looked up once per device, with
-// that device current).  In host code the array's name is only a host-side
-// stand-in; this lookup is the address a kernel may be given.
+// Device address of the array on `device`, looked up with that device
+// current.  In host code the array's name is only a host-side stand-in; this
+// lookup is the address a kernel may be given.  Only a successful lookup is
+// kept: after a failure (which also clears the runtime's last-error state)
+// the next call tries again.
 void* static_ws_ptr(int device) {
   if (device < 0 || device >= kMaxDevices) return nullptr;
   StaticWs& s = static_ws();
-  std::call_once(s.once[device], [&] {
-    int prev = -1;
-    s.err[device] = cudaGetDevice(&prev);
-    if (s.err[device] != cudaSuccess) return;
-    if (prev != device && (s.err[device] = cudaSetDevice(device)) != cudaSuccess) return;
-    void* p = nullptr;
-    s.err[device] = cudaGetSymbolAddress(&p, g_da_static_ws);
-    if (s.err[device] == cudaSuccess) s.ptr[device] = p;
-    if (prev != device) cudaSetDevice(prev);
-  });
-  return s.err[device] == cudaSuccess ? s.ptr[device] : nullptr;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ptr[device]) return s.ptr[device];
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_da_static_ws) == cudaSuccess) {
+    s.ptr[device] = p;
+  } else {
+    p = nullptr;
+    cudaGetLastError();
+  }
+  if (prev != device) cudaSetDevice(prev);
+  return p;
 }
 
 }  // namespace

@@ -99,6 +99,8 @@ typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP32 = 1 } da_dtype;
  * rows fill n8 MMA tiles and QK^T / PV are dense contractions. */
 #define DA_ENGINE_CUDA_CORE 0  /* <= 8 rows: FP32 FMA path                        */
 #define DA_ENGINE_MMA       1  /* 5..32 rows, bf16: m16n8k16 tensor-core path     */
+#define DA_ENGINE_TC05      2  /* <= 32 rows, bf16, head_dim 128: tcgen05 MMAs with
+                                  TMEM accumulators (da_params.engine = 3)         */
 
 typedef struct {
   double  rope_theta;        /* RoPE base theta, > 0; 0 = NoPE (no rotation)      */
@@ -124,7 +126,9 @@ typedef struct {
   float   softmax_scale;     /* logit scale c; 0 selects 1/sqrt(head_dim)          */
   int32_t num_ctas;          /* persistent CTAs; 0 = one per SM (tests vary this)  */
   int32_t engine;            /* 0 automatic, 1 CUDA cores (<= 8 rows), 2 tensor
-                                cores (bf16 only); see DA_ENGINE_*                */
+                                cores (mma.sync, bf16 only), 3 tcgen05 tensor
+                                cores (bf16, head_dim 128, no FP8 side cache);
+                                see DA_ENGINE_*                                  */
   int32_t min_pages_per_cta; /* split floor: a call whose selection has P pages
                                 (over all sequences and KV heads) runs on
                                 min(num_ctas, ceil(P / this)) CTAs; 0 = default
@@ -162,7 +166,22 @@ typedef struct {
                                 (then at most 4 rows per KV head;
                                 DA_ERR_UNSUPPORTED otherwise).                   */
   float   side_scale;        /* > 0 and finite with side_fp8 = 1, else 0           */
-  int32_t reserved[2];       /* must be zero                                       */
+  int32_t cluster_ctas;      /* window mode: how the attention kernel splits the
+                                work.  0 = automatic: when num_ctas and
+                                min_pages_per_cta are 0 and one cluster per
+                                (sequence, KV head) fits on the GPU at once, the
+                                cluster partition (below) with as many CTAs per
+                                cluster (up to 16) as fit, else the flat one;
+                                -1 = always the flat partition (persistent CTAs
+                                take equal stretches of every head's pages and
+                                the last CTA of each head merges through the
+                                workspace); 1..16 = the cluster partition with
+                                that many CTAs per cluster: one thread-block
+                                cluster per (sequence, KV head), each CTA an
+                                equal share of that head's pages, the partial
+                                results merged through distributed shared
+                                memory.  Other modes: 0 or -1 (flat).          */
+  int32_t reserved[1];       /* must be zero                                       */
 } da_params;
 
 typedef struct {
@@ -173,7 +192,9 @@ typedef struct {
   int32_t engine;            /* DA_ENGINE_*                                        */
   int32_t stages;            /* shared-memory pipeline depth (pages in flight)     */
   int32_t smem_bytes;        /* dynamic shared memory of the split-KV kernel       */
-  int32_t reserved;
+  int32_t cluster_ctas;      /* CTAs per cluster of the cluster partition (window
+                                mode; the grid is batch * num_kv_heads clusters),
+                                0 for the flat partition (grid num_ctas)         */
   size_t  workspace_bytes;   /* what draft_attn_run needs                          */
 } da_plan_info;
 
@@ -298,7 +319,8 @@ int draft_attn_ring_block_table(int32_t* table, int64_t max_pages, const int32_t
  * deployment only.)
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    stream capture.  A failed lookup is not cached (the call returns
+ *    DA_ERR_CUDA and the next call tries again).
  *  - Returns DA_ERR_WORKSPACE_TOO_SMALL when the plan's workspace_bytes
  *    exceeds DA_STATIC_WORKSPACE_BYTES.
  *  - Every call shares the one array: each call first clears its counters

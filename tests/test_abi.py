@@ -105,16 +105,25 @@ def _ok_params(**kw):
     (dict(mode="fold", window=128, alpha=2.0, far_mix=0.5, k_ring_pages=3), 0),
     (dict(mode="full", k_ring_pages=5), -1),
     (dict(mode="window", window=200, k_ring_pages=5), -1),
+    # the cluster partition: window mode, 1..16 CTAs per cluster (-1 = flat)
+    (dict(mode="window", window=2048, cluster_ctas=16), 0),
+    (dict(mode="window", window=2048, cluster_ctas=1), 0),
+    (dict(mode="window", window=2048, cluster_ctas=-1), 0),
+    (dict(mode="window", window=2048, cluster_ctas=17), -1),
+    (dict(mode="window", window=2048, cluster_ctas=-2), -1),
+    (dict(mode="full", cluster_ctas=-1), 0),
+    (dict(mode="full", cluster_ctas=4), -1),
+    (dict(mode="fold", window=64, alpha=2.0, far_mix=0.5, cluster_ctas=2), -1),
+    (dict(mode="window", window=2048, cluster_ctas=4, num_ctas=20), -1),
 ])
 def test_check_params(kw, code):
     assert B.draft_attn_check_params(_ok_params(**kw)) == code
 
 
 def test_reserved_must_be_zero():
-    for i in range(2):
-        p = _ok_params()
-        p.reserved[i] = 1
-        assert B.draft_attn_check_params(p) == -1
+    p = _ok_params()
+    p.reserved[0] = 1
+    assert B.draft_attn_check_params(p) == -1
 
 
 def test_null_params_and_plan_rejected():
