@@ -187,7 +187,7 @@ class DraftLoop:
     """Caches of one workload shape plus, per mode, a plan and a CUDA graph of
     the draft loop (append one token, attend) x steps."""
 
-    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None):
+    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None, engine=0):
         from draft_attention_decode_b300 import binding as B
         self.B = B
         self.wl = wl
@@ -235,7 +235,7 @@ class DraftLoop:
         self.qpos = [p.expand(wl.batch, wl.n_q).contiguous() if wl.draft_steps else p
                      for p in self.pos]
         self.out = torch.empty_like(self.q[0])
-        self.plans = {m: self._plan(m) for m in modes}
+        self.plans = {m: self._plan(m, engine) for m in modes}
 
     def _plan(self, mode, engine=0):
         wl = self.wl
@@ -692,6 +692,9 @@ def run_ours(args, dist):
     others = None if args.no_workloads else all_workloads(
         dev, args, flush, dist, peak, ("fold_4x256k", "ragged_tree_16x8"))
     if others is not None:
+        if args.tc_rows:
+            others += all_workloads(dev, args, flush, dist, peak, ("ragged_tree_16x8",),
+                                    engine="tc05")
         others.append(fold_ring_row(dev, args, flush, dist, peak))
         others.append(fold_fp8_row(dev, args, flush, dist, peak))
         others.append(fold_fp8_row(dev, args, flush, dist, peak, engine="cuda_core"))
@@ -803,19 +806,22 @@ def context_sweep(dev, args, flush, dist, peak):
             "draft_loop_1m": loop}
 
 
-def all_workloads(dev, args, flush, dist, peak, names):
+def all_workloads(dev, args, flush, dist, peak, names, engine=0):
     """The other workloads, each mode's attention call replayed from a CUDA
-    graph (inputs resident, L2 flushed between replays)."""
+    graph (inputs resident, L2 flushed between replays); `engine` forces one
+    (e.g. "tc05") instead of the automatic choice."""
     table = []
     for name in names:
         wl = WL.WORKLOADS[name]
-        dl = DraftLoop(wl, dev, wl.modes)
+        dl = DraftLoop(wl, dev, wl.modes, engine=engine)
         for m in wl.modes:
             g = dl.capture(m)
             ms = median_replay(g, args.steps, args.warmup, flush, dist)
             nb = dl.kv_bytes(m)
+            info = dl.plans[m].info()
             table.append({"workload": name, "mode": m, "us": round(ms * 1e3, 2),
-                          "kv_bytes": nb, **rates(nb, ms, peak)})
+                          "kv_bytes": nb, **rates(nb, ms, peak),
+                          "engine": info["engine_name"], "cluster_ctas": info["cluster_ctas"]})
         dl.close()
         del dl
         torch.cuda.empty_cache()
@@ -920,7 +926,7 @@ def profile_loop(args):
         wl = WL.resized(wl, args.ctx)
     if args.ctx_cap:
         wl = WL.resized(wl, [min(c, args.ctx_cap) for c in wl.ctx])
-    dl = DraftLoop(wl, dev, (args.profile_loop,))
+    dl = DraftLoop(wl, dev, (args.profile_loop,), engine=args.engine)
     torch.cuda.synchronize()
     if args.side_fp8:
         # FOLD with the side cache as E4M3 codes: the attention call on the first
@@ -970,6 +976,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the FOLD 4x256K and ragged draft-tree timings")
+    ap.add_argument("--tc-rows", action="store_true",
+                    help="also time the ragged draft tree on the tcgen05 engine")
     ap.add_argument("--all", default=None, help="also time every workload; write JSON here")
     ap.add_argument("--profile-loop", default=None, metavar="MODE",
                     help="run the draft loop of --workload in MODE --reps times, untimed")
@@ -978,6 +986,8 @@ def main():
     ap.add_argument("--ctx-cap", type=int, default=0,
                     help="cap every context of the workload at this length (ragged batches)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--engine", default="auto", choices=("auto", "cuda_core", "mma", "tc05"),
+                    help="with --profile-loop: force this engine")
     ap.add_argument("--side-fp8", action="store_true",
                     help="with --profile-loop fold: the attention call over an E4M3 side cache")
     args = ap.parse_args()

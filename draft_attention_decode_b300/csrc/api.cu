@@ -469,6 +469,18 @@ int draft_attn_step(da_plan_t pl, const void* k_new, const void* v_new, const in
   int rc = prepare_run(pl, q, q_pos, ctx_lens, block_table, k_cache, v_cache, k_side, tree_mask,
                        out, workspace, workspace_bytes, &r);
   if (rc != DA_OK) return rc;
+  if (pl->choice.cluster > 0 && pl->choice.engine != DA_ENGINE_TC05 && n_new > 0 &&
+      n_new <= da::kMaxFusedNew) {
+    // The cluster partition appends the tokens itself: one launch per step.
+    r.a.k_new = k_new;
+    r.a.v_new = v_new;
+    r.a.new_pos = pos;
+    r.a.k_cache_w = k_cache;
+    r.a.v_cache_w = v_cache;
+    r.a.n_new = n_new;
+    r.a.inputs_ready = 0;
+    return launch_run(pl, r, stream);
+  }
   r.a.inputs_ready = n_new > 0 && pl->p.batch > 0;
   // The append runs first; the attention kernel is launched behind it with
   // programmatic dependent launch.  Its set-up, the block-table reads and the

@@ -68,10 +68,11 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   for (int u = 0; u < D / 64; ++u) {
     const int f = lane + 32 * u;
     const float x = to_f32<T>(kx[u]), y = to_f32<T>(ky[u]);
-    float c, s;
+    float c, s, xr, yr;
     rope_cos_sin(pos, a.turn_freq[f], c, s);
-    kc[f] = from_f32<T>(x * c - y * s);
-    kc[f + D / 2] = from_f32<T>(y * c + x * s);
+    rope_pair(x, y, c, s, xr, yr);
+    kc[f] = from_f32<T>(xr);
+    kc[f + D / 2] = from_f32<T>(yr);
     if (ks) {
       ks[f] = kx[u];
       ks[f + D / 2] = ky[u];

@@ -18,6 +18,7 @@ constexpr int kPage = 64;            // tokens per page (the only page size buil
 constexpr int kSwizzleRow = 128;     // bytes per row of a 128B-swizzled TMA box
 constexpr int kBoxBytes = kPage * kSwizzleRow;  // one 64-row x 128-byte box
 constexpr int kMaxBatch = 1024;
+constexpr int kMaxFusedNew = 8;      // tokens per sequence one fused draft step may append
 // Kernel variants (shared-memory layout): 0 CUDA cores, 1 tensor cores.
 // Both run two consumer warpgroups plus one producer warpgroup (only its
 // first warp works), launched at 168 registers per thread; the producer group
@@ -64,6 +65,15 @@ struct DecodeArgs {
   int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + ring_slot(P)
   int32_t k_ring_sp;    // pages of sinks at the head of each sequence's ring
   int32_t cluster;      // CTAs per cluster of the cluster partition (0: flat partition)
+  // Cluster partition, one draft step in one launch: n_new tokens per
+  // sequence to append (keys un-rotated, values, positions [B][n_new]) into
+  // the caches k_cache_w / v_cache_w before they are attended; 0: none.
+  const void* k_new;
+  const void* v_new;
+  const int32_t* new_pos;
+  void* k_cache_w;
+  void* v_cache_w;
+  int32_t n_new;
   float2 turn_freq[64];  // theta^(-2i/d) / 2pi as hi + lo floats, i < d/2
 };
 
@@ -170,6 +180,15 @@ __device__ __forceinline__ void rope_cos_sin(int32_t pos, float2 f, float& c, fl
   const float te = __fmaf_rn(p, f.x, -th);
   const float t = __fadd_rn(th, -rintf(th)) + (te + p * f.y);
   sincospif(2.f * t, &s, &c);
+}
+
+// Rotate-half RoPE of one pair: (x cos - y sin, y cos + x sin), each with one
+// product rounded and the other fused.  Every kernel that writes a rotated
+// key uses this, so that a key appended by any of them is the same bits.
+__device__ __forceinline__ void rope_pair(float x, float y, float c, float s, float& xr,
+                                          float& yr) {
+  xr = __fmaf_rn(x, c, -__fmul_rn(y, s));
+  yr = __fmaf_rn(y, c, __fmul_rn(x, s));
 }
 
 // ---------------------------------------------------------------------------
@@ -324,11 +343,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// L2 policy for data read once (the KV stream): evict first.
+// L2 policy for data read once (the KV stream of full, FOLD and SharpDraft
+// attention): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+// L2 policy for a window's keys, which the next draft step reads again (all
+// but one token): normal eviction.
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// The policy for the KV loads of `mode`.
+__device__ __forceinline__ uint64_t kv_policy(int mode) {
+  return mode == DA_MODE_WINDOW ? policy_evict_normal() : policy_evict_first();
 }
 
 template <int N>
@@ -441,6 +472,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+// The two halves of the cluster barrier: every thread arrives once (release)
+// and, before it depends on the other CTAs, waits once (acquire).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"

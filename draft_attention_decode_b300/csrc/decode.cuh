@@ -1321,15 +1321,26 @@ template <typename T, int D, int RK, int NCT>
 __device__ inline void recv_merge(const DecodeArgs& a, const Smem& s, int b, int h) {
   constexpr int C4 = D / 4;
   constexpr int64_t SF = slot_floats(RK, D);
+  constexpr int kBatch = 8;   // slots whose loads are in flight together
   const int cn = (int)cluster_size();
   for (int item = threadIdx.x; item < a.R * C4; item += NCT) {
     const int r = item / C4, c4 = item - r * C4;
     MergeState st;
     st.init();
-    for (int k = 0; k < cn; ++k) {
-      const float* slot = s.recv + k * SF;
-      st.add(slot[r], slot[RK + r],
-             *reinterpret_cast<const float4*>(slot + slot_o_off(RK) + r * D + 4 * c4));
+    for (int k0 = 0; k0 < cn; k0 += kBatch) {
+      float mm[kBatch], ll[kBatch];
+      float4 oo[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int k = k0 + u;
+        const float* slot = s.recv + k * SF;
+        mm[u] = k < cn ? slot[r] : -INFINITY;
+        ll[u] = k < cn ? slot[RK + r] : 0.f;
+        oo[u] = k < cn ? *reinterpret_cast<const float4*>(slot + slot_o_off(RK) + r * D + 4 * c4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) st.add(mm[u], ll[u], oo[u]);
     }
     float res[4];
 #pragma unroll
@@ -1338,6 +1349,145 @@ __device__ inline void recv_merge(const DecodeArgs& a, const Smem& s, int b, int
     T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + 4 * c4;
     store4<T>(out, res);
   }
+}
+
+// Cluster partition, before the wait for the predecessor: L2 prefetches of
+// the small inputs this CTA reads first (its sequence's context length, new
+// positions and query positions, its KV head's query rows and new tokens).
+// A prefetch returns nothing to the SM and L2 is the point of coherence, so
+// the loads after the wait still see the predecessor's writes; they only
+// find the lines closer.  One warp.
+template <typename T, int D>
+__device__ inline void prefetch_head_inputs(const DecodeArgs& a, int b, int h) {
+  const int lane = threadIdx.x & 31;
+  const char* const q = static_cast<const char*>(a.q);
+  constexpr int ROWB = D * (int)sizeof(T);
+  const int qlines = a.n_q * ((a.G * ROWB + 127) / 128);
+  for (int i = lane; i < qlines; i += 32) {
+    const int t = i / ((a.G * ROWB + 127) / 128), l = i - t * ((a.G * ROWB + 127) / 128);
+    prefetch_l2(q + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G) * ROWB + l * 128);
+  }
+  if (a.n_new > 0) {
+    const int nl = 2 * a.n_new * ((ROWB + 127) / 128);
+    for (int i = lane; i < nl; i += 32) {
+      const int kv = i & 1, rest = i >> 1;
+      const int j = rest / ((ROWB + 127) / 128), l = rest - j * ((ROWB + 127) / 128);
+      const char* src = static_cast<const char*>(kv ? a.v_new : a.k_new);
+      prefetch_l2(src + ((int64_t)(b * a.n_new + j) * a.H_kv + h) * ROWB + l * 128);
+    }
+  }
+  if (lane == 0) {
+    prefetch_l2(a.ctx_lens + b);
+    prefetch_l2(a.q_pos + (int64_t)b * a.n_q);
+    if (a.n_new > 0) prefetch_l2(a.new_pos + (int64_t)b * a.n_new);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One launch per draft step (cluster partition): the step's new tokens are
+// appended by the attention kernel itself.  A spare warp of every CTA writes
+// its share of the new keys (rotated at their positions) and values of the
+// cluster's (sequence, KV head) to the caches, as the append kernel would;
+// the pages this step reads that hold a new token are loaded from the cache
+// as they were and have the token's rows replaced in shared memory, from a
+// copy the consumers computed at the start with the same arithmetic.  Keys
+// and values are therefore bit-identical to an append followed by the call.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__device__ inline void fused_append(const DecodeArgs& a, const Smem& s, int b, int h, uint32_t cr,
+                                    uint32_t cn) {
+  const int lane = threadIdx.x & 31;
+  for (int j = (int)cr; j < a.n_new; j += (int)cn) {
+    const int32_t pos = s.newpos[j];
+    if (pos < 0) continue;                          // padding
+    const int32_t pg = pos / kPage;
+    if (pg >= a.max_pages) {
+      if (lane == 0) atomicOr(a.status, DA_STATUS_BAD_POSITION);
+      continue;
+    }
+    const int32_t phys = __ldg(a.block_table + (int64_t)b * a.max_pages + pg);
+    if (phys < 0 || phys >= a.num_pages) {
+      if (lane == 0) atomicOr(a.status, DA_STATUS_BAD_PAGE);
+      continue;
+    }
+    const int64_t src = ((int64_t)(b * a.n_new + j) * a.H_kv + h) * D;
+    const int64_t dst = (((int64_t)phys * a.H_kv + h) * kPage + (pos - pg * kPage)) * D;
+    const T* k = static_cast<const T*>(a.k_new) + src;
+    const T* v = static_cast<const T*>(a.v_new) + src;
+    T* kc = static_cast<T*>(a.k_cache_w) + dst;
+    T* vc = static_cast<T*>(a.v_cache_w) + dst;
+#pragma unroll
+    for (int u = 0; u < D / 64; ++u) {
+      const int f = lane + 32 * u;
+      float c, sn, xr, yr;
+      rope_cos_sin(pos, s.invf[f], c, sn);
+      rope_pair(to_f32<T>(k[f]), to_f32<T>(k[f + D / 2]), c, sn, xr, yr);
+      kc[f] = from_f32<T>(xr);
+      kc[f + D / 2] = from_f32<T>(yr);
+      vc[f] = v[f];
+      vc[f + D / 2] = v[f + D / 2];
+    }
+  }
+}
+
+// Consumers: the rotated key and the value of every new token of sequence b,
+// KV head h, into s.newkv (one consumer warp per token).
+template <typename T, int D>
+__device__ inline void stage_new_tokens(const DecodeArgs& a, const Smem& s, int b, int h) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < a.n_new) {
+    const int32_t pos = s.newpos[warp];
+    if (pos >= 0) {
+      const int64_t src = ((int64_t)(b * a.n_new + warp) * a.H_kv + h) * D;
+      const T* k = static_cast<const T*>(a.k_new) + src;
+      const T* v = static_cast<const T*>(a.v_new) + src;
+      T* dk = reinterpret_cast<T*>(s.newkv) + (size_t)warp * 2 * D;
+      T* dv = dk + D;
+#pragma unroll
+      for (int u = 0; u < D / 64; ++u) {
+        const int f = lane + 32 * u;
+        float c, sn, xr, yr;
+        rope_cos_sin(pos, s.invf[f], c, sn);
+        rope_pair(to_f32<T>(k[f]), to_f32<T>(k[f + D / 2]), c, sn, xr, yr);
+        dk[f] = from_f32<T>(xr);
+        dk[f + D / 2] = from_f32<T>(yr);
+        dv[f] = v[f];
+        dv[f + D / 2] = v[f + D / 2];
+      }
+    }
+  }
+  named_barrier(1, kConsumerThreads);
+}
+
+// Consumers, after stage st landed: the new tokens it holds replace their
+// rows of the staged keys and values (128-byte swizzled boxes); every
+// consumer thread reads the same mask, so the barrier is met by all or none.
+template <typename T, int D, int NCT>
+__device__ inline void patch_new_tokens(const Smem& s, const Layout& L, uint32_t st) {
+  const uint32_t nm = s.pnew[st];
+  if (nm == 0) return;
+  constexpr int ROWB = D * (int)sizeof(T);       // bytes of one key or value row
+  constexpr int NCB = ROWB / kSwizzleRow;        // 128-byte boxes per row
+  constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
+  if (threadIdx.x < 32) {
+    uint8_t* kst = s.stage + st * L.stage_bytes;
+    uint8_t* vst = kst + NCB * kBoxBytes;
+    uint32_t m = nm;
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      const int slot = s.newpos[j] & (kPage - 1);
+      const uint8_t* src = s.newkv + (size_t)j * 2 * ROWB;
+      for (int c = threadIdx.x; c < 2 * CPR; c += 32) {
+        const int kv = c / CPR, cc = c - kv * CPR;
+        const int box = cc >> 3, ch16 = cc & 7;
+        uint8_t* dst = (kv ? vst : kst) + box * kBoxBytes + slot * kSwizzleRow +
+                       ((ch16 ^ (slot & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src + kv * ROWB + cc * 16);
+      }
+    }
+  }
+  named_barrier(1, NCT);
 }
 
 // Rows of (b, h) whose selection is empty get a zero output (nobody merges
@@ -1394,14 +1544,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t Lb = 0;
   if constexpr (CLUSTER) {
     // No page prefix: the CTA knows its (sequence, KV head) from its cluster
-    // and its pages from that one context length, read by every thread.
-    cluster_start<D, NCW>(a, s, L);
+    // and its pages from that one context length, read by every thread (the
+    // load is issued first, so that its latency overlaps the set-up).
     cr = cluster_rank();
     const uint32_t cn = cluster_size();
     const int bh = (int)(blockIdx.x / cn);
     cb = bh / a.H_kv;
     ch = bh - cb * a.H_kv;
-    Lb = clamp_ctx(__ldg(a.ctx_lens + cb), a.max_pages, a.status);
+    // Inputs known to be ready (behind this library's append kernel) are read
+    // at once; otherwise the set-up overlaps the predecessor's tail and every
+    // global access waits for it.
+    int32_t Lraw = a.inputs_ready ? __ldg(a.ctx_lens + cb) : 0;
+    if (!a.inputs_ready && threadIdx.x < 32) prefetch_head_inputs<T, D>(a, cb, ch);
+    cluster_start<D, NCW>(a, s, L);
+    if (!a.inputs_ready) {
+      grid_dep_wait();
+      Lraw = __ldg(a.ctx_lens + cb);
+    }
+    if (a.n_new > 0) {   // one launch for the draft step: the new tokens' positions
+      if (threadIdx.x < a.n_new) s.newpos[threadIdx.x] = __ldg(a.new_pos + cb * a.n_new + threadIdx.x);
+      __syncthreads();
+    }
+    Lb = clamp_ctx(Lraw, a.max_pages, a.status);
     s.len[cb] = Lb;   // query preparation reads it (every thread writes the same value)
     const Ranges rg = mode_ranges(a.mode, Lb, a.W, a.n_sink);
     const int64_t nb = range_pages(rg.k0[0], rg.k1[0]) + range_pages(rg.k0[1], rg.k1[1]) +
@@ -1423,8 +1587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer_head<ES, NCB, Engine::kSideF8>(a, s, L, cb, ch, Lb, xs, xe, &mk, &mv, &ms);
       else
         producer<ES, NCB, Engine::kSideF8>(a, s, L, xs, xe, &mk, &mv, &ms);
+    } else if (CLUSTER && warp == NCW + 1 && a.n_new > 0) {
+      fused_append<T, D>(a, s, cb, ch, cr, cluster_size());
     }
-    return;
+    return;   // arrived at the cluster barrier in cluster_start; nothing to wait for
   }
   regs_inc<kConsumerRegs>();
   Engine eng;
@@ -1436,6 +1602,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const dst_part =
       CLUSTER ? dsmem_ptr(s.recv + (size_t)cr * slot_floats(RK, D), 0u) : nullptr;
   bool wrote = false;
+  // A fused draft step: the new tokens' rotated keys and values, for pages
+  // that hold them (patched into the staged copy before they are read).
+  if constexpr (CLUSTER) {
+    if (a.n_new > 0) stage_new_tokens<T, D>(a, s, cb, ch);
+  }
   // The first piece's queries are prepared while its first pages load.
   if (xs < xe) {
     int32_t seq;
@@ -1456,6 +1627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st = n % L.stages;
     if (!mbar_wait(&s.full[st], (n / L.stages) & 1u, a.status, s.abort)) break;
     const PageInfo inf = s.info[st];
+    if constexpr (CLUSTER) {
+      if (a.n_new > 0) patch_new_tokens<T, D, NCT>(s, L, st);
+    }
     if ((inf.flags & kFirst) && x != xs) {
       prep_queries<T, D, RK, NCT, Engine::kFarScaleInQ>(a, s, inf.seq);
       if constexpr (Engine::kSideF8) eng.begin_far(s, (inf.seq & 1) == 0); else eng.begin(s);
@@ -1473,6 +1647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st1 = (n + 1) % L.stages;
         if (!mbar_wait(&s.full[st1], ((n + 1) / L.stages) & 1u, a.status, s.abort)) break;
         const PageInfo inf1 = s.info[st1];
+        if constexpr (CLUSTER) {
+          if (a.n_new > 0) patch_new_tokens<T, D, NCT>(s, L, st1);
+        }
         const uint32_t kb1 = base + st1 * L.stage_bytes;
         const uint32_t kb[2] = {kb0, kb1};
         const uint32_t vb[2] = {kb0 + NCB * kBoxBytes, kb1 + NCB * kBoxBytes};
@@ -1544,7 +1721,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Every consumer thread releases its stores into rank 0's slot and
     // arrives on rank 0's merge barrier; rank 0 merges once all have arrived
-    // (the other CTAs are done: nothing reads their shared memory).
+    // (the other CTAs are done: nothing reads their shared memory).  The
+    // cluster wait (every CTA arrived at its start) precedes the arrival.
+    __syncwarp();
+    cluster_wait();
     mbar_arrive_remote(s.merge_bar, 0u);
     if (cr == 0 && mbar_wait_cluster(s.merge_bar, 0u, a.status, s.abort))
       recv_merge<T, D, RK, NCT>(a, s, cb, ch);

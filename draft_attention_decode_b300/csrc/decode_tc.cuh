@@ -89,6 +89,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 lanes x 16 columns (thread i: lane base + i, columns col .. col + 15).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Scales 32 columns of TMEM (this warp's lanes) by the per-column factors f,
+// 16 columns at a time.
+__device__ __forceinline__ void tmem_scale32(uint32_t taddr, const float* f) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[16];
+    tmem_ld16(taddr + 16u * h, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f[16 * h + i]);
+    tmem_st16(taddr + 16u * h, v);
+  }
+}
+// Float maximum over a warp's lanes by the integer reduction (the bits of a
+// float map to an integer of the same order: negative values flipped).
+__device__ __forceinline__ float warp_max(float x) {
+  const int b = __float_as_int(x);
+  const int key = b >= 0 ? b : b ^ 0x7fffffff;
+  const int m = __reduce_max_sync(0xffffffffu, key);
+  return __int_as_float(m >= 0 ? m : m ^ 0x7fffffff);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -138,9 +180,15 @@ __device__ __forceinline__ bool barrier_or(int id, int threads, bool pred) {
 constexpr int kTcRows = 32;            // query rows the kernel computes (N of both MMAs)
 constexpr int kTcStageBytes = 65536;   // two pages of K and V, head_dim 128, bf16
 constexpr int kTcMaxStages = 3;
-constexpr uint32_t kTcCols = 128;      // TMEM: S^T A | S^T B | O^T A | O^T B
+constexpr uint32_t kTcCols = 256;      // TMEM: S^T A | S^T B | O^T A | O^T B | l A | l B
 constexpr int kPair = 8;               // PageInfo flag: the step holds two pages
 constexpr int kTcEndBarrier = 5;       // the MMA warp waits for the consumers before freeing TMEM
+// Register split of this kernel (launched at 168 per thread): the producer
+// warpgroup (TMA and MMA issue) keeps 72, the softmax warpgroups take 208:
+// 128 * 72 + 256 * 208 = 62464 <= 384 * 168.
+constexpr int kTcProducerRegs = 72;
+constexpr int kTcConsumerRegs = 208;
+static_assert(128 * kTcProducerRegs + 256 * kTcConsumerRegs <= 384 * 168, "register split");
 
 struct TcLayout {
   uint32_t stages, qb_off, pt_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
@@ -156,8 +204,9 @@ __host__ __device__ inline TcLayout make_tc_layout(int stages, int batch) {
                                                               // also query-prep scratch and
                                                               // the piece-end merge buffer
   L.info_off = off; off += align_up((uint32_t)stages * 2 * sizeof(PageInfo), 128);
-  L.bar_off = off;  off += 256;                               // 16 mbarriers, then the TMEM
-                                                              // address slot
+  L.bar_off = off;  off += 512;                               // 16 mbarriers, the TMEM
+                                                              // address slot, a 128-byte
+                                                              // tile of bf16 ones
   L.invf_off = off; off += align_up(64 * 8, 128);
   L.len_off = off;  off += align_up((uint32_t)batch * 4, 128);
   L.pfx_off = off;  off += align_up((uint32_t)(batch + 1) * 4, 128);
@@ -185,6 +234,7 @@ __host__ __device__ inline int tc_layout_check(const TcLayout& L, int stages, in
   // pair, q_full, drain; the TMEM slot after them, all before invf
   if (stages > kTcMaxStages) return 7;
   if (L.invf_off < L.bar_off + (2 * kTcMaxStages + 10) * 8 + 4) return 8;
+  if (L.invf_off < L.bar_off + 256 + 128) return 9;           // the ones tile
   if (L.mm_off < L.red_off + 2 * 4 * kTcRows * 4) return 5;
   if (L.total < L.mm_off + 4 * kTcRows * 4 + 1024) return 5;
   if (batch < 1) return 6;
@@ -205,6 +255,7 @@ struct TcSmem {
   uint64_t* q_full;  // [1]
   uint64_t* drain;   // [1]
   uint32_t* tslot;
+  uint8_t* ones;     // 128 bytes of bf16 1.0: the A operand of the row-sum MMA
   float* red;        // [2][4][32]
   float* mref;       // [2][32] reference maxima of each group
   float* alpha;      // [2][32] rescale factors of a raise
@@ -229,6 +280,7 @@ __device__ inline Smem tc_carve(uint8_t* raw, const TcLayout& L, TcSmem& t) {
   t.q_full = t.o_done + 2;
   t.drain = t.q_full + 1;
   t.tslot = reinterpret_cast<uint32_t*>(t.drain + 1);
+  t.ones = p + L.bar_off + 256;
   t.red = reinterpret_cast<float*>(p + L.red_off);
   t.mref = reinterpret_cast<float*>(p + L.mm_off);
   t.alpha = t.mref + 2 * kTcRows;
@@ -262,7 +314,7 @@ __device__ inline void tc_producer(const DecodeArgs& a, Smem& s, const TcSmem& t
                                    int64_t xs, int64_t xe, const CUtensorMap* mk,
                                    const CUtensorMap* mv, const CUtensorMap* ms) {
   const int lane = threadIdx.x & 31;
-  const uint64_t pol = policy_evict_first();
+  const uint64_t pol = kv_policy(a.mode);
   if (lane == 0) {
     prefetch_tmap(mk);
     prefetch_tmap(mv);
@@ -374,6 +426,8 @@ struct TcTmem {
   uint32_t base;
   __device__ __forceinline__ uint32_t s(int g) const { return base + 32u * g; }
   __device__ __forceinline__ uint32_t o(int g) const { return base + 64u + 32u * g; }
+  // row sums of P (every lane holds the same 32 sums)
+  __device__ __forceinline__ uint32_t l(int g) const { return base + 128u + 32u * g; }
 };
 
 __device__ __forceinline__ void tc_issue_qk(const TcSmem& t, const TcTmem& tm, uint32_t st, int g) {
@@ -399,25 +453,41 @@ __device__ __forceinline__ void tc_issue_pv(const TcSmem& t, const TcTmem& tm, u
     const uint64_t bd = tc_desc(pb + kk * 1024, 8192, 512, 4);
     tc_mma(tm.o(g), ad, bd, id, (acc || kk > 0) ? 1u : 0u);
   }
+  // l^T += 1 P^T: the probabilities' row sums accumulate on the tensor core
+  // beside O^T (every row of the all-ones A, read from one 128-byte tile with
+  // zero strides, is the same, so every TMEM lane holds the sums).
+  constexpr uint32_t idl = tc_idesc(128, kTcRows, 0, 1);
+  const uint64_t od = tc_desc(smem_u32(t.ones), 0, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t bd = tc_desc(pb + kk * 1024, 8192, 512, 4);
+    tc_mma(tm.l(g), od, bd, idl, (acc || kk > 0) ? 1u : 0u);
+  }
 }
 
-__device__ inline void tc_mma_thread(const DecodeArgs& a, Smem& s, const TcSmem& t, const TcTmem& tm,
-                                     uint32_t stages, int64_t xs, int64_t xe) {
-  uint32_t u = 0, ng[2] = {0u, 0u}, piece = 0;
-  bool fresh[2] = {true, true};
-  bool pend = false, pend_acc = false;
-  uint32_t pend_st = 0, pend_c = 0;
-  int pend_g = 0;
-  bool ok = true;
-  auto issue_pv = [&](uint32_t st, int g, uint32_t c, bool acc) {
-    if (!mbar_wait(&t.p_full[g], c & 1u, a.status, s.abort)) return false;
-    tc_fence_after();
-    tc_issue_pv(t, tm, st, g, acc);
-    tc_commit(&t.o_done[g]);
-    tc_commit(&t.empty[st]);
-    return true;
-  };
-  for (int64_t x = xs; x < xe && ok;) {
+// PV (and the row sums) of group g's step in stage st, once its P^T is
+// written (the group's c-th step); the commits release the stage and tell
+// the group its P^T buffer is free.
+__device__ __forceinline__ bool tc_pv_when_ready(const DecodeArgs& a, Smem& s, const TcSmem& t,
+                                                 const TcTmem& tm, uint32_t st, int g, uint32_t c,
+                                                 bool acc) {
+  if (!mbar_wait(&t.p_full[g], c & 1u, a.status, s.abort)) return false;
+  tc_fence_after();
+  tc_issue_pv(t, tm, st, g, acc);
+  tc_commit(&t.o_done[g]);
+  tc_commit(&t.empty[st]);
+  return true;
+}
+
+__device__ __forceinline__ void tc_mma_thread(const DecodeArgs& a, Smem& s, const TcSmem& t,
+                                           const TcTmem& tm, uint32_t stages, int64_t xs,
+                                           int64_t xe) {
+  uint32_t u = 0, ng0 = 0, ng1 = 0, piece = 0;
+  bool fresh0 = true, fresh1 = true;
+  // the previous step's PV, issued after the next step's QK^T (its P^T is
+  // being written meanwhile); bit 31 set = none pending
+  uint32_t pend = 1u << 31;
+  for (int64_t x = xs; x < xe;) {
     const uint32_t st = u % stages;
     if (!mbar_wait(&t.full[st], (u / stages) & 1u, a.status, s.abort)) break;
     const PageInfo ia = t.info[2 * st], ib = t.info[2 * st + 1];
@@ -426,29 +496,27 @@ __device__ inline void tc_mma_thread(const DecodeArgs& a, Smem& s, const TcSmem&
     if (ia.flags & kFirst) {
       if (!mbar_wait(t.q_full, piece & 1u, a.status, s.abort)) break;
       ++piece;
-      fresh[0] = fresh[1] = true;
+      fresh0 = fresh1 = true;
     }
     const int g = (int)(u & 1u);
-    const uint32_t c = ng[g];
+    const uint32_t c = g ? ng1 : ng0;
     if (c > 0 && !mbar_wait(&t.s_free[g], (c - 1) & 1u, a.status, s.abort)) break;
     tc_fence_after();
     tc_issue_qk(t, tm, st, g);
     tc_commit(&t.s_full[g]);
-    if (pend) {
-      if (!issue_pv(pend_st, pend_g, pend_c, pend_acc)) break;
-      pend = false;
+    if (!(pend >> 31)) {
+      // pend: stage (bits 0-7), group (8), count (9-29), accumulate (30)
+      if (!tc_pv_when_ready(a, s, t, tm, pend & 0xffu, (int)((pend >> 8) & 1u),
+                            (pend >> 9) & 0x1fffffu, ((pend >> 30) & 1u) != 0))
+        break;
+      pend = 1u << 31;
     }
-    const bool acc = !fresh[g];
-    fresh[g] = false;
-    ng[g] = c + 1;
+    const bool acc = g ? !fresh1 : !fresh0;
+    if (g) { fresh1 = false; ng1 = c + 1; } else { fresh0 = false; ng0 = c + 1; }
     if (last) {
-      if (!issue_pv(st, g, c, acc)) break;
+      if (!tc_pv_when_ready(a, s, t, tm, st, g, c, acc)) break;
     } else {
-      pend = true;
-      pend_st = st;
-      pend_g = g;
-      pend_c = c;
-      pend_acc = acc;
+      pend = st | ((uint32_t)g << 8) | ((c & 0x1fffffu) << 9) | ((uint32_t)acc << 30);
     }
     x += np;
     ++u;
@@ -490,6 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(t.drain, 1);
     fence_barrier_init();
   }
+  if (tid < 32) reinterpret_cast<uint32_t*>(t.ones)[tid] = 0x3F803F80u;   // bf16 1.0 pairs
+  fence_async_smem();
   if (warp == kConsumerWarps + 1) tmem_alloc(t.tslot, kTcCols);
   tc_fence_before();
   Layout pl{};        // the shared prologue's view: no stages of its own
@@ -517,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp >= kConsumerWarps) {
-    regs_dec<kProducerRegs>();
+    regs_dec<kTcProducerRegs>();
     if (warp == kConsumerWarps) {
       tc_producer(a, s, t, stages, xs, xe, &mk, &mv, &ms);
     } else if (warp == kConsumerWarps + 1) {
@@ -533,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
-  regs_inc<kConsumerRegs>();
+  regs_inc<kTcConsumerRegs>();
   if constexpr (!CLUSTER) zero_empty<T, D, NCT>(a, s);
   const int grp = warp >> 2;                 // softmax group
   const int gt = tid & 127;                  // thread in the group = key of the step, or dimension
@@ -543,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const alph = t.alpha + grp * RK;    // rescale factors of a raise
   bool wrote = false;
 
-  float l_part[RK];                          // this thread's key: probability sums per row
   uint32_t u = 0, ns[2] = {0u, 0u}, pages = 0;
   bool have[2] = {false, false};
   int64_t x = xs;
@@ -567,8 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(t.q_full);
       have[0] = have[1] = false;
       if (gt < RK) mref[gt] = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < RK; ++r) l_part[r] = 0.f;
       named_barrier(1, NCT);
     }
     const int g = (int)(u & 1u);
@@ -608,23 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // group-wide vote: a raise of the reference maxima (rare)
       if (barrier_or(3 + g, 128, need)) {
-        // exact row maxima over the group's keys: a reduce-scatter by max
-        // leaves lane r with row r's maximum over the warp's keys
-        float v[RK];
-#pragma unroll
-        for (int r = 0; r < RK; ++r) v[r] = sc[r];
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-          const bool up = (lane & m) != 0;
-#pragma unroll
-          for (int i = 0; i < m; ++i) {
-            const float send = up ? v[i] : v[i + m];
-            const float keep = up ? v[i + m] : v[i];
-            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
-          }
-        }
+        // exact row maxima over the group's keys: per warp by one integer
+        // reduction per row, then over the group's four warps
         float* red = t.red + g * 4 * RK;
-        red[(warp & 3) * RK + lane] = v[0];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) {
+          const float mx = warp_max(sc[r]);
+          if (lane == 0) red[(warp & 3) * RK + r] = mx;
+        }
         named_barrier(3 + g, 128);
         if (gt < RK) {
           const float mx = fmaxf(fmaxf(red[gt], red[RK + gt]), fmaxf(red[2 * RK + gt], red[3 * RK + gt]));
@@ -636,21 +694,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_barrier(3 + g, 128);
         bool any_alpha = false;
 #pragma unroll
-        for (int r = 0; r < RK; ++r) {
-          const float al = alph[r];
-          any_alpha |= al != 1.f;
-          l_part[r] *= al;
-        }
+        for (int r = 0; r < RK; ++r) any_alpha |= alph[r] != 1.f;
         if (have[g] && any_alpha) {
-          // O^T holds this piece's earlier PVs: scale it (thread gt = dimension gt)
+          // O^T and l^T hold this piece's earlier PVs: scale them (thread gt =
+          // dimension gt; every lane of l^T holds the same sums)
           ok = ok && mbar_wait(&t.o_done[g], (c - 1) & 1u, a.status, s.abort);
           if (ok) {
             tc_fence_after();
-            uint32_t o[RK];
-            tmem_ld32(tm.o(g) + lane_off, o);
-#pragma unroll
-            for (int r = 0; r < RK; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alph[r]);
-            tmem_st32(tm.o(g) + lane_off, o);
+            tmem_scale32(tm.o(g) + lane_off, alph);
+            tmem_scale32(tm.l(g) + lane_off, alph);
             tc_fence_before();
           }
         }
@@ -664,10 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p1 = sc[r + 1] > -INFINITY ? fast_exp2(sc[r + 1] - m4.y) : 0.f;
         const float p2 = sc[r + 2] > -INFINITY ? fast_exp2(sc[r + 2] - m4.z) : 0.f;
         const float p3 = sc[r + 3] > -INFINITY ? fast_exp2(sc[r + 3] - m4.w) : 0.f;
-        l_part[r] += p0;
-        l_part[r + 1] += p1;
-        l_part[r + 2] += p2;
-        l_part[r + 3] += p3;
         pw[r / 2] = pack_bf16(p0, p1);
         pw[r / 2 + 1] = pack_bf16(p2, p3);
       }
@@ -713,20 +761,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < RK; ++r) oo[r] = ok ? __uint_as_float(o[r]) : 0.f;
         mine = ok;
       }
-      // per-row sums of the group: reduce-scatter (lane r: the warp's row r)
+      // the group's row sums: every lane of l^T holds them; the group's
+      // thread 0 (lane 0 of its first warp) publishes them
+      if ((warp & 3) == 0 && mine) {   // a whole warp: tcgen05.ld is warp-wide
+        uint32_t lw[RK];
+        tmem_ld32(tm.l(grp) + lane_off, lw);
+        if (lane == 0) {
 #pragma unroll
-      for (int r = 0; r < RK; ++r) l_part[r] = mine ? l_part[r] : 0.f;
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        const bool up = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < m; ++i) {
-          const float send = up ? l_part[i] : l_part[i + m];
-          const float keep = up ? l_part[i + m] : l_part[i];
-          l_part[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          for (int r = 0; r < RK; ++r) t.red[grp * RK + r] = __uint_as_float(lw[r]);
         }
       }
-      t.red[grp * 4 * RK + (warp & 3) * RK + lane] = l_part[0];
+      if (gt < RK && !mine) t.red[grp * RK + gt] = 0.f;
       if (gt < RK && !mine) mref[gt] = -INFINITY;
       // group A's o for the merge goes to the P^T region ([row][dim]): every
       // PV of the piece has completed, so the region is free
@@ -751,9 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float oa = mob[r * D + gt];
           part[slot_o_off(RK) + r * D + gt] = (sa > 0.f ? sa * oa : 0.f) + (sb > 0.f ? sb * oo[r] : 0.f);
           if (gt == 0) {
-            const float la = t.red[r] + t.red[RK + r] + t.red[2 * RK + r] + t.red[3 * RK + r];
-            const float lb = t.red[4 * RK + r] + t.red[5 * RK + r] + t.red[6 * RK + r] +
-                             t.red[7 * RK + r];
+            const float la = t.red[r], lb = t.red[RK + r];
             part[r] = M;
             part[RK + r] = (sa > 0.f ? sa * la : 0.f) + (sb > 0.f ? sb * lb : 0.f);
           }

@@ -37,7 +37,8 @@ struct PageInfo {
 struct Layout {
   uint32_t stage_bytes, stages;
   uint32_t q_off, mo_off, ml_off, p_off, info_off, bar_off, invf_off, len_off, pfx_off, n0_off,
-      n01_off, flag_off, tm_off, rm_off, recv_off, recv_slots, mbar_off, total;
+      n01_off, flag_off, tm_off, rm_off, recv_off, recv_slots, mbar_off, pnew_off, newpos_off,
+      newkv_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -72,6 +73,11 @@ __host__ __device__ inline Layout make_layout(int variant, int es, int d, int rk
   L.recv_off = off;  L.recv_slots = (uint32_t)recv_slots;
   off += align_up((uint32_t)recv_slots * slot_floats(rk, d) * 4, 128);
   L.mbar_off = off;  off += recv_slots > 0 ? 128 : 0;   // the merge barrier
+  // cluster partition, a fused draft step: per stage the new tokens the page
+  // holds, the new positions, and the new tokens' keys (rotated) and values
+  L.pnew_off = off;   off += recv_slots > 0 ? align_up((uint32_t)stages * 4, 128) : 0;
+  L.newpos_off = off; off += recv_slots > 0 ? 128 : 0;
+  L.newkv_off = off;  off += recv_slots > 0 ? align_up((uint32_t)kMaxFusedNew * 2 * d * es, 128) : 0;
 
   L.total = off + 1024;  // slack to align the dynamic base to 1024 bytes
   return L;
@@ -111,6 +117,9 @@ __host__ __device__ inline int layout_check(const Layout& L, int variant, int es
       {L.rm_off, (uint32_t)rk * 4},
       {L.recv_off, L.recv_slots * (uint32_t)slot_floats(rk, d) * 4},
       {L.mbar_off, L.recv_slots ? 8u : 0u},
+      {L.pnew_off, L.recv_slots ? (uint32_t)stages * 4 : 0u},
+      {L.newpos_off, L.recv_slots ? (uint32_t)kMaxFusedNew * 4 : 0u},
+      {L.newkv_off, L.recv_slots ? (uint32_t)(kMaxFusedNew * 2 * d * es) : 0u},
   };
   constexpr int n = sizeof(r) / sizeof(r[0]);
   for (int i = 1; i < n; ++i) {
@@ -144,6 +153,9 @@ struct Smem {
   float* rmult;         // [rk] logit multiplier of each row of the current piece
   float* recv;          // cluster partition, rank 0: one partial slot per CTA of the cluster
   uint64_t* merge_bar;  // cluster partition, rank 0: every CTA's consumers arrive once filled
+  uint32_t* pnew;       // fused step: [stages] bit j = the page holds new token j
+  int32_t* newpos;      // fused step: [kMaxFusedNew] positions of the sequence's new tokens
+  uint8_t* newkv;       // fused step: [kMaxFusedNew][2][d] rotated keys and values (cache dtype)
 };
 
 __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
@@ -170,6 +182,9 @@ __device__ inline Smem carve(uint8_t* raw, const Layout& L) {
   s.rmult = reinterpret_cast<float*>(p + L.rm_off);
   s.recv = reinterpret_cast<float*>(p + L.recv_off);
   s.merge_bar = reinterpret_cast<uint64_t*>(p + L.mbar_off);
+  s.pnew = reinterpret_cast<uint32_t*>(p + L.pnew_off);
+  s.newpos = reinterpret_cast<int32_t*>(p + L.newpos_off);
+  s.newkv = p + L.newkv_off;
   return s;
 }
 
@@ -261,6 +276,7 @@ __device__ __forceinline__ Where locate(const Smem& s, int B, int H, int64_t x) 
 // Per-page fields the producer derives for flat position x.
 struct PageFields {
   int32_t seq, lohi, flags, phys, far, h, toff, kphys;
+  uint32_t newmask;   // fused step: the new tokens among the page's read keys
 };
 
 // Fields of page P (of range r of sequence b's KV head h), the page being
@@ -274,6 +290,7 @@ __device__ __forceinline__ PageFields page_fields(const DecodeArgs& a, const Sme
   const int32_t pk0 = P * kPage;
   const int32_t lo = max(k0, pk0) - pk0, hi = min(k1, pk0 + kPage) - pk0;
   PageFields f;
+  f.newmask = 0;
   f.h = h;
   f.seq = piece_seq(a.mode, b, h, a.H_kv, r);
   f.lohi = lo | (hi << 16);
@@ -299,7 +316,7 @@ __device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout&
                                      int64_t xe, const CUtensorMap* mk, const CUtensorMap* mv,
                                      const CUtensorMap* ms, Fields&& fields) {
   const int lane = threadIdx.x & 31;
-  const uint64_t pol = policy_evict_first();
+  const uint64_t pol = kv_policy(a.mode);
   if (lane == 0) {
     prefetch_tmap(mk);
     prefetch_tmap(mv);
@@ -311,10 +328,11 @@ __device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout&
     const int64_t x = base + lane;
     int32_t seq = 0, lohi = 0, flags = 0, phys = -1, far = 0, h = 0, toff = kNoTree;
     int32_t kphys = -1;   // page of the K array (the ring slot of a FOLD local page)
+    uint32_t newmask = 0;
     if (x < xe) {
       const PageFields f = fields(x);
       seq = f.seq; lohi = f.lohi; flags = f.flags; phys = f.phys; far = f.far; h = f.h;
-      toff = f.toff; kphys = f.kphys;
+      toff = f.toff; kphys = f.kphys; newmask = f.newmask;
     }
     const int cnt = (xe - base) < 32 ? (int)(xe - base) : 32;
     for (int j = 0; j < cnt; ++j) {
@@ -326,6 +344,7 @@ __device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout&
       const int32_t jh = __shfl_sync(0xffffffffu, h, j);
       const int32_t jtoff = __shfl_sync(0xffffffffu, toff, j);
       const int32_t jkphys = __shfl_sync(0xffffffffu, kphys, j);
+      const uint32_t jnew = __shfl_sync(0xffffffffu, newmask, j);
       int gave_up = 0;
       if (lane == 0) {
         const uint32_t st = n % L.stages;
@@ -336,6 +355,7 @@ __device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout&
         }
         if (mbar_wait(&s.empty[st], par ^ 1u, a.status, s.abort)) {
           s.info[st] = PageInfo{jseq, jlohi, jflags, jtoff};
+          if (L.recv_slots) s.pnew[st] = jnew;
           uint8_t* kdst = s.stage + st * L.stage_bytes;
           uint8_t* vdst = kdst + NCB * kBoxBytes;
           if (jflags & kValid) {
@@ -417,14 +437,26 @@ __device__ inline void producer_head(const DecodeArgs& a, Smem& s, const Layout&
     const int kr = k - (r == 0 ? 0 : (r == 1 ? n0 : n01));
     const bool first = x == k_lo || k == 0 || (fold && k == n0);
     const bool last = x == k_hi - 1 || k == nb - 1 || (fold && k == n0 - 1);
-    return page_fields(a, s, b, h, Lb, rg, r, kr, first, last);
+    PageFields f = page_fields(a, s, b, h, Lb, rg, r, kr, first, last);
+    if (a.n_new > 0 && (f.flags & kValid)) {   // a fused step: new tokens this page reads
+      const int32_t pk0 = (rg.lo(r) / kPage + kr) * kPage;
+      const int32_t lo = pk0 + (f.lohi & 0xffff), hi = pk0 + (f.lohi >> 16);
+      for (int j = 0; j < a.n_new; ++j) {
+        const int32_t p = s.newpos[j];
+        if (p >= lo && p < hi) f.newmask |= 1u << j;
+      }
+    }
+    return f;
   });
 }
 
 // Cluster partition start: barriers (the stage ring, and the merge barrier
 // that rank 0's consumers wait on: every consumer thread of every CTA of the
-// cluster arrives once), the angle table, flags; then a cluster barrier, so
-// that no CTA arrives on rank 0's merge barrier before rank 0 initialised it.
+// cluster arrives once), the angle table, flags; a CTA barrier; and the
+// arrival half of a cluster barrier, whose wait (cluster_wait, before a CTA
+// first touches rank 0's shared memory) guarantees that rank 0 initialised
+// its merge barrier.  Every thread of the CTA arrives here; only the
+// consumers wait (the producer and idle warps exit, which the barrier allows).
 template <int D, int NCW>
 __device__ inline void cluster_start(const DecodeArgs& a, Smem& s, const Layout& L) {
   const int tid = threadIdx.x;
@@ -440,8 +472,8 @@ __device__ inline void cluster_start(const DecodeArgs& a, Smem& s, const Layout&
     mbar_init(s.merge_bar, L.recv_slots * kConsumerThreads);
     fence_barrier_init();
   }
-  if (!a.inputs_ready) grid_dep_wait();
-  cluster_sync_all();
+  __syncthreads();
+  cluster_arrive();
 }
 
 }  // namespace da

@@ -93,7 +93,10 @@ def _ok_params(**kw):
     (dict(engine="mma"), 0),                           # 4 rows forced onto tensor cores
     (dict(engine="cuda_core", num_q_heads=64), 0),     # 8 rows forced onto CUDA cores
     (dict(engine="mma", dtype="fp32"), -2),            # tensor-core path is bf16 only
-    (dict(engine=3), -1),
+    (dict(engine=3), 0),                               # tcgen05 engine
+    (dict(engine=4), -1),
+    (dict(engine=3, head_dim=64), -2),
+    (dict(engine=3, dtype="fp32", num_q_heads=8), -2),
     (dict(tree_size=8), 0),
     (dict(tree_size=65), -1),
     (dict(tree_size=-1), -1),

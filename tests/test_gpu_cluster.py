@@ -41,8 +41,18 @@ def test_cluster_parity(cluster, shape, dtype, d):
     # ragged: a window well inside the context, one shorter than it, a single
     # key, an empty context, and a window of exactly one page boundary
     ctx = [3001, 129, 1, 0, 1024]
-    s = Setup(batch=len(ctx), n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=d, dtype=dtype,
-              ctx=ctx, mode="window", window=300, n_sink=4, cluster_ctas=cluster, seed=31)
+    rows = (h // hk) * nq
+    try:
+        s = Setup(batch=len(ctx), n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=d,
+                  dtype=dtype, ctx=ctx, mode="window", window=300, n_sink=4,
+                  cluster_ctas=cluster, seed=31)
+    except B.DraftAttnError as e:
+        # rank 0 keeps one partial per CTA of the cluster in shared memory:
+        # a forced size whose partials cannot fit is refused
+        rk = 8 if rows <= 8 and rows > 4 else (rows if rows <= 4 else (16 if rows <= 16 else 32))
+        slot = (((2 * rk + 3) // 4) * 4 + rk * d) * 4
+        assert e.code == B.DA_ERR_UNSUPPORTED and cluster * slot > 64 * 1024, (cluster, rows, d)
+        pytest.skip(f"{cluster} partials of {rows} rows do not fit in shared memory")
     assert s.da.info()["cluster_ctas"] == cluster
     out = s.run()
     compare(out, s.oracle(), dtype, f"cluster {cluster} {shape} {dtype} d{d}")
@@ -84,9 +94,14 @@ def test_cluster_tree_masks(shape, cluster):
     L0 = [2500, 40, 777]
     ctx = [c + nq for c in L0]
     q_pos = [[c + t for t in range(nq)] for c in L0]
-    s = Setup(batch=3, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
-              ctx=ctx, q_pos=q_pos, mode="window", window=300, n_sink=4, tree_size=nq,
-              cluster_ctas=cluster, seed=19)
+    try:
+        s = Setup(batch=3, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
+                  ctx=ctx, q_pos=q_pos, mode="window", window=300, n_sink=4, tree_size=nq,
+                  cluster_ctas=cluster, seed=19)
+    except B.DraftAttnError as e:
+        # 32 rows x 16 CTAs: rank 0 cannot hold 16 partials of 16 KB
+        assert e.code == B.DA_ERR_UNSUPPORTED and (h // hk) * nq * cluster > 256
+        pytest.skip("the cluster's partials do not fit in shared memory")
     masks = random_tree_masks(3, nq, 5)
     tm = torch.tensor(masks.view(np.int64), device=s.dev)
     compare(s.run(tree_mask=tm), s.oracle(tree_masks=masks), "bf16", f"tree cluster {cluster}")
@@ -154,4 +169,53 @@ def test_cluster_long_window_sampled():
     out = s.run()
     compare(out, s.oracle(groups=[(0, 0, g) for g in (0, 3, 7)]), "bf16", "1M-shape window")
     assert s.status() == (B.DA_OK, 0)
+    s.close()
+
+
+@pytest.mark.parametrize("n_new", [1, 2, 8, 9])
+def test_cluster_step_appends_in_one_launch(n_new):
+    """draft_attn_step on the cluster partition appends up to 8 tokens per
+    sequence inside the attention kernel (more go through the append kernel):
+    either way outputs and caches are bit-identical to draft_attn_append_kv
+    followed by draft_attn_run, with the new tokens read in the same call."""
+    L0 = [2000, 63, 777]
+    s = Setup(batch=3, n_q=1, num_q_heads=64, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=L0, mode="window", window=300, n_sink=4, extra_tokens=n_new, seed=37,
+              q_pos=[[c + n_new - 1] for c in L0])
+    assert s.da.info()["cluster_ctas"] >= 1
+    kc, vc = s.k_cache.clone(), s.v_cache.clone()
+    lens = torch.tensor([c + n_new for c in L0], dtype=torch.int32, device=s.dev)
+    k_new = torch.stack([s.k_raw[b][c:c + n_new] for b, c in enumerate(L0)]).contiguous()
+    v_new = torch.stack([s.v[b][c:c + n_new] for b, c in enumerate(L0)]).contiguous()
+    pos = torch.tensor([[c + j for j in range(n_new)] for c in L0], dtype=torch.int32,
+                       device=s.dev)
+    s.da.append_kv(k_new, v_new, pos, s.block_table, s.k_cache, s.v_cache, None)
+    want = s.run(ctx_lens=lens).clone()
+    got = s.da.step(k_new, v_new, pos, s.q, s.q_pos, lens, s.block_table, kc, vc, None)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    assert _same(kc, s.k_cache) and _same(vc, s.v_cache)
+    compare(got, s.oracle(ctx=[c + n_new for c in L0]), "bf16", f"step {n_new}")
+    assert s.status() == (B.DA_OK, 0)
+    s.close()
+
+
+def test_cluster_step_bad_position_sets_status():
+    """A new token past the block table: the one-launch step flags it (as the
+    append kernel does), writes nothing for it and still attends."""
+    L0 = [1000]
+    s = Setup(batch=1, n_q=1, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+              ctx=L0, mode="window", window=300, n_sink=4, extra_tokens=1, seed=41,
+              q_pos=[[1000]])
+    kc, vc = s.k_cache.clone(), s.v_cache.clone()
+    far = s.block_table.shape[1] * 64 + 5
+    pos = torch.tensor([[far]], dtype=torch.int32, device=s.dev)
+    k_new = s.k_raw[0][1000:1001].unsqueeze(0).contiguous()
+    v_new = s.v[0][1000:1001].unsqueeze(0).contiguous()
+    lens = torch.tensor(L0, dtype=torch.int32, device=s.dev)
+    got = s.da.step(k_new, v_new, pos, s.q, s.q_pos, lens, s.block_table, kc, vc, None)
+    torch.cuda.synchronize()
+    assert s.status() == (B.DA_ERR_DEVICE_FAULT, B.DA_STATUS_BAD_POSITION)
+    assert _same(kc, s.k_cache) and _same(vc, s.v_cache)
+    compare(got, s.oracle(), "bf16", "step, bad position")
     s.close()
