@@ -187,9 +187,10 @@ class DraftLoop:
     """Caches of one workload shape plus, per mode, a plan and a CUDA graph of
     the draft loop (append one token, attend) x steps."""
 
-    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None, engine=0):
+    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None, engine=0, tables_ready=0):
         from draft_attention_decode_b300 import binding as B
         self.B = B
+        self.tables_ready = tables_ready
         self.wl = wl
         self.dev = dev
         dt = wl.torch_dtype
@@ -245,7 +246,7 @@ class DraftLoop:
             num_pages=self.npg, max_pages_per_seq=self.bt.shape[1], dtype=wl.dtype, mode=mode,
             window=wl.window_for(mode), n_sink=wl.sinks_for(mode), alpha=wl.alpha,
             far_mix=wl.far_mix, scale_slope=wl.scale_slope, scale_ref=wl.scale_ref,
-            rope_theta=wl.rope_theta, engine=engine)
+            rope_theta=wl.rope_theta, engine=engine, tables_ready=self.tables_ready)
 
     # -- one draft loop through the C ABI --------------------------------
     def loop(self, mode, lens=None, fused=True):

@@ -72,7 +72,7 @@ class da_params(ctypes.Structure):
         ("side_fp8", ctypes.c_int32),
         ("side_scale", ctypes.c_float),
         ("cluster_ctas", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 1),
+        ("tables_ready", ctypes.c_int32),
     ]
 
 
@@ -147,7 +147,8 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
                 dtype="bf16", mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0,
                 scale_slope=0.0, scale_ref=4096, rope_theta=1e4, softmax_scale=0.0, num_ctas=0,
                 page_size=64, engine=0, min_pages_per_cta=0, stages=0, tree_size=0,
-                k_ring_pages=0, side_fp8=0, side_scale=0.0, cluster_ctas=0) -> da_params:
+                k_ring_pages=0, side_fp8=0, side_scale=0.0, cluster_ctas=0,
+                tables_ready=0) -> da_params:
     p = da_params()
     p.rope_theta = float(rope_theta)
     p.batch, p.n_q = int(batch), int(n_q)
@@ -165,6 +166,7 @@ def make_params(*, batch, n_q, num_q_heads, num_kv_heads, head_dim, num_pages, m
     p.k_ring_pages = int(k_ring_pages)
     p.side_fp8, p.side_scale = int(side_fp8), float(side_scale)
     p.cluster_ctas = int(cluster_ctas)
+    p.tables_ready = int(tables_ready)
     return p
 
 

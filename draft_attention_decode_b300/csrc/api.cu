@@ -117,6 +117,7 @@ void fill_args(const da_plan_s* pl, da::DecodeArgs* a) {
   a->k_ring = p.k_ring_pages;
   a->k_ring_sp = p.k_ring_pages > 0 ? ring_sink_pages(p) : 0;
   a->cluster = pl->choice.cluster;
+  a->tables_ready = p.tables_ready == 1 && pl->choice.engine != DA_ENGINE_TC05;
   for (int i = 0; i < 64; ++i) a->turn_freq[i] = pl->turn_freq[i];
 }
 
@@ -173,7 +174,7 @@ int draft_attn_check_params(const da_params* p) {
   if (p->tree_size > 0 && (p->mode == DA_MODE_WINDOW || p->mode == DA_MODE_FOLD) &&
       p->tree_size > p->window)
     return DA_ERR_INVALID_ARG;
-  if (p->reserved[0] != 0) return DA_ERR_INVALID_ARG;
+  if (p->tables_ready != 0 && p->tables_ready != 1) return DA_ERR_INVALID_ARG;
   if (p->cluster_ctas < -1 || p->cluster_ctas > 16) return DA_ERR_INVALID_ARG;
   if (p->cluster_ctas > 0 &&
       (p->mode != DA_MODE_WINDOW || p->num_ctas != 0 || p->min_pages_per_cta != 0))

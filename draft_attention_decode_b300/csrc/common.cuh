@@ -62,6 +62,12 @@ struct DecodeArgs {
   // this kernel start, so every input but the caches it writes may be read
   // before griddepcontrol.wait; only the producer's first cache load waits.
   int32_t inputs_ready;
+  // Nonzero when the caller promises that ctx_lens, block_table and new_pos
+  // were final before the previous kernel started: those are read (and the
+  // producer translates its first pages) before griddepcontrol.wait; the
+  // consumers still wait before they read queries, masks or new tokens, the
+  // producer before its first cache load.
+  int32_t tables_ready;
   int32_t k_ring;       // FOLD: rotated K of page P of sequence b at b * k_ring + ring_slot(P)
   int32_t k_ring_sp;    // pages of sinks at the head of each sequence's ring
   int32_t cluster;      // CTAs per cluster of the cluster partition (0: flat partition)

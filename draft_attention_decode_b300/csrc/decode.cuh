@@ -1317,34 +1317,43 @@ __device__ inline void cluster_merge(const DecodeArgs& a, int b, int h, uint32_t
 
 // Cluster partition, rank 0: merge of the partials every CTA of the cluster
 // stored into this CTA's receive slots.  Work items are (row, 4 dimensions).
+// The largest slot maximum is found first, so that the C slots' weights are
+// independent and their sums form short chains instead of one dependent
+// rescale after another.
 template <typename T, int D, int RK, int NCT>
 __device__ inline void recv_merge(const DecodeArgs& a, const Smem& s, int b, int h) {
   constexpr int C4 = D / 4;
-  constexpr int64_t SF = slot_floats(RK, D);
-  constexpr int kBatch = 8;   // slots whose loads are in flight together
+  constexpr int SF = slot_floats(RK, D);
+  constexpr int kMaxCluster = 16;
   const int cn = (int)cluster_size();
   for (int item = threadIdx.x; item < a.R * C4; item += NCT) {
     const int r = item / C4, c4 = item - r * C4;
-    MergeState st;
-    st.init();
-    for (int k0 = 0; k0 < cn; k0 += kBatch) {
-      float mm[kBatch], ll[kBatch];
-      float4 oo[kBatch];
+    float mk[kMaxCluster];
+    float M = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int k = k0 + u;
-        const float* slot = s.recv + k * SF;
-        mm[u] = k < cn ? slot[r] : -INFINITY;
-        ll[u] = k < cn ? slot[RK + r] : 0.f;
-        oo[u] = k < cn ? *reinterpret_cast<const float4*>(slot + slot_o_off(RK) + r * D + 4 * c4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) st.add(mm[u], ll[u], oo[u]);
+    for (int k = 0; k < kMaxCluster; ++k) {
+      mk[k] = k < cn ? s.recv[k * SF + r] : -INFINITY;
+      M = fmaxf(M, mk[k]);
     }
-    float res[4];
+    float l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) res[q] = st.l > 0.f ? st.o[q] / st.l : 0.f;
+      for (int k = 0; k < kMaxCluster; ++k) {
+        if (k < cn && mk[k] != -INFINITY) {
+          const float* slot = s.recv + k * SF;
+          const float w = fast_exp2(mk[k] - M);
+          const float4 v = *reinterpret_cast<const float4*>(slot + slot_o_off(RK) + r * D + 4 * c4);
+          l = fmaf(w, slot[RK + r], l);
+          o.x = fmaf(w, v.x, o.x);
+          o.y = fmaf(w, v.y, o.y);
+          o.z = fmaf(w, v.z, o.z);
+          o.w = fmaf(w, v.w, o.w);
+        }
+      }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float res[4] = {o.x * inv, o.y * inv, o.z * inv, o.w * inv};
     const int t = r / a.G, j = r - t * a.G;
     T* out = static_cast<T*>(a.out) + ((int64_t)(b * a.n_q + t) * a.H_q + h * a.G + j) * D + 4 * c4;
     store4<T>(out, res);
@@ -1551,18 +1560,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = (int)(blockIdx.x / cn);
     cb = bh / a.H_kv;
     ch = bh - cb * a.H_kv;
-    // Inputs known to be ready (behind this library's append kernel) are read
-    // at once; otherwise the set-up overlaps the predecessor's tail and every
-    // global access waits for it.
-    int32_t Lraw = a.inputs_ready ? __ldg(a.ctx_lens + cb) : 0;
+    // Inputs known to be ready (all but the caches behind this library's
+    // append kernel; the context lengths, positions and block table when the
+    // caller sets tables_ready) are read at once; otherwise the set-up overlaps
+    // the predecessor's tail and every global access waits for it.
+    const bool early = a.inputs_ready || a.tables_ready;
+    int32_t Lraw = early ? __ldg(a.ctx_lens + cb) : 0;
+    int32_t npos = 0;
+    if (early && threadIdx.x < a.n_new) npos = __ldg(a.new_pos + cb * a.n_new + threadIdx.x);
     if (!a.inputs_ready && threadIdx.x < 32) prefetch_head_inputs<T, D>(a, cb, ch);
     cluster_start<D, NCW>(a, s, L);
-    if (!a.inputs_ready) {
+    if (!early) {
       grid_dep_wait();
       Lraw = __ldg(a.ctx_lens + cb);
+      if (threadIdx.x < a.n_new) npos = __ldg(a.new_pos + cb * a.n_new + threadIdx.x);
     }
     if (a.n_new > 0) {   // one launch for the draft step: the new tokens' positions
-      if (threadIdx.x < a.n_new) s.newpos[threadIdx.x] = __ldg(a.new_pos + cb * a.n_new + threadIdx.x);
+      if (threadIdx.x < a.n_new) s.newpos[threadIdx.x] = npos;
       __syncthreads();
     }
     Lb = clamp_ctx(Lraw, a.max_pages, a.status);
@@ -1588,6 +1602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         producer<ES, NCB, Engine::kSideF8>(a, s, L, xs, xe, &mk, &mv, &ms);
     } else if (CLUSTER && warp == NCW + 1 && a.n_new > 0) {
+      if (a.tables_ready && !a.inputs_ready) grid_dep_wait();   // before the caches are written
       fused_append<T, D>(a, s, cb, ch, cr, cluster_size());
     }
     return;   // arrived at the cluster barrier in cluster_start; nothing to wait for
@@ -1596,6 +1611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Engine eng;
   eng.init();
   if constexpr (!Engine::kFarScaleInQ) eng.kscale = a.far_kscale;
+  // tables read early: the queries, masks, new tokens, the workspace and the
+  // output wait for the previous kernel
+  if (a.tables_ready && !a.inputs_ready) grid_dep_wait();
   if constexpr (!CLUSTER) zero_empty<T, D, NCT>(a, s);
   // cluster partition: this CTA's partial goes straight to its slot in rank
   // 0's shared memory

@@ -206,7 +206,7 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
   }
   // global memory from here on (the caches only after the producer's wait
   // when the inputs are known to be ready)
-  if (!a.inputs_ready) grid_dep_wait();
+  if (!a.inputs_ready && !a.tables_ready) grid_dep_wait();
   for (int b = tid; b < a.B; b += blockDim.x)
     s.len[b] = clamp_ctx(__ldg(a.ctx_lens + b), a.max_pages, a.status);
   // Small query tensors are pulled into L2 now, while the lengths load: the
@@ -236,6 +236,7 @@ __device__ inline void prologue(const DecodeArgs& a, Smem& s, const Layout& L) {
         s.n0[b] = n0;
         s.n01[b] = n01;
       }
+
       int32_t inc = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -349,7 +350,7 @@ __device__ inline void producer_loop(const DecodeArgs& a, Smem& s, const Layout&
       if (lane == 0) {
         const uint32_t st = n % L.stages;
         const uint32_t par = (n / L.stages) & 1u;
-        if (n == 0 && a.inputs_ready) {   // the append kernel's writes land first
+        if (n == 0 && (a.inputs_ready || a.tables_ready)) {   // the predecessor's writes land first
           grid_dep_wait();
           fence_proxy_async_global();
         }

@@ -181,7 +181,18 @@ typedef struct {
                                 equal share of that head's pages, the partial
                                 results merged through distributed shared
                                 memory.  Other modes: 0 or -1 (flat).          */
-  int32_t reserved[1];       /* must be zero                                       */
+  int32_t tables_ready;      /* 0 or 1.  1 promises that ctx_lens, block_table and
+                                draft_attn_step's pos hold their final values
+                                before the kernel issued just before this call
+                                on the stream starts (filled by the host, or by
+                                work that completes before that kernel begins).
+                                The attention kernel then reads them, and
+                                translates the block table, before it waits
+                                for that kernel (programmatic dependent launch);
+                                queries, tree masks, new tokens and the caches
+                                are still read only after the wait.  0: every
+                                input is read after the wait.  The tcgen05
+                                engine ignores it.                              */
 } da_params;
 
 typedef struct {

@@ -26,7 +26,7 @@ class Setup:
                  mode="full", window=0, n_sink=0, alpha=1.0, far_mix=0.0, scale_slope=0.0,
                  scale_ref=4096, rope_theta=1e4, num_ctas=0, seed=0, extra_tokens=0,
                  spare_pages=3, q_pos=None, fill=True, engine=0, tree_size=0,
-                 side_fp8_scale=0.0, cluster_ctas=0):
+                 side_fp8_scale=0.0, cluster_ctas=0, tables_ready=0):
         self.dev = torch.device("cuda", 0)
         self.dtype = dtype
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -53,7 +53,7 @@ class Setup:
             scale_slope=scale_slope, scale_ref=scale_ref, rope_theta=rope_theta,
             num_ctas=num_ctas, engine=engine, tree_size=tree_size,
             side_fp8=1 if side_fp8_scale > 0 else 0, side_scale=side_fp8_scale,
-            cluster_ctas=cluster_ctas)
+            cluster_ctas=cluster_ctas, tables_ready=tables_ready)
         shape = (npg, num_kv_heads, WL.PAGE, head_dim)
         # NaN-filled so that a read of a slot nobody wrote shows up in the output
         self.k_cache = torch.full(shape, float("nan"), dtype=tdt, device=self.dev)

@@ -123,10 +123,11 @@ def test_check_params(kw, code):
     assert B.draft_attn_check_params(_ok_params(**kw)) == code
 
 
-def test_reserved_must_be_zero():
+@pytest.mark.parametrize("v,code", [(0, 0), (1, 0), (2, -1), (-1, -1)])
+def test_tables_ready_is_a_flag(v, code):
     p = _ok_params()
-    p.reserved[0] = 1
-    assert B.draft_attn_check_params(p) == -1
+    p.tables_ready = v
+    assert B.draft_attn_check_params(p) == code
 
 
 def test_null_params_and_plan_rejected():
@@ -145,14 +146,14 @@ def test_struct_layout_matches_header(tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "draft_attn.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(da_params),"
-        " offsetof(da_params, side_scale), offsetof(da_params, reserved),"
+        " offsetof(da_params, side_scale), offsetof(da_params, tables_ready),"
         " sizeof(da_plan_info), offsetof(da_plan_info, workspace_bytes));return 0;}\n")
     exe = tmp_path / "layout"
     inc = os.path.join(os.path.dirname(B.HEADER))
     subprocess.run(["gcc", f"-I{inc}", str(src), "-o", str(exe)], check=True)
     got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     want = [ctypes.sizeof(B.da_params), B.da_params.side_scale.offset,
-            B.da_params.reserved.offset, ctypes.sizeof(B.da_plan_info),
+            B.da_params.tables_ready.offset, ctypes.sizeof(B.da_plan_info),
             B.da_plan_info.workspace_bytes.offset]
     assert [int(x) for x in got] == want
 

@@ -138,3 +138,46 @@ def test_step_error_leaves_cache_untouched():
     torch.cuda.synchronize()
     assert _same(kc, s.k_cache)          # unwritten slots hold NaN
     s.close()
+
+
+@pytest.mark.parametrize("mode,kw,cluster", [
+    ("full", {}, 0), ("window", dict(window=300, n_sink=4), 0),
+    ("window", dict(window=300, n_sink=4), -1), ("fold", dict(window=200, alpha=2.0, far_mix=0.5), 0)],
+    ids=["full", "window-cluster", "window-flat", "fold"])
+@pytest.mark.parametrize("shape", [(32, 8, 1), (64, 8, 1)], ids=["r4", "r8"])
+def test_tables_ready_changes_nothing(mode, kw, cluster, shape):
+    """tables_ready = 1 lets the attention kernel read the context lengths,
+    positions and block table before it waits for the previous kernel.  A
+    draft loop of back-to-back steps (each kernel may start while the one
+    before it still appends and attends) gives outputs and caches bit-identical
+    to the same loop without it."""
+    h, hk, nq = shape
+    L0 = [2000, 63, 777]
+    steps = 4
+    outs, caches = [], []
+    for tr in (0, 1):
+        s = Setup(batch=3, n_q=nq, num_q_heads=h, num_kv_heads=hk, head_dim=128, dtype="bf16",
+                  ctx=L0, mode=mode, extra_tokens=steps, seed=31, cluster_ctas=cluster,
+                  tables_ready=tr, **kw)
+        qs = [WL.randn(tuple(s.q.shape), s.q.dtype, s.dev, 900 + st) for st in range(steps)]
+        k_new = [torch.stack([s.k_raw[b][c + st:c + st + 1] for b, c in enumerate(L0)]).contiguous()
+                 for st in range(steps)]
+        v_new = [torch.stack([s.v[b][c + st:c + st + 1] for b, c in enumerate(L0)]).contiguous()
+                 for st in range(steps)]
+        pos = [torch.tensor([[c + st] for c in L0], dtype=torch.int32, device=s.dev)
+               for st in range(steps)]
+        lens = [torch.tensor([c + st + 1 for c in L0], dtype=torch.int32, device=s.dev)
+                for st in range(steps)]
+        res = [torch.empty_like(s.q) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for st in range(steps):   # no host work or other kernel between the steps
+            s.da.step(k_new[st], v_new[st], pos[st], qs[st], pos[st], lens[st], s.block_table,
+                      s.k_cache, s.v_cache, s.k_side, out=res[st])
+        torch.cuda.synchronize()
+        assert s.status() == (B.DA_OK, 0)
+        outs.append([r.clone() for r in res])
+        caches.append((s.k_cache.clone(), s.v_cache.clone()))
+        s.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    assert _same(caches[0][0], caches[1][0]) and _same(caches[0][1], caches[1][1])
