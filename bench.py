@@ -249,11 +249,13 @@ class DraftLoop:
             rope_theta=wl.rope_theta, engine=engine, tables_ready=self.tables_ready)
 
     # -- one draft loop through the C ABI --------------------------------
-    def loop(self, mode, lens=None, fused=True):
+    def loop(self, mode, lens=None, fused=True, reps=1):
         """fused: each draft step is one draft_attn_step launch (append +
-        attend); otherwise draft_attn_append_kv then draft_attn_run."""
+        attend); otherwise draft_attn_append_kv then draft_attn_run.  reps > 1
+        runs the steps again (the same tokens at the same positions: the same
+        work per step), to time the steps after the first."""
         da = self.plans[mode]
-        for s in range(self.steps):
+        for s in [s for _ in range(reps) for s in range(self.steps)]:
             L = self.lens[s] if lens is None else lens
             if self.wl.draft_steps and fused:
                 da.step(self.k_new[s], self.v_new[s], self.pos[s], self.q[s], self.qpos[s], L,
@@ -282,7 +284,7 @@ class DraftLoop:
                 tot += selected_keys(mode, Lb, wl.window_for(mode), wl.sinks_for(mode)) * per_tok
         return tot
 
-    def capture(self, mode, lens=None, fused=True):
+    def capture(self, mode, lens=None, fused=True, reps=1):
         g = torch.cuda.CUDAGraph()
         st = torch.cuda.Stream()
         st.wait_stream(torch.cuda.current_stream())
@@ -291,7 +293,7 @@ class DraftLoop:
         torch.cuda.current_stream().wait_stream(st)
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
-            self.loop(mode, lens, fused)
+            self.loop(mode, lens, fused, reps)
         torch.cuda.synchronize()
         return g
 
@@ -654,6 +656,28 @@ def run_ours(args, dist):
         two[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 3),
                   **rates(dl.kv_bytes(m), ms, peak)}
         del g2
+    # The steps after a loop's first (L2 flushed before each replay, so the
+    # first step reads its window from DRAM and starts behind the flush): the
+    # loop twice in one graph minus the loop once, per step; also with
+    # tables_ready = 1 (lengths, positions and block table read before the
+    # wait for the previous step), which this loop satisfies.
+    further = {}
+    for tr in (0, 1):
+        saved = dl.plans
+        if tr:
+            dl.tables_ready = 1
+            dl.plans = {m: dl._plan(m) for m in ("full", "window")}
+        for m in ("full", "window"):
+            t1 = median_replay(dl.capture(m), args.steps, args.warmup, flush, dist)
+            t2 = median_replay(dl.capture(m, reps=2), args.steps, args.warmup, flush, dist)
+            further[m + ("_tables_ready" if tr else "")] = {
+                "us_per_draft_step": round(t1 * 1e3 / dl.steps, 3),
+                "us_per_further_step": round((t2 - t1) * 1e3 / dl.steps, 3)}
+        if tr:
+            for p in dl.plans.values():
+                p.close()
+            dl.plans = saved
+            dl.tables_ready = 0
 
     # roofline of the dominant kernel: the full-mode attention call of the
     # last draft step, timed on its own launch stream
@@ -712,6 +736,7 @@ def run_ours(args, dist):
                   for m, r in res.items()},
         "window_speedup_vs_full": round(res["full"]["ms_per_loop"] / res["window"]["ms_per_loop"], 2),
         "modes_separate_append": two,
+        "loop_steps": further,
         "engines": engines,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -797,7 +822,9 @@ def context_sweep(dev, args, flush, dist, peak):
         g = dl.capture(m)
         ms = median_replay(g, args.steps, args.warmup, flush, dist)
         nb = dl.kv_bytes(m)
-        loop[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 2), **rates(nb, ms, peak)}
+        ms2 = median_replay(dl.capture(m, reps=2), args.steps, args.warmup, flush, dist)
+        loop[m] = {"us_per_draft_step": round(ms * 1e3 / dl.steps, 2),
+                   "us_per_further_step": round((ms2 - ms) * 1e3 / dl.steps, 2), **rates(nb, ms, peak)}
     dl.close()
     del dl
     torch.cuda.empty_cache()

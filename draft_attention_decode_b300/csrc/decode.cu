@@ -9,6 +9,19 @@ namespace da {
 bool choose_kernel(int dtype, int d, int rows, int batch, int mode, int engine_hint, int stages,
                    int max_smem, bool side_f8, Choice* c) {
   const int es = dtype == DA_DTYPE_BF16 ? 2 : 4;
+  // Automatic choice: 17..32 rows (draft trees over a GQA group) scanning a
+  // long selection (full, FOLD, SharpDraft) go to the tcgen05 kernel; measured
+  // on the ragged draft-tree workload it reads 0.90 of the copy bandwidth
+  // there against 0.86 on mma.sync.  A window's single short piece per CTA
+  // stays on mma.sync (0.55 against 0.46).
+  if (engine_hint == 0 && dtype == DA_DTYPE_BF16 && d == 128 && rows > 16 && rows <= kTcRows &&
+      !side_f8 && mode != DA_MODE_WINDOW && stages <= kTcMaxStages) {
+    Choice t = *c;
+    if (choose_kernel(dtype, d, rows, batch, mode, 3, stages, max_smem, side_f8, &t)) {
+      *c = t;
+      return true;
+    }
+  }
   if (engine_hint == 3) {
     // the tcgen05 kernel: bf16, head_dim 128, up to 32 rows, no FP8 side cache
     if (dtype != DA_DTYPE_BF16 || d != 128 || rows > kTcRows || side_f8) return false;
