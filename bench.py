@@ -187,10 +187,12 @@ class DraftLoop:
     """Caches of one workload shape plus, per mode, a plan and a CUDA graph of
     the draft loop (append one token, attend) x steps."""
 
-    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None, engine=0, tables_ready=0):
+    def __init__(self, wl: WL.Workload, dev, modes, cache_ctx=None, engine=0, tables_ready=0,
+                 cluster_ctas=0):
         from draft_attention_decode_b300 import binding as B
         self.B = B
         self.tables_ready = tables_ready
+        self.cluster_ctas = cluster_ctas
         self.wl = wl
         self.dev = dev
         dt = wl.torch_dtype
@@ -246,7 +248,8 @@ class DraftLoop:
             num_pages=self.npg, max_pages_per_seq=self.bt.shape[1], dtype=wl.dtype, mode=mode,
             window=wl.window_for(mode), n_sink=wl.sinks_for(mode), alpha=wl.alpha,
             far_mix=wl.far_mix, scale_slope=wl.scale_slope, scale_ref=wl.scale_ref,
-            rope_theta=wl.rope_theta, engine=engine, tables_ready=self.tables_ready)
+            rope_theta=wl.rope_theta, engine=engine, tables_ready=self.tables_ready,
+            cluster_ctas=self.cluster_ctas if mode == "window" else 0)
 
     # -- one draft loop through the C ABI --------------------------------
     def loop(self, mode, lens=None, fused=True, reps=1):
@@ -608,11 +611,16 @@ def e2e_full(dl: DraftLoop, steps, warmup, dist):
     for _ in range(warmup):
         one()
     torch.cuda.synchronize(); dist.barrier(); torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    # each loop ends in a host read of its outputs, so loops are timed one by
+    # one on the host clock; the median of them (host jitter between loops is
+    # not the path's)
+    times = []
     for _ in range(steps):
+        t0 = time.perf_counter()
         one()
+        times.append(time.perf_counter() - t0)
     torch.cuda.synchronize(); dist.barrier(); torch.cuda.synchronize()
-    dt = dist.max((time.perf_counter() - t0) / steps)
+    dt = dist.max(statistics.median(times))
     return dt, h2d, d2h
 
 
@@ -706,7 +714,7 @@ def run_ours(args, dist):
                round(ms_mma * 1e3, 2), "note": "attention call alone, full mode; the default "
                "keeps <= 4 rows per KV head on the CUDA cores"}
 
-    e2e_s, h2d, d2h = e2e_full(dl, max(args.steps // 4, 5), args.warmup, dist)
+    e2e_s, h2d, d2h = e2e_full(dl, max(args.steps, MIN_REPLAYS), args.warmup, dist)
     e2e_val = res["full"]["kv_bytes_per_loop"] / e2e_s / 1e9
     launches = dl.launches_per_loop(fused=True) * args.steps * 2
     dl.close()
@@ -744,7 +752,8 @@ def run_ours(args, dist):
                 "d2h_bytes_per_step": d2h,
                 "note": "full mode, pinned host buffers; per step (one 4-draft-step loop) one "
                         "H2D copy of all its inputs, four draft_attn_step calls, one D2H copy "
-                        "of the four outputs and a host sync, inside the timed region"},
+                        "of the four outputs and a host sync, inside the timed region; each "
+                        "loop timed on the host clock, the median of at least 50 loops"},
         "gpu_launches": launches,
         "clocks": clk,
         "sweep": sweep,
