@@ -976,7 +976,7 @@ def profile_loop(args):
             num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_pages=dl.npg,
             max_pages_per_seq=dl.bt.shape[1], dtype=wl.dtype, mode="fold", window=wl.window,
             alpha=wl.alpha, far_mix=wl.far_mix, rope_theta=wl.rope_theta, side_fp8=1,
-            side_scale=scale)
+            side_scale=scale, engine=args.engine)
         ks8 = torch.empty(dl.k_side.shape, dtype=torch.uint8, device=dev)
         for i in range(0, dl.k_side.shape[0], 1024):
             ks8[i:i + 1024] = (dl.k_side[i:i + 1024].float() / scale).to(
