@@ -1,7 +1,8 @@
 // Host-only check of the decode kernels' shared-memory layouts: every
-// (engine variant, element size, head_dim, rows, pipeline depth, batch) a
-// plan can pick must pass layout_check (alignment, extent and order of every
-// region), and every (depth, batch) of the tcgen05 kernel tc_layout_check.  Prints one line per failure and "ok <count>" at the end.
+// (engine variant, element size, head_dim, rows, pipeline depth, batch,
+// cluster receive slots) a plan can pick must pass layout_check (alignment,
+// extent and order of every region), and every (depth, batch) of the tcgen05
+// kernel tc_layout_check.  Prints one line per failure and "ok <count>" at the end.
 #include <cstdio>
 
 #include "decode_tc.cuh"
@@ -21,18 +22,21 @@ int main() {
     for (int d : {64, 128})
       for (int i = 0; i < v.nrk; ++i)
         for (int stages = 2; stages <= 8; ++stages)
-          for (int j = 0; j < nb; ++j) {
-            const int rk = v.rks[i], batch = batches[j];
-            const Layout L = make_layout(v.variant, v.es, d, rk, stages, batch);
-            const int rc = layout_check(L, v.variant, v.es, d, rk, stages, batch);
-            ++count;
-            if (rc != 0) {
-              ++bad;
-              if (bad < 20)
-                std::printf("bad layout: variant %d es %d d %d rk %d stages %d batch %d: check %d\n",
-                            v.variant, v.es, d, rk, stages, batch, rc);
+          for (int j = 0; j < nb; ++j)
+            // 0: the flat partition; otherwise the cluster partition with that
+            // many receive slots in rank 0
+            for (int recv : {0, 1, 2, 4, 8, 10, 16}) {
+              const int rk = v.rks[i], batch = batches[j];
+              const Layout L = make_layout(v.variant, v.es, d, rk, stages, batch, recv);
+              const int rc = layout_check(L, v.variant, v.es, d, rk, stages, batch, recv);
+              ++count;
+              if (rc != 0) {
+                ++bad;
+                if (bad < 20)
+                  std::printf("bad layout: variant %d es %d d %d rk %d stages %d batch %d recv %d: "
+                              "check %d\n", v.variant, v.es, d, rk, stages, batch, recv, rc);
+              }
             }
-          }
   // the tcgen05 kernel's own layout
   for (int stages = 2; stages <= kTcMaxStages; ++stages)
     for (int j = 0; j < nb; ++j) {
