@@ -762,16 +762,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mine = ok;
       }
       // the group's row sums: every lane of l^T holds them; the group's
-      // thread 0 (lane 0 of its first warp) publishes them
+      // thread 0 (lane 0 of its first warp) publishes them into the group's
+      // own part of red (the other group may still use its part for a raise
+      // in its last step)
+      float* const lred = t.red + grp * 4 * RK;
       if ((warp & 3) == 0 && mine) {   // a whole warp: tcgen05.ld is warp-wide
         uint32_t lw[RK];
         tmem_ld32(tm.l(grp) + lane_off, lw);
         if (lane == 0) {
 #pragma unroll
-          for (int r = 0; r < RK; ++r) t.red[grp * RK + r] = __uint_as_float(lw[r]);
+          for (int r = 0; r < RK; ++r) lred[r] = __uint_as_float(lw[r]);
         }
       }
-      if (gt < RK && !mine) t.red[grp * RK + gt] = 0.f;
+      if (gt < RK && !mine) lred[gt] = 0.f;
       if (gt < RK && !mine) mref[gt] = -INFINITY;
       // group A's o for the merge goes to the P^T region ([row][dim]): every
       // PV of the piece has completed, so the region is free
@@ -796,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float oa = mob[r * D + gt];
           part[slot_o_off(RK) + r * D + gt] = (sa > 0.f ? sa * oa : 0.f) + (sb > 0.f ? sb * oo[r] : 0.f);
           if (gt == 0) {
-            const float la = t.red[r], lb = t.red[RK + r];
+            const float la = t.red[r], lb = t.red[4 * RK + r];
             part[r] = M;
             part[RK + r] = (sa > 0.f ? sa * la : 0.f) + (sb > 0.f ? sb * lb : 0.f);
           }
