@@ -802,25 +802,39 @@ def context_sweep(dev, args, flush, dist, peak):
     base = WL.WORKLOADS["mtp_draft_1m"]
     wl = dataclasses.replace(base, draft_steps=0)
     dl = DraftLoop(wl, dev, ("full", "window"))
-    rows = []
-    for L in (131072, 262144, 524288, 1048576):
+    contexts = (131072, 262144, 524288, 1048576)
+    graphs = {}
+    for L in contexts:
         lens = torch.tensor([L], dtype=torch.int32, device=dev)
         qpos = torch.tensor([[L]], dtype=torch.int32, device=dev)
-        row = {"context": L}
         for m in ("full", "window"):
             da = dl.plans[m]
 
-            def call():
+            def call(da=da, qpos=qpos, lens=lens):
                 da.run(dl.q[0], qpos, lens, dl.bt, dl.k_cache, dl.v_cache, None, out=dl.out)
             call()
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 call()
-            ms = median_replay(g, args.steps, args.warmup, flush, dist)
+            graphs[(L, m)] = (g, lens, qpos)
+    # the contexts take turns, in rounds, so that a drift of the GPU's state
+    # during the sweep reaches every context alike; the median per context
+    times = {k: [] for k in graphs}
+    rounds = 5
+    per_round = (max(args.steps, MIN_REPLAYS) + rounds - 1) // rounds
+    for _ in range(rounds):
+        for k, (g, _, _) in graphs.items():
+            times[k] += time_graph(g, per_round, args.warmup, flush, dist)[1]
+    rows = []
+    for L in contexts:
+        row = {"context": L}
+        for m in ("full", "window"):
+            ms = dist.max(statistics.median(times[(L, m)]))
             nb = selected_keys(m, L, wl.window_for(m), wl.sinks_for(m)) * 2 * 8 * 128 * 2
             row[m] = {"us": round(ms * 1e3, 2), **rates(nb, ms, peak)}
         rows.append(row)
+    del graphs
     dl.close()
     del dl
     torch.cuda.empty_cache()
