@@ -803,29 +803,37 @@ def context_sweep(dev, args, flush, dist, peak):
     wl = dataclasses.replace(base, draft_steps=0)
     dl = DraftLoop(wl, dev, ("full", "window"))
     contexts = (131072, 262144, 524288, 1048576)
+    # One graph per mode reads the context length and query position from
+    # device tensors that are rewritten between contexts: every context is
+    # timed through the same graph instance (separately captured instances of
+    # the same call were seen to settle about 1.5 us apart), and the contexts
+    # take turns in rounds, so that a drift of the GPU's state reaches every
+    # context alike.  The median per context.
+    lens = torch.zeros(1, dtype=torch.int32, device=dev)
+    qpos = torch.zeros((1, 1), dtype=torch.int32, device=dev)
     graphs = {}
-    for L in contexts:
-        lens = torch.tensor([L], dtype=torch.int32, device=dev)
-        qpos = torch.tensor([[L]], dtype=torch.int32, device=dev)
-        for m in ("full", "window"):
-            da = dl.plans[m]
+    for m in ("full", "window"):
+        da = dl.plans[m]
 
-            def call(da=da, qpos=qpos, lens=lens):
-                da.run(dl.q[0], qpos, lens, dl.bt, dl.k_cache, dl.v_cache, None, out=dl.out)
+        def call(da=da):
+            da.run(dl.q[0], qpos, lens, dl.bt, dl.k_cache, dl.v_cache, None, out=dl.out)
+        lens.fill_(contexts[-1])
+        qpos.fill_(contexts[-1])
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
             call()
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                call()
-            graphs[(L, m)] = (g, lens, qpos)
-    # the contexts take turns, in rounds, so that a drift of the GPU's state
-    # during the sweep reaches every context alike; the median per context
-    times = {k: [] for k in graphs}
+        graphs[m] = g
+    times = {(L, m): [] for L in contexts for m in graphs}
     rounds = 5
     per_round = (max(args.steps, MIN_REPLAYS) + rounds - 1) // rounds
     for _ in range(rounds):
-        for k, (g, _, _) in graphs.items():
-            times[k] += time_graph(g, per_round, args.warmup, flush, dist)[1]
+        for L in contexts:
+            lens.fill_(L)
+            qpos.fill_(L)
+            for m, g in graphs.items():
+                times[(L, m)] += time_graph(g, per_round, args.warmup, flush, dist)[1]
     rows = []
     for L in contexts:
         row = {"context": L}
