@@ -381,13 +381,15 @@ struct CoreEngine {
     constexpr int NS = PAIR ? NIT / 2 : NIT;   // scores per lane
     const int kw = (warp & (GW - 1)) * KPW + kg;   // the lane's key on pass 0
     float sc[NS];
-    bool ok[NIT];
+    // bit it: the key of pass it is inside [lo, hi) of its page (a mask in one
+    // register rather than NIT predicates)
+    uint32_t okm = 0;
     float vp[PAIR ? 2 * RK : 1];   // PAIR: the even pass's partial sums
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int pg = it / PP, ps = it % PP;
       const int key = kw + KG * ps;
-      ok[it] = key >= lo[pg] && key < hi[pg];
+      okm |= (key >= lo[pg] && key < hi[pg]) ? 1u << it : 0u;
       // With turn-taking groups, two accumulators per row (even and odd element
       // pairs) halve the chain of dependent FFMA2s behind each dot product
       // (FOLD 4 x 256K 694 -> 686 us; the shared-step window engine is faster
@@ -447,13 +449,13 @@ struct CoreEngine {
         if (it & 1) sc[it >> 1] = reduce_scatter<2 * RK, LPK>(vp, ds);
       } else {
         const float sr = reduce_scatter<RK, LPK>(v, ds);
-        sc[it] = ok[it] ? sr : -INFINITY;
+        sc[it] = ((okm >> it) & 1u) ? sr : -INFINITY;
       }
     }
     if constexpr (PAIR) {
 #pragma unroll
       for (int j = 0; j < NS; ++j)
-        if (!((ds & 4) ? ok[2 * j + 1] : ok[2 * j])) sc[j] = -INFINITY;
+        if (!((okm >> (2 * j + ((ds & 4) ? 1 : 0))) & 1u)) sc[j] = -INFINITY;
     }
     // Draft-tree keys the row does not see (only pages that hold tree keys).
     bool has_tree = false;
@@ -510,7 +512,7 @@ struct CoreEngine {
 #pragma unroll
       for (int i = 0; i < NCH; ++i) {
         float f[EPC];
-        Chunk<T>::load(ok[it] ? vb[pg] + off_of(ps, i) : s.zero16, f);
+        Chunk<T>::load(((okm >> it) & 1u) ? vb[pg] + off_of(ps, i) : s.zero16, f);
 #pragma unroll
         for (int e = 0; e < EPC / 2; ++e) {
           const float2 vv = make_float2(f[2 * e], f[2 * e + 1]);
