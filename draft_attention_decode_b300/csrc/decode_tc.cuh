@@ -180,14 +180,15 @@ __device__ __forceinline__ bool barrier_or(int id, int threads, bool pred) {
 constexpr int kTcRows = 32;            // query rows the kernel computes (N of both MMAs)
 constexpr int kTcStageBytes = 65536;   // two pages of K and V, head_dim 128, bf16
 constexpr int kTcMaxStages = 3;
-constexpr uint32_t kTcCols = 256;      // TMEM: S^T A | S^T B | O^T A | O^T B | l A | l B
+constexpr uint32_t kTcCols = 128;      // TMEM: S^T A | S^T B | O^T A | O^T B
 constexpr int kPair = 8;               // PageInfo flag: the step holds two pages
 constexpr int kTcEndBarrier = 5;       // the MMA warp waits for the consumers before freeing TMEM
 // Register split of this kernel (launched at 168 per thread): the producer
-// warpgroup (TMA and MMA issue) keeps 72, the softmax warpgroups take 208:
-// 128 * 72 + 256 * 208 = 62464 <= 384 * 168.
-constexpr int kTcProducerRegs = 72;
-constexpr int kTcConsumerRegs = 208;
+// warpgroup (TMA and MMA issue) keeps 56, the softmax warpgroups take 224
+// (their scores, probabilities and row-sum shares): 128 * 56 + 256 * 224 =
+// 64512 = 384 * 168.
+constexpr int kTcProducerRegs = 56;
+constexpr int kTcConsumerRegs = 224;
 static_assert(128 * kTcProducerRegs + 256 * kTcConsumerRegs <= 384 * 168, "register split");
 
 struct TcLayout {
@@ -205,8 +206,7 @@ __host__ __device__ inline TcLayout make_tc_layout(int stages, int batch) {
                                                               // the piece-end merge buffer
   L.info_off = off; off += align_up((uint32_t)stages * 2 * sizeof(PageInfo), 128);
   L.bar_off = off;  off += 512;                               // 16 mbarriers, the TMEM
-                                                              // address slot, a 128-byte
-                                                              // tile of bf16 ones
+                                                              // address slot
   L.invf_off = off; off += align_up(64 * 8, 128);
   L.len_off = off;  off += align_up((uint32_t)batch * 4, 128);
   L.pfx_off = off;  off += align_up((uint32_t)(batch + 1) * 4, 128);
@@ -234,7 +234,6 @@ __host__ __device__ inline int tc_layout_check(const TcLayout& L, int stages, in
   // pair, q_full, drain; the TMEM slot after them, all before invf
   if (stages > kTcMaxStages) return 7;
   if (L.invf_off < L.bar_off + (2 * kTcMaxStages + 10) * 8 + 4) return 8;
-  if (L.invf_off < L.bar_off + 256 + 128) return 9;           // the ones tile
   if (L.mm_off < L.red_off + 2 * 4 * kTcRows * 4) return 5;
   if (L.total < L.mm_off + 4 * kTcRows * 4 + 1024) return 5;
   if (batch < 1) return 6;
@@ -255,7 +254,6 @@ struct TcSmem {
   uint64_t* q_full;  // [1]
   uint64_t* drain;   // [1]
   uint32_t* tslot;
-  uint8_t* ones;     // 128 bytes of bf16 1.0: the A operand of the row-sum MMA
   float* red;        // [2][4][32]
   float* mref;       // [2][32] reference maxima of each group
   float* alpha;      // [2][32] rescale factors of a raise
@@ -280,7 +278,6 @@ __device__ inline Smem tc_carve(uint8_t* raw, const TcLayout& L, TcSmem& t) {
   t.q_full = t.o_done + 2;
   t.drain = t.q_full + 1;
   t.tslot = reinterpret_cast<uint32_t*>(t.drain + 1);
-  t.ones = p + L.bar_off + 256;
   t.red = reinterpret_cast<float*>(p + L.red_off);
   t.mref = reinterpret_cast<float*>(p + L.mm_off);
   t.alpha = t.mref + 2 * kTcRows;
@@ -426,8 +423,6 @@ struct TcTmem {
   uint32_t base;
   __device__ __forceinline__ uint32_t s(int g) const { return base + 32u * g; }
   __device__ __forceinline__ uint32_t o(int g) const { return base + 64u + 32u * g; }
-  // row sums of P (every lane holds the same 32 sums)
-  __device__ __forceinline__ uint32_t l(int g) const { return base + 128u + 32u * g; }
 };
 
 __device__ __forceinline__ void tc_issue_qk(const TcSmem& t, const TcTmem& tm, uint32_t st, int g) {
@@ -453,19 +448,9 @@ __device__ __forceinline__ void tc_issue_pv(const TcSmem& t, const TcTmem& tm, u
     const uint64_t bd = tc_desc(pb + kk * 1024, 8192, 512, 4);
     tc_mma(tm.o(g), ad, bd, id, (acc || kk > 0) ? 1u : 0u);
   }
-  // l^T += 1 P^T: the probabilities' row sums accumulate on the tensor core
-  // beside O^T (every row of the all-ones A, read from one 128-byte tile with
-  // zero strides, is the same, so every TMEM lane holds the sums).
-  constexpr uint32_t idl = tc_idesc(128, kTcRows, 0, 1);
-  const uint64_t od = tc_desc(smem_u32(t.ones), 0, 0, 0);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t bd = tc_desc(pb + kk * 1024, 8192, 512, 4);
-    tc_mma(tm.l(g), od, bd, idl, (acc || kk > 0) ? 1u : 0u);
-  }
 }
 
-// PV (and the row sums) of group g's step in stage st, once its P^T is
+// PV of group g's step in stage st, once its P^T is
 // written (the group's c-th step); the commits release the stage and tell
 // the group its P^T buffer is free.
 __device__ __forceinline__ bool tc_pv_when_ready(const DecodeArgs& a, Smem& s, const TcSmem& t,
@@ -558,8 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(t.drain, 1);
     fence_barrier_init();
   }
-  if (tid < 32) reinterpret_cast<uint32_t*>(t.ones)[tid] = 0x3F803F80u;   // bf16 1.0 pairs
-  fence_async_smem();
   if (warp == kConsumerWarps + 1) tmem_alloc(t.tslot, kTcCols);
   tc_fence_before();
   Layout pl{};        // the shared prologue's view: no stages of its own
@@ -615,6 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint32_t u = 0, ns[2] = {0u, 0u}, pages = 0;
   bool have[2] = {false, false};
+  // this thread's share of its group's row sums: the probabilities of the
+  // keys it owned in the group's steps of the piece (summed over the group's
+  // threads at the piece's end)
+  float lsum[RK];
+#pragma unroll
+  for (int r = 0; r < RK; ++r) lsum[r] = 0.f;
   int64_t x = xs;
   // Every consumer thread takes the same path through the loop (the steps'
   // page information is read from shared memory by all), so that the named
@@ -635,6 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(t.q_full);
       have[0] = have[1] = false;
+#pragma unroll
+      for (int r = 0; r < RK; ++r) lsum[r] = 0.f;
       if (gt < RK) mref[gt] = -INFINITY;
       named_barrier(1, NCT);
     }
@@ -695,14 +686,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool any_alpha = false;
 #pragma unroll
         for (int r = 0; r < RK; ++r) any_alpha |= alph[r] != 1.f;
+        if (any_alpha) {
+#pragma unroll
+          for (int r = 0; r < RK; ++r) lsum[r] *= alph[r];
+        }
         if (have[g] && any_alpha) {
-          // O^T and l^T hold this piece's earlier PVs: scale them (thread gt =
-          // dimension gt; every lane of l^T holds the same sums)
+          // O^T holds this piece's earlier PVs: scale it (thread gt = dimension gt)
           ok = ok && mbar_wait(&t.o_done[g], (c - 1) & 1u, a.status, s.abort);
           if (ok) {
             tc_fence_after();
             tmem_scale32(tm.o(g) + lane_off, alph);
-            tmem_scale32(tm.l(g) + lane_off, alph);
             tc_fence_before();
           }
         }
@@ -716,6 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p1 = sc[r + 1] > -INFINITY ? fast_exp2(sc[r + 1] - m4.y) : 0.f;
         const float p2 = sc[r + 2] > -INFINITY ? fast_exp2(sc[r + 2] - m4.z) : 0.f;
         const float p3 = sc[r + 3] > -INFINITY ? fast_exp2(sc[r + 3] - m4.w) : 0.f;
+        lsum[r] += p0;
+        lsum[r + 1] += p1;
+        lsum[r + 2] += p2;
+        lsum[r + 3] += p3;
         pw[r / 2] = pack_bf16(p0, p1);
         pw[r / 2 + 1] = pack_bf16(p2, p3);
       }
@@ -748,6 +745,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     ns[g] = c + 1;
     if (last) {
       // ---- end of the piece: merge the two groups' states ----
+      // The group's row sums first (their 32 registers are free before the
+      // group's O^T is read): a reduce-scatter leaves lane r of each warp with
+      // row r's sum over the warp's keys, which goes to the group's own part
+      // of red (the other group may still use its part for a raise in its
+      // last step); thread r of the group adds the four warps' after the
+      // barrier below.
+      float* const lred = t.red + grp * 4 * RK;
+      static_assert(RK == 32, "one row per lane");
+#pragma unroll
+      for (int h = 16; h >= 1; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+          const float send = upper ? lsum[i] : lsum[i + h];
+          const float keep = upper ? lsum[i + h] : lsum[i];
+          lsum[i] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+      }
       bool mine = have[grp];
       float oo[RK];
       if (mine) {
@@ -761,26 +776,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < RK; ++r) oo[r] = ok ? __uint_as_float(o[r]) : 0.f;
         mine = ok;
       }
-      // the group's row sums: every lane of l^T holds them; the group's
-      // thread 0 (lane 0 of its first warp) publishes them into the group's
-      // own part of red (the other group may still use its part for a raise
-      // in its last step)
-      float* const lred = t.red + grp * 4 * RK;
-      if ((warp & 3) == 0 && mine) {   // a whole warp: tcgen05.ld is warp-wide
-        uint32_t lw[RK];
-        tmem_ld32(tm.l(grp) + lane_off, lw);
-        if (lane == 0) {
-#pragma unroll
-          for (int r = 0; r < RK; ++r) lred[r] = __uint_as_float(lw[r]);
-        }
-      }
-      if (gt < RK && !mine) lred[gt] = 0.f;
+      lred[(warp & 3) * RK + lane] = mine ? lsum[0] : 0.f;
       if (gt < RK && !mine) mref[gt] = -INFINITY;
       // group A's o for the merge goes to the P^T region ([row][dim]): every
       // PV of the piece has completed, so the region is free
       float* mob = reinterpret_cast<float*>(t.pt);
       tc_fence_before();
       named_barrier(1, NCT);
+      if (gt < RK) lred[gt] += lred[RK + gt] + lred[2 * RK + gt] + lred[3 * RK + gt];
       if (grp == 0) {
 #pragma unroll
         for (int r = 0; r < RK; ++r) mob[r * D + gt] = oo[r];
