@@ -785,12 +785,24 @@ def profiled_traffic():
         return None
 
 
+# The files decode_kernel (the CUDA-core, mma.sync and cluster engines) and its
+# launch are built from; the tcgen05 kernel, the append kernel and the static
+# entry point live elsewhere and do not change its code.
+DECODE_KERNEL_SOURCES = ("draft_attention_decode_b300/csrc/common.cuh",
+                         "draft_attention_decode_b300/csrc/pipeline.cuh",
+                         "draft_attention_decode_b300/csrc/decode.cuh",
+                         "draft_attention_decode_b300/csrc/decode.cu",
+                         "draft_attention_decode_b300/csrc/api.cu",
+                         "draft_attention_decode_b300/csrc/internal.h",
+                         "include/draft_attn.h")
+
+
 def sources_sha():
+    """Hash of the sources the headline decode_kernel is compiled from."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "draft_attention_decode_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
+    for f in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
