@@ -540,27 +540,33 @@ struct CoreEngine {
 #pragma unroll
     for (int m = RK == 4 ? RK : LPK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
     if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
+    // The four key groups' partial outputs, reduce-scattered over lane bits
+    // 4 and 3: the lane's RK (D / 8) values, as float2 slots f = r (DQ / 2) + e,
+    // halve twice, and key group kg is left with the totals of the quarter
+    // of slots from kg (NV / 4) on, which it writes.
+    constexpr int NV = RK * (DQ / 2);
+    static_assert(NV % 4 == 0, "quarters");
+    float2* const v = &o2[0][0];
+    const bool b1 = (kg & 2) != 0, b0 = (kg & 1) != 0;
 #pragma unroll
-    for (int r = 0; r < RK; ++r)
+    for (int i = 0; i < NV / 2; ++i) {
+      const float2 send = b1 ? v[i] : v[i + NV / 2];
+      const float2 keep = b1 ? v[i + NV / 2] : v[i];
+      v[i] = make_float2(keep.x + __shfl_xor_sync(0xffffffffu, send.x, 16),
+                         keep.y + __shfl_xor_sync(0xffffffffu, send.y, 16));
+    }
 #pragma unroll
-      for (int e = 0; e < DQ / 2; ++e) {
-        float2 v = o2[r][e];
+    for (int i = 0; i < NV / 4; ++i) {
+      const float2 send = b0 ? v[i] : v[i + NV / 4];
+      const float2 keep = b0 ? v[i + NV / 4] : v[i];
+      v[i] = make_float2(keep.x + __shfl_xor_sync(0xffffffffu, send.x, 8),
+                         keep.y + __shfl_xor_sync(0xffffffffu, send.y, 8));
+    }
 #pragma unroll
-        for (int m = LPK; m < 32; m <<= 1) {
-          v.x += __shfl_xor_sync(0xffffffffu, v.x, m);
-          v.y += __shfl_xor_sync(0xffffffffu, v.y, m);
-        }
-        o2[r][e] = v;
-      }
-    if (kg == 0) {
-#pragma unroll
-      for (int i = 0; i < NCH; ++i)
-#pragma unroll
-        for (int r = 0; r < RK; ++r)
-#pragma unroll
-          for (int e = 0; e < EPC / 2; ++e)
-            *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + dim_of(i, 2 * e)) =
-                o2[r][i * (EPC / 2) + e];
+    for (int i = 0; i < NV / 4; ++i) {
+      const int f = kg * (NV / 4) + i;
+      const int r = f / (DQ / 2), e = f % (DQ / 2);
+      *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + dim_of(e / (EPC / 2), 2 * (e % (EPC / 2)))) = v[i];
     }
     named_barrier(1, NCT);
     for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
