@@ -446,6 +446,18 @@ __device__ __forceinline__ T* dsmem_ptr(T* local, uint32_t rank) {
   asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
   return reinterpret_cast<T*>(r);
 }
+// Asynchronous stores into (possibly another cluster CTA's) shared memory at
+// shared::cluster address `addr`; each completes `bar` (a shared::cluster
+// mbarrier address in the same CTA as `addr`) with its byte count, which
+// makes the data visible to a thread that sees the barrier's phase complete.
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1,%2,%3,%4}, [%5];"
+               ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+               ::"r"(addr), "f"(v), "r"(bar) : "memory");
+}
 // Arrive on the mbarrier at `local`'s place in CTA `rank`, releasing this
 // thread's earlier writes (its distributed-shared-memory stores included) to
 // the cluster.

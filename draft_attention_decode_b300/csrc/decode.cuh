@@ -259,6 +259,27 @@ __device__ __forceinline__ void load_slice(uint32_t addr, float (&f)[DPL]) {
 // unswizzled 64-byte row, four consecutive keys filling 256 contiguous bytes),
 // and the piece's queries are laid out in that order (begin_far).
 // ---------------------------------------------------------------------------
+// Where a piece's partial (m[RK], l[RK], pad, o[RK][D], as floats) goes: plain
+// stores through `p` (the workspace), or, on the cluster partition,
+// asynchronous stores into rank 0's slot (shared::cluster address `sa`), each
+// counted on rank 0's merge barrier (`bar`).  Offsets are in floats.
+struct PartOut {
+  float* p;
+  uint32_t sa, bar;
+  __device__ __forceinline__ void put4(int off, float4 v) const {
+    if (bar) st_async_f32x4(sa + 4u * (uint32_t)off, v, bar);
+    else *reinterpret_cast<float4*>(p + off) = v;
+  }
+  __device__ __forceinline__ void put1(int off, float v) const {
+    if (bar) st_async_f32(sa + 4u * (uint32_t)off, v, bar);
+    else p[off] = v;
+  }
+};
+// Bytes a partial of RK rows sends to rank 0 (m, l and o; not the pad).
+__host__ __device__ constexpr uint32_t part_bytes(int rk, int d) {
+  return (uint32_t)(2 * rk + rk * d) * 4u;
+}
+
 template <typename T, int D, int RK, bool PINGPONG, bool F8 = false>
 struct CoreEngine {
   static constexpr int NCW = kConsumerWarps;
@@ -534,7 +555,7 @@ struct CoreEngine {
 
   // Sum the key groups, merge the consumer warps, write the piece's partial.
   // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
-  __device__ __forceinline__ void finish(const Smem& s, float* part) {
+  __device__ __forceinline__ void finish(const Smem& s, const PartOut& part) {
     float lt = l_run;
     // with 4 rows lanes ds and ds ^ 4 hold one row's sums over different keys
 #pragma unroll
@@ -569,25 +590,30 @@ struct CoreEngine {
       *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + dim_of(e / (EPC / 2), 2 * (e % (EPC / 2)))) = v[i];
     }
     named_barrier(1, NCT);
-    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
-      const int r = idx / D, dim = idx - r * D;
+    for (int idx = threadIdx.x; idx < RK * D / 4; idx += NCT) {
+      const int r = idx / (D / 4), d4 = idx - r * (D / 4);
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
-      float o = 0.f, l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NCW; ++w) {
           const float2 ml = s.ml[w * RK + r];
           const float sc = fast_exp2(ml.x - M);
-          o += sc * s.mo[(w * RK + r) * D + dim];
-          l += sc * ml.y;
+          const float4 v = *reinterpret_cast<const float4*>(s.mo + (w * RK + r) * D + 4 * d4);
+          o.x = fmaf(sc, v.x, o.x);
+          o.y = fmaf(sc, v.y, o.y);
+          o.z = fmaf(sc, v.z, o.z);
+          o.w = fmaf(sc, v.w, o.w);
+          l = fmaf(sc, ml.y, l);
         }
       }
-      part[slot_o_off(RK) + r * D + dim] = o;
-      if (dim == 0) {
-        part[r] = M;
-        part[RK + r] = l;
+      part.put4(slot_o_off(RK) + r * D + 4 * d4, o);
+      if (d4 == 0) {
+        part.put1(r, M);
+        part.put1(RK + r, l);
       }
     }
     named_barrier(1, NCT);
@@ -752,7 +778,7 @@ struct CoreEngineWide {
 
   // Merge the eight warps' states and write the piece's partial to `slot`.
   // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
-  __device__ __forceinline__ void finish(const Smem& s, float* part) {
+  __device__ __forceinline__ void finish(const Smem& s, const PartOut& part) {
     float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
     lt += __shfl_xor_sync(0xffffffffu, lt, 16);
     if (kg == 0 && ds < RK) s.ml[warp * RK + ds] = make_float2(m_run, lt);
@@ -762,25 +788,30 @@ struct CoreEngineWide {
       for (int e = 0; e < DPL / 2; ++e)
         *reinterpret_cast<float2*>(s.mo + (warp * RK + r) * D + lane * DPL + 2 * e) = o2[r][e];
     named_barrier(1, NCT);
-    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
-      const int r = idx / D, dim = idx - r * D;
+    for (int idx = threadIdx.x; idx < RK * D / 4; idx += NCT) {
+      const int r = idx / (D / 4), d4 = idx - r * (D / 4);
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, s.ml[w * RK + r].x);
-      float o = 0.f, l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NCW; ++w) {
           const float2 ml = s.ml[w * RK + r];
           const float sc = fast_exp2(ml.x - M);
-          o += sc * s.mo[(w * RK + r) * D + dim];
-          l += sc * ml.y;
+          const float4 v = *reinterpret_cast<const float4*>(s.mo + (w * RK + r) * D + 4 * d4);
+          o.x = fmaf(sc, v.x, o.x);
+          o.y = fmaf(sc, v.y, o.y);
+          o.z = fmaf(sc, v.z, o.z);
+          o.w = fmaf(sc, v.w, o.w);
+          l = fmaf(sc, ml.y, l);
         }
       }
-      part[slot_o_off(RK) + r * D + dim] = o;
-      if (dim == 0) {
-        part[r] = M;
-        part[RK + r] = l;
+      part.put4(slot_o_off(RK) + r * D + 4 * d4, o);
+      if (d4 == 0) {
+        part.put1(r, M);
+        part.put1(RK + r, l);
       }
     }
     named_barrier(1, NCT);
@@ -1053,7 +1084,7 @@ struct MmaEngine {
 
   // Merge the warps holding each row and write the piece's partial to `slot`.
   // part: where the piece's partial (m[RK], l[RK], pad, o[RK][D]) goes (global or shared).
-  __device__ __forceinline__ void finish(const Smem& s, float* part) {
+  __device__ __forceinline__ void finish(const Smem& s, const PartOut& part) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1077,28 +1108,33 @@ struct MmaEngine {
       }
     named_barrier(1, NCT);
     constexpr int NW = SPLIT_PAGES ? 8 : 4;   // warps holding one row
-    for (int idx = threadIdx.x; idx < RK * D; idx += NCT) {
-      const int r = idx / D, dim = idx - r * D;
+    for (int idx = threadIdx.x; idx < RK * D / 4; idx += NCT) {
+      const int r = idx / (D / 4), d4 = idx - r * (D / 4);
       const int w0 = SPLIT_PAGES ? 0 : (r / RW) * 4;
       const int lr = SPLIT_PAGES ? r : r % RW;
       float M = -INFINITY;
 #pragma unroll
       for (int k = 0; k < NW; ++k) M = fmaxf(M, s.ml[(w0 + k) * 16 + lr].x);
-      float o = 0.f, lsum = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int k = 0; k < NW; ++k) {
           const int w = w0 + k;
           const float2 ml = s.ml[w * 16 + lr];
           const float sc = fast_exp2(ml.x - M);
-          o += sc * s.mo[(w * 16 + lr) * D + dim];
-          lsum += sc * ml.y;
+          const float4 v = *reinterpret_cast<const float4*>(s.mo + (w * 16 + lr) * D + 4 * d4);
+          o.x = fmaf(sc, v.x, o.x);
+          o.y = fmaf(sc, v.y, o.y);
+          o.z = fmaf(sc, v.z, o.z);
+          o.w = fmaf(sc, v.w, o.w);
+          lsum = fmaf(sc, ml.y, lsum);
         }
       }
-      part[slot_o_off(RK) + r * D + dim] = o;
-      if (dim == 0) {
-        part[r] = M;
-        part[RK + r] = lsum;
+      part.put4(slot_o_off(RK) + r * D + 4 * d4, o);
+      if (d4 == 0) {
+        part.put1(r, M);
+        part.put1(RK + r, lsum);
       }
     }
     named_barrier(1, NCT);
@@ -1624,10 +1660,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.tables_ready && !a.inputs_ready) grid_dep_wait();
   if constexpr (!CLUSTER) zero_empty<T, D, NCT>(a, s);
   // cluster partition: this CTA's partial goes straight to its slot in rank
-  // 0's shared memory
-  float* const dst_part =
-      CLUSTER ? dsmem_ptr(s.recv + (size_t)cr * slot_floats(RK, D), 0u) : nullptr;
-  bool wrote = false;
+  // 0's shared memory, by asynchronous stores counted on rank 0's merge
+  // barrier (rank 0 itself stores its own slot directly)
+  PartOut cpart{nullptr, 0u, 0u};
+  if constexpr (CLUSTER) {
+    float* const own = s.recv + (size_t)cr * slot_floats(RK, D);
+    if (cr == 0) {
+      cpart.p = own;
+    } else {
+      cpart.sa = dsmem_addr(smem_u32(own), 0u);
+      cpart.bar = dsmem_addr(smem_u32(s.merge_bar), 0u);
+    }
+  }
+  bool wrote = false, cwaited = false;
   // A fused draft step: the new tokens' rotated keys and values, for pages
   // that hold them (patched into the staged copy before they are read).
   if constexpr (CLUSTER) {
@@ -1724,10 +1769,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++unit;
     if (last) {
       if constexpr (CLUSTER) {
-        eng.finish(s, dst_part);   // the CTA's one piece
+        // rank 0 initialised its merge barrier before its cluster arrival
+        cluster_wait();
+        cwaited = true;
+        eng.finish(s, cpart);   // the CTA's one piece
         wrote = true;
       } else {
-        eng.finish(s, a.part + ((int64_t)blockIdx.x + inf.seq) * slot_floats(RK, D));
+        eng.finish(s, PartOut{a.part + ((int64_t)blockIdx.x + inf.seq) * slot_floats(RK, D), 0u, 0u});
         ticket<T, D, RK, NCT>(a, s, inf.seq, pages);
       }
       pages = 0;
@@ -1737,23 +1785,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // land first when a wait gave up).
   named_barrier_arrive(kEndBarrier, NCT + 32);
   if constexpr (CLUSTER) {
-    // A CTA with no pages (a selection shorter than the cluster) or one whose
-    // wait gave up contributes an empty partial.
-    if (!wrote || *s.abort) {
+    if (!cwaited) cluster_wait();
+    // A CTA with no pages (a selection shorter than the cluster) or whose wait
+    // gave up before its piece's end sends an empty partial, so that every
+    // CTA but rank 0 sends part_bytes to rank 0's barrier.
+    if (!wrote) {
+      for (int i = threadIdx.x; i < RK * D / 4; i += NCT)
+        cpart.put4(slot_o_off(RK) + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
       for (int r = threadIdx.x; r < RK; r += NCT) {
-        dst_part[r] = -INFINITY;
-        dst_part[RK + r] = 0.f;
+        cpart.put1(r, -INFINITY);
+        cpart.put1(RK + r, 0.f);
       }
     }
-    // Every consumer thread releases its stores into rank 0's slot and
-    // arrives on rank 0's merge barrier; rank 0 merges once all have arrived
-    // (the other CTAs are done: nothing reads their shared memory).  The
-    // cluster wait (every CTA arrived at its start) precedes the arrival.
-    __syncwarp();
-    cluster_wait();
-    mbar_arrive_remote(s.merge_bar, 0u);
-    if (cr == 0 && mbar_wait_cluster(s.merge_bar, 0u, a.status, s.abort))
-      recv_merge<T, D, RK, NCT>(a, s, cb, ch);
+    // Rank 0 expects the other CTAs' bytes on its merge barrier (a single
+    // arrival) and merges once they have landed and its own consumers have
+    // written its slot.  The other CTAs are done: nothing reads their shared
+    // memory, and their stores carry registers, not shared memory.
+    if (cr == 0) {
+      if (threadIdx.x == 0) mbar_arrive_expect_tx(s.merge_bar, (cluster_size() - 1) * part_bytes(RK, D));
+      named_barrier(1, NCT);
+      if (mbar_wait_cluster(s.merge_bar, 0u, a.status, s.abort)) recv_merge<T, D, RK, NCT>(a, s, cb, ch);
+    }
   }
 }
 

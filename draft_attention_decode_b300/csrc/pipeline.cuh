@@ -452,8 +452,8 @@ __device__ inline void producer_head(const DecodeArgs& a, Smem& s, const Layout&
 }
 
 // Cluster partition start: barriers (the stage ring, and the merge barrier
-// that rank 0's consumers wait on: every consumer thread of every CTA of the
-// cluster arrives once), the angle table, flags; a CTA barrier; and the
+// that rank 0's consumers wait on: rank 0 arrives once, expecting the bytes
+// the other CTAs' partials bring), the angle table, flags; a CTA barrier; and the
 // arrival half of a cluster barrier, whose wait (cluster_wait, before a CTA
 // first touches rank 0's shared memory) guarantees that rank 0 initialised
 // its merge barrier.  Every thread of the CTA arrives here; only the
@@ -470,7 +470,7 @@ __device__ inline void cluster_start(const DecodeArgs& a, Smem& s, const Layout&
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], NCW);
     }
-    mbar_init(s.merge_bar, L.recv_slots * kConsumerThreads);
+    mbar_init(s.merge_bar, 1);   // rank 0's expect-tx arrival; the other CTAs' bytes complete it
     fence_barrier_init();
   }
   __syncthreads();
