@@ -157,6 +157,14 @@ def test_cluster_automatic_choice():
     assert info(num_ctas=64)["cluster_ctas"] == 0
     assert info(cluster_ctas=-1)["cluster_ctas"] == 0
     assert info(cluster_ctas=3)["cluster_ctas"] == 3
+    # The fewest CTAs for the longest stretch: one CTA fewer would lengthen it
+    # (a window of W keys plus sinks spans at most ceil(W / 64) + 1 pages, and
+    # one more for the sinks).
+    for w, ns in ((2048, 0), (4096, 4), (1000, 0)):
+        c = info(window=w, n_sink=ns)["cluster_ctas"]
+        pmax = (1 if ns else 0) + -(-w // 64) + 1
+        longest = -(-pmax // c)
+        assert c == 1 or -(-pmax // (c - 1)) > longest, (w, ns, c)
 
 
 def test_cluster_long_window_sampled():
