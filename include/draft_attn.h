@@ -170,8 +170,10 @@ typedef struct {
                                 work.  0 = automatic: when num_ctas and
                                 min_pages_per_cta are 0 and one cluster per
                                 (sequence, KV head) fits on the GPU at once, the
-                                cluster partition (below) with as many CTAs per
-                                cluster (up to 16) as fit, else the flat one;
+                                cluster partition (below): the largest size (up
+                                to 16) at which every cluster is resident, cut to
+                                the fewest CTAs that keep the most pages any CTA
+                                scans the same; else the flat one;
                                 -1 = always the flat partition (persistent CTAs
                                 take equal stretches of every head's pages and
                                 the last CTA of each head merges through the
