@@ -997,7 +997,8 @@ def profile_loop(args):
         wl = WL.resized(wl, args.ctx)
     if args.ctx_cap:
         wl = WL.resized(wl, [min(c, args.ctx_cap) for c in wl.ctx])
-    dl = DraftLoop(wl, dev, (args.profile_loop,), engine=args.engine)
+    dl = DraftLoop(wl, dev, (args.profile_loop,), engine=args.engine,
+                   cluster_ctas=args.cluster_ctas)
     torch.cuda.synchronize()
     if args.side_fp8:
         # FOLD with the side cache as E4M3 codes: the attention call on the first
@@ -1059,6 +1060,8 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--engine", default="auto", choices=("auto", "cuda_core", "mma", "tc05"),
                     help="with --profile-loop: force this engine")
+    ap.add_argument("--cluster-ctas", type=int, default=0,
+                    help="with --profile-loop window: CTAs per cluster (-1: the flat partition)")
     ap.add_argument("--side-fp8", action="store_true",
                     help="with --profile-loop fold: the attention call over an E4M3 side cache")
     args = ap.parse_args()
