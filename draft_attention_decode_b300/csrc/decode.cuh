@@ -1571,10 +1571,10 @@ __device__ inline void zero_empty(const DecodeArgs& a, const Smem& s) {
 //  * cluster (CLUSTER true; one-segment modes whose selection is short, such
 //    as window mode): one thread-block cluster of a.cluster CTAs per
 //    (sequence, KV head).  CTA r of the cluster takes an equal r-th share of
-//    that head's pages (one piece), leaves its partial in its own shared
-//    memory, and after a cluster barrier the CTAs merge the partials through
-//    distributed shared memory and write the output: no workspace round trip,
-//    no ticket, and no CTA merges alone at the end.
+//    that head's pages (one piece) and sends its partial into slot r of rank
+//    0's shared memory by asynchronous stores that complete rank 0's merge
+//    barrier by their byte count; rank 0 merges the slots and writes the
+//    output: no workspace round trip and no ticket.
 template <typename T, int D, class Engine, int VARIANT, int RK, bool CLUSTER = false>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap mk,
