@@ -64,3 +64,20 @@ def test_reference_arm_prints_on_rank0_only(tmp_path):
     line = json.loads(outs[0].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_record_follows_the_kernel_sources(monkeypatch):
+    """roofline.traffic comes from the committed ncu record only while the
+    headline kernel's sources hash to the value the record was taken on; the
+    record's bytes are those of one 128K full-mode call (K and V of 131,075
+    keys over 8 KV heads, plus the partials and the output written)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for f in bench.DECODE_KERNEL_SOURCES:
+        assert os.path.exists(os.path.join(ROOT, f)), f
+    assert bench.sources_sha() == bench.sources_sha()
+    t = bench.profiled_traffic()
+    algorithmic = 131075 * 8 * 2 * 128 * 2
+    assert t is None or algorithmic <= t <= 1.02 * algorithmic
+    monkeypatch.setattr(bench, "sources_sha", lambda: "0" * 16)
+    assert bench.profiled_traffic() is None
