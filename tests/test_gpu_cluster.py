@@ -31,7 +31,7 @@ def _same(a, b):
 SHAPES = [(8, 8, 1), (32, 8, 1), (64, 8, 1), (32, 8, 4), (32, 8, 8)]
 
 
-@pytest.mark.parametrize("cluster", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("cluster", [1, 2, 3, 5, 8, 9, 10, 16])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "h%d_%d_q%d" % s)
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp32", 128)])
 def test_cluster_parity(cluster, shape, dtype, d):
