@@ -120,6 +120,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "draft_attn_debug_gather": (ctypes.c_int, [VP, VP, VP, VP, VP, I32, I32, VP, VP, VP, VP, VP,
                                                    I64, VP, VP]),
         "draft_attn_get_status": (ctypes.c_int, [VP, VP, P(ctypes.c_uint32)]),
+        "draft_attn_debug_wait_timeout": (ctypes.c_int, [VP, VP]),
         "draft_attn_ring_size": (ctypes.c_int, [I32, I32, P(I32), P(I32)]),
         "draft_attn_ring_block_table": (ctypes.c_int, [P(I32), I64, P(I32), I32, I32]),
         "draft_attn_error_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -348,6 +349,12 @@ def draft_attn_ring_block_table(max_pages, ring_pages, n_sink_pages):
         table.ctypes.data_as(I32p), int(max_pages), ring.ctypes.data_as(I32p), int(ring.size),
         int(n_sink_pages)), "draft_attn_ring_block_table")
     return table
+
+
+def draft_attn_debug_wait_timeout(plan, stream=None):
+    """Launches the bounded-wait give-up hook (about a second on the device)."""
+    _check(load_library().draft_attn_debug_wait_timeout(plan, _stream(stream)),
+           "draft_attn_debug_wait_timeout")
 
 
 def draft_attn_get_status(plan, stream=None):

@@ -550,6 +550,15 @@ int draft_attn_ring_block_table(int32_t* table, int64_t max_pages, const int32_t
   return DA_OK;
 }
 
+int draft_attn_debug_wait_timeout(da_plan_t pl, void* stream) {
+  if (!pl) return DA_ERR_INVALID_ARG;
+  DeviceGuard g(pl->device);
+  if (!g.ok) return DA_ERR_CUDA;
+  return da::launch_wait_timeout(pl->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_CUDA;
+}
+
 int draft_attn_get_status(da_plan_t pl, void* stream, uint32_t* bits) {
   if (!pl) return DA_ERR_INVALID_ARG;
   DeviceGuard g(pl->device);

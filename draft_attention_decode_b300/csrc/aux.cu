@@ -167,4 +167,25 @@ cudaError_t launch_gather(const DecodeArgs& a, int b, int t, const GatherOut& o,
   return cudaGetLastError();
 }
 
+// The give-up path of the kernels' bounded wait: one warp waits, with the
+// same mbar_wait, on an mbarrier that nothing ever arrives on.  After about
+// 2^31 cycles the first thread to give up sets DA_STATUS_WAIT_TIMEOUT in the
+// status word and raises the abort flag; the others then return at once.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0u, status, &abort_flag);
+}
+
+cudaError_t launch_wait_timeout(uint32_t* status, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 }  // namespace da

@@ -105,5 +105,6 @@ struct GatherOut {
   int64_t* count;
 };
 cudaError_t launch_gather(const DecodeArgs& a, int b, int t, const GatherOut& o, cudaStream_t st);
+cudaError_t launch_wait_timeout(uint32_t* status, cudaStream_t st);
 
 }  // namespace da

@@ -363,6 +363,15 @@ int draft_attn_debug_gather(da_plan_t plan, const int32_t* q_pos, const int32_t*
                             int32_t* q_rope_pos, int8_t* segment, int64_t capacity,
                             int64_t* count, void* stream);
 
+/* Test hook for the kernels' bounded waits: launches, on `stream`, one warp
+ * that waits on an mbarrier nothing ever completes, with the same bounded wait
+ * the attention kernels use.  After about 2^31 cycles (about a second) the
+ * wait gives up and sets DA_STATUS_WAIT_TIMEOUT in the plan device's status
+ * word, read with draft_attn_get_status; nothing faults and the context stays
+ * usable.  Returns DA_ERR_INVALID_ARG for a NULL plan, DA_ERR_CUDA when the
+ * launch fails. */
+int draft_attn_debug_wait_timeout(da_plan_t plan, void* stream);
+
 /* Synchronises `stream`, reads and clears the plan device's status word.
  * Returns DA_OK when it was zero, DA_ERR_DEVICE_FAULT otherwise; *bits (host
  * pointer, may be NULL) receives the DA_STATUS_* bits. */

@@ -359,6 +359,23 @@ def test_context_beyond_block_table_sets_status():
     s.close()
 
 
+def test_bounded_wait_gives_up_and_reports():
+    """A wait that nothing completes gives up after about a second, sets the
+    timeout bit in the status word, and leaves the context usable: a normal
+    call after it matches the oracle and reports nothing."""
+    s = Setup(batch=1, n_q=1, num_q_heads=8, num_kv_heads=2, head_dim=64, dtype="bf16",
+              ctx=[640], mode="full")
+    assert s.status() == (B.DA_OK, 0)
+    B.draft_attn_debug_wait_timeout(s.da.plan)
+    code, bits = s.status()
+    assert code == B.DA_ERR_DEVICE_FAULT and bits == B.DA_STATUS_WAIT_TIMEOUT
+    assert s.status() == (B.DA_OK, 0)          # read-and-clear
+    out = s.run()
+    compare(out, s.oracle(), "bf16", "after a wait gave up")
+    assert s.status() == (B.DA_OK, 0)
+    s.close()
+
+
 def test_workspace_too_small_rejected():
     s = Setup(batch=1, n_q=1, num_q_heads=8, num_kv_heads=2, head_dim=64, dtype="bf16",
               ctx=[64], mode="full")
